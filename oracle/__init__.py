@@ -1,0 +1,9 @@
+"""Oracle of the routed + shared-expert MoE layer forward (test infrastructure).
+
+A plain, slow, float64 CPU statement of the layer, written from the pages that
+define the method.  Only the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU baseline / reference arm use it.  It shares no code with the
+CUDA library, and the library never calls it.
+"""
+from .moe_oracle import *  # noqa: F401,F403
+from . import moe_oracle  # noqa: F401
