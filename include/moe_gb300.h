@@ -1,0 +1,221 @@
+/*
+ * moe_gb300.h - C ABI of the routed + shared-expert MoE layer forward on one GB300 (sm_103a).
+ *
+ * The layer (Section 21 "Merging Routed and Shared Expert Activations", Eq. 80):
+ *
+ *     y(x) = sum_{i in S(x)} r_i(x) f_i(x) + s(x) g(x),        |S(x)| = K,
+ *
+ * with f_i the SwiGLU routed experts and g the shared SwiGLU expert (Section 20
+ * "One Shared Expert Is All You Need", Eq. 74), the router, the scores, the
+ * selection and the coefficient rules of Appendix E "Expert-Merge Normalization
+ * in Public MoE Models" (Table 52), and the requested / kept counts, capacity
+ * policies and packed per-expert segments of Section 10 "Routing, Capacity, and
+ * Load Balancing" (Eq. 19-27).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named in the argument lists are DEVICE pointers unless marked
+ *   "host".  The caller owns every buffer; the library allocates nothing and
+ *   frees nothing.  Scratch memory comes from a caller-provided workspace of
+ *   at least moe_workspace_size() bytes, 256-byte aligned.
+ * - Tensors are dense row-major.  Element type of activations and weights is
+ *   cfg->dtype (fp32 or bf16).  Router logits, coefficients, the shared
+ *   coefficient and y are fp32.  Indices and counts are int32.
+ * - Weight storage: W_router [N][d] (one row per expert, z = x W_router^T);
+ *   W_gate, W_up [N][d_expert][d] (one row per intermediate unit, the columns
+ *   of W_g / W_u of Eq. 74); W_down [N][d][d_expert] (one row per output
+ *   dimension, the columns of W_d); shared Ws_gate, Ws_up [d_shared][d],
+ *   Ws_down [d][d_shared].
+ * - All work is enqueued on the given stream.  No entry point synchronises
+ *   the host with the device or copies device data to the host, except
+ *   moe_read_status() which says so.  Arguments are validated on the host
+ *   before anything is enqueued; an invalid call returns an error status and
+ *   enqueues nothing.  A launch failure returns MOE_ERR_CUDA.
+ * - Kernels never trap.  Anything a kernel detects (a bounded wait that ran
+ *   out, an index out of range) is written to a status word inside the
+ *   workspace; moe_read_status() returns and clears it.
+ * - Thread safety: calls on different streams must use different workspaces.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,        /* a null pointer, a size out of range, an unknown enum */
+  MOE_ERR_UNSUPPORTED = -2,        /* valid layer, but a shape this build has no kernel for */
+  MOE_ERR_CUDA = -3,               /* a CUDA runtime call or launch failed */
+  MOE_ERR_WORKSPACE_TOO_SMALL = -4,
+  MOE_ERR_TIMEOUT = -5,            /* device status: a bounded wait inside a kernel ran out */
+  MOE_ERR_DEVICE_BOUNDS = -6,      /* device status: a kernel saw an index out of range */
+  MOE_ERR_MISALIGNED = -7          /* a pointer is not 16-byte aligned */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Router score (Appendix E, Table 52): softmax over all N experts, or sigmoid affinities. */
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score;
+
+/* Selected-weight rule (Appendix E, Table 52):
+ *   NONE              w = q_S (routed mass m_K < 1 for a softmax over N > K)
+ *   L1_SELECTED       w = q_S / sum_S q (Section 21.1; the Olmo and DeepSeek-V3 rows)
+ *   SOFTMAX_SELECTED  w = softmax(z_S), the softmax over the selected logits (Mixtral row)
+ * The routed coefficients are r = alpha * w. */
+typedef enum { MOE_NORM_NONE = 0, MOE_NORM_L1_SELECTED = 1, MOE_NORM_SOFTMAX_SELECTED = 2 } moe_norm;
+
+/* Shared coefficient s(x) of Eq. 80: none (0), a constant gain, or sigmoid(w_s . x) (Eq. 77). */
+typedef enum { MOE_SHARED_NONE = 0, MOE_SHARED_CONST = 1, MOE_SHARED_SIGMOID_GATE = 2 } moe_shared_mode;
+
+/* Capacity (Section 10.3): none; per expert b = max(1, ceil(c K T / N)) (Eq. 25);
+ * rank-wide B = max(1, ceil(c K T / M_E)) shared by the experts rho maps to one rank (Eq. 23),
+ * admitted in ascending local expert order.  Kept routes of an expert are its first
+ * requests in token order. */
+typedef enum { MOE_CAP_NONE = 0, MOE_CAP_PER_EXPERT = 1, MOE_CAP_RANK_WIDE = 2 } moe_cap_policy;
+
+typedef struct moe_config {
+  int64_t T;              /* tokens in the batch, >= 0 */
+  int32_t d_model;        /* d */
+  int32_t N;              /* routed experts, 1..256 */
+  int32_t K;              /* selected per token, 1..min(N, 8) */
+  int32_t d_expert;       /* routed intermediate width d_r */
+  int32_t d_shared;       /* shared intermediate width d_s, 0 = no shared expert */
+  int32_t dtype;          /* moe_dtype */
+  int32_t score;          /* moe_score */
+  int32_t norm;           /* moe_norm */
+  float alpha;            /* routed scale, finite */
+  int32_t shared_mode;    /* moe_shared_mode */
+  float shared_gain;      /* s for MOE_SHARED_CONST */
+  int32_t cap_policy;     /* moe_cap_policy */
+  double capacity_factor; /* c > 0 when a capacity policy is set */
+  int32_t num_ranks;      /* M_E >= 1: destination ranks of rho (Eq. 20) */
+  const int32_t* rho;     /* HOST [N], values in [0, num_ranks); NULL means rho(i) = i mod num_ranks */
+} moe_config;
+
+/* Weights of one layer (device pointers, layouts above).  router_bias [N] fp32 and
+ * shared_gate_w [d] may be NULL; shared weights are ignored when d_shared == 0. */
+typedef struct moe_weights {
+  const void* W_router;
+  const float* router_bias;
+  const void* shared_gate_w;
+  const void* W_gate;
+  const void* W_up;
+  const void* W_down;
+  const void* Ws_gate;
+  const void* Ws_up;
+  const void* Ws_down;
+} moe_weights;
+
+/* Outputs of moe_layer_forward (device pointers).  y is required when T > 0; every
+ * other pointer may be NULL, in which case that result is kept in the workspace. */
+typedef struct moe_outputs {
+  float* y;               /* [T][d] fp32 */
+  int32_t* topk_idx;      /* [T][K] selected experts, slot order = descending key, lower index on ties */
+  float* topk_w;          /* [T][K] r = alpha * w */
+  float* shared_coef;     /* [T]    s(x) */
+  float* logits;          /* [T][N] router logits z (+ bias) as used for selection */
+  int32_t* counts_req;    /* [N]    C^req (Eq. 19) */
+  int32_t* counts_keep;   /* [N]    C^keep (Eq. 21) */
+  int32_t* offsets;       /* [N+1]  o_e = sum_{i<e} C_i^keep (Eq. 26, exclusive form) */
+  int32_t* route_pos;     /* [T][K] packed row of each route, -1 if dropped */
+  int32_t* perm_src;      /* [K*T]  token of each packed row; rows >= offsets[N] are unspecified */
+  int32_t* R_req;         /* [num_ranks] destination totals (Eq. 20) */
+  int32_t* R_keep;        /* [num_ranks] (Eq. 21) */
+  int32_t* drop_stats;    /* [4] dropped routes, tokens losing >= 1 route, tokens losing all K, 0 */
+} moe_outputs;
+
+/* Library version string (host). */
+const char* moe_version(void);
+
+/* Human-readable name of a status code (host). */
+const char* moe_status_string(int32_t status);
+
+/* Workspace bytes needed by every entry point for this layer (host only, no CUDA call).
+ * Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a layer the library cannot run. */
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Router, scores, top-K and coefficients for every token (Section 10, Table 16 first row;
+ * Appendix E, Table 52; Eq. 80 coefficients r and s).
+ *   x [T][d]; W_router [N][d]; router_bias [N] fp32 or NULL; shared_gate_w [d] or NULL
+ *   (required iff shared_mode is the sigmoid gate).
+ * Out: topk_idx [T][K]; topk_w [T][K]; shared_coef [T] (may be NULL); logits [T][N] (may be NULL).
+ * The selection key is the fp32 logit z + bias; ties go to the lower expert index. */
+moe_status moe_route(const moe_config* cfg, const void* x, const void* W_router,
+                     const float* router_bias, const void* shared_gate_w,
+                     int32_t* topk_idx, float* topk_w, float* shared_coef, float* logits,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Requested and kept counts, capacity, packed offsets and the row permutation
+ * (Section 10.1, Eq. 19-21; Section 10.3, Eq. 23, 25, 26, 27).
+ *   x [T][d]; topk_idx [T][K] as produced by moe_route (values in [0, N)).
+ * Out: counts_req [N], counts_keep [N], offsets [N+1], route_pos [T][K], perm_src [K*T],
+ *   x_perm [K*T][d] (rows [0, offsets[N]) hold x[perm_src[row]], the rest unspecified),
+ *   R_req / R_keep [num_ranks], drop_stats [4].  counts_req, R_req, R_keep and drop_stats may
+ *   be NULL; the others are required.
+ * Within one expert, packed rows ascend with the token index.  Deterministic. */
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                       int32_t* counts_req, int32_t* counts_keep, int32_t* offsets,
+                       int32_t* route_pos, int32_t* perm_src, void* x_perm,
+                       int32_t* R_req, int32_t* R_keep, int32_t* drop_stats,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Routed experts over densely packed segments (Section 20.1 Eq. 74 per segment; Section 10.3,
+ * Eq. 26: rows [offsets[e], offsets[e+1]) of x_perm belong to expert e, nothing else is computed).
+ *   x_perm [K*T][d]; offsets [N+1] (device; read on the device, never copied to the host).
+ * Out: f [K*T][d] (dtype): f[row] = SwiGLU_e(x_perm[row]) for rows < offsets[N].
+ * The intermediate h = SiLU(x W_g) * (x W_u) is kept in the workspace (dtype). */
+moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                              const void* W_gate, const void* W_up, const void* W_down,
+                              void* f, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
+/* The one (merged) shared expert over all tokens (Section 20.1, Eq. 74-76).
+ *   x [T][d]; Ws_gate, Ws_up [d_shared][d]; Ws_down [d][d_shared].
+ * Out: g [T][d] (dtype).  Requires d_shared > 0. */
+moe_status moe_shared_mlp(const moe_config* cfg, const void* x, const void* Ws_gate,
+                          const void* Ws_up, const void* Ws_down, void* g,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Weighted combine, Eq. 80: y_t = sum_{k: route_pos[t][k] >= 0} topk_w[t][k] * f[route_pos[t][k]]
+ *   + shared_coef[t] * g_t, accumulated in fp32 in slot order, then the shared term.
+ *   f [K*T][d]; route_pos, topk_w [T][K]; g [T][d] and shared_coef [T] may both be NULL
+ *   (no shared term).  Out: y [T][d] fp32.  Dropped routes add nothing and the kept
+ *   coefficients are not renormalised. */
+moe_status moe_combine(const moe_config* cfg, const void* f, const int32_t* route_pos,
+                       const float* topk_w, const void* g, const float* shared_coef, float* y,
+                       cudaStream_t stream);
+
+/* The whole layer: moe_route, moe_permute, moe_grouped_swiglu, moe_shared_mlp, moe_combine in
+ * that order on one stream, with intermediates in the workspace.  No host synchronisation. */
+moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x,
+                             const moe_outputs* out, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream);
+
+/* Eq. 75: merge n_parts ungated shared experts into one.  Part j has width widths[j] (HOST array);
+ * gate_parts[j], up_parts[j] are [widths[j]][d], down_parts[j] is [d][widths[j]] (HOST arrays of
+ * DEVICE pointers).  Out: Ws_gate, Ws_up [sum widths][d] (rows concatenated), Ws_down
+ * [d][sum widths] (columns concatenated).  Device-to-device copies on the stream. */
+moe_status moe_merge_shared(int32_t d_model, int32_t dtype, int32_t n_parts, const int32_t* widths,
+                            const void* const* gate_parts, const void* const* up_parts,
+                            const void* const* down_parts, void* Ws_gate, void* Ws_up,
+                            void* Ws_down, cudaStream_t stream);
+
+/* Prepare a fresh workspace: zero its device status word (the first 256 bytes).  Call once
+ * after allocating a workspace, before its first use.  Asynchronous on the stream. */
+moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Read and clear the device status word of a workspace.  Synchronises the stream and copies
+ * 4 bytes to the host.  *code (host) receives MOE_OK or the first device-detected error. */
+moe_status moe_read_status(void* workspace, int32_t* code, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,444 @@
+// C ABI of the MoE layer library: argument validation, the workspace layout and
+// the entry points declared in moe_gb300.h.  Validation happens on the host
+// before anything is enqueued; every entry point is asynchronous on its stream.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <type_traits>
+
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_cfg(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->T > (int64_t{1} << 28)) return MOE_ERR_INVALID_ARG;
+  if (c->d_model < 1 || c->N < 1 || c->K < 1 || c->d_expert < 1 || c->d_shared < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->N > kMaxExperts || c->K > kMaxTopK || c->K > c->N) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (c->norm < MOE_NORM_NONE || c->norm > MOE_NORM_SOFTMAX_SELECTED) return MOE_ERR_INVALID_ARG;
+  if (c->shared_mode < MOE_SHARED_NONE || c->shared_mode > MOE_SHARED_SIGMOID_GATE)
+    return MOE_ERR_INVALID_ARG;
+  if ((c->d_shared > 0) != (c->shared_mode != MOE_SHARED_NONE)) return MOE_ERR_INVALID_ARG;
+  if (c->cap_policy < MOE_CAP_NONE || c->cap_policy > MOE_CAP_RANK_WIDE) return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(c->alpha) || !std::isfinite(c->shared_gain)) return MOE_ERR_INVALID_ARG;
+  if (c->cap_policy != MOE_CAP_NONE &&
+      (!std::isfinite(c->capacity_factor) || c->capacity_factor <= 0.0))
+    return MOE_ERR_INVALID_ARG;
+  if (c->num_ranks < 1 || c->num_ranks > kMaxExperts) return MOE_ERR_INVALID_ARG;
+  if (c->rho) {
+    for (int i = 0; i < c->N; ++i)
+      if (c->rho[i] < 0 || c->rho[i] >= c->num_ranks) return MOE_ERR_INVALID_ARG;
+  }
+  const int64_t d = c->d_model, dr = c->d_expert, ds = c->d_shared;
+  if (c->dtype == MOE_BF16) {
+    // 16-byte rows for TMA and vector copies, and at least one 64-wide K block.
+    if (d % 8 || dr % 8 || ds % 8 || d < 64 || dr < 64 || (ds > 0 && ds < 64))
+      return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (d % 4) return MOE_ERR_UNSUPPORTED;
+  }
+  if (c->T * c->K * std::max<int64_t>(d, std::max(dr, ds)) > (int64_t{1} << 40))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int32_t capacity_budget(const moe_config& c) {
+  if (c.cap_policy == MOE_CAP_NONE) return 0;
+  const double routes = static_cast<double>(c.K) * static_cast<double>(c.T);
+  const double denom = c.cap_policy == MOE_CAP_PER_EXPERT ? c.N : c.num_ranks;
+  const double b = std::ceil(c.capacity_factor * routes / denom);
+  if (b < 1.0) return 1;
+  if (b > 2147483647.0) return 2147483647;
+  return static_cast<int32_t>(b);
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+moe_status check_ws(const moe_config& c, void* ws, size_t bytes, Layout* L) {
+  *L = make_layout(c);
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_MISALIGNED;
+  if (bytes < L->total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+RouteParams route_params(const moe_config& c, const void* x, const void* W_router,
+                         const float* bias, const void* gate_w, int32_t* idx, float* w,
+                         float* s, float* logits, int32_t* status) {
+  RouteParams p{};
+  p.x = x;
+  p.W_router = W_router;
+  p.router_bias = bias;
+  p.shared_gate_w = gate_w;
+  p.T = c.T;
+  p.d = c.d_model;
+  p.N = c.N;
+  p.K = c.K;
+  p.score = c.score;
+  p.norm = c.norm;
+  p.shared_mode = c.shared_mode;
+  p.alpha = c.alpha;
+  p.shared_gain = c.shared_gain;
+  p.topk_idx = idx;
+  p.topk_w = w;
+  p.shared_coef = s;
+  p.logits = logits;
+  p.status = status;
+  return p;
+}
+
+moe_status do_route(const moe_config& c, const void* x, const void* W_router, const float* bias,
+                    const void* gate_w, int32_t* idx, float* w, float* s, float* logits,
+                    int32_t* status, cudaStream_t st) {
+  if (c.T > 0 && (!x || !W_router || !idx || !w)) return MOE_ERR_INVALID_ARG;
+  if (c.shared_mode == MOE_SHARED_SIGMOID_GATE && !gate_w) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_route(route_params(c, x, W_router, bias, gate_w, idx, w, s, logits, status), c.dtype,
+                   st));
+}
+
+struct PermOut {
+  int32_t *counts_req, *counts_keep, *offsets, *route_pos, *perm_src, *R_req, *R_keep, *drops;
+  void* x_perm;
+};
+
+moe_status do_permute(const moe_config& c, const Layout& L, void* ws, const void* x,
+                      const int32_t* topk_idx, const PermOut& o, cudaStream_t st) {
+  if (c.T > 0 && (!x || !topk_idx || !o.route_pos || !o.perm_src || !o.x_perm))
+    return MOE_ERR_INVALID_ARG;
+  if (!o.counts_keep || !o.offsets) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(o.x_perm)) return MOE_ERR_MISALIGNED;
+  PermuteParams p{};
+  p.x = x;
+  p.topk_idx = topk_idx;
+  p.T = c.T;
+  p.d = c.d_model;
+  p.N = c.N;
+  p.K = c.K;
+  p.cap_policy = c.cap_policy;
+  p.cap = capacity_budget(c);
+  p.num_ranks = c.num_ranks;
+  for (int i = 0; i < c.N; ++i) p.rho[i] = c.rho ? c.rho[i] : i % c.num_ranks;
+  p.elem_bytes = static_cast<int32_t>(elem_bytes(c));
+  p.hist = at<int32_t>(ws, L.hist);
+  p.hist_tiles = L.hist_tiles;
+  p.counts_req = o.counts_req;
+  p.counts_keep = o.counts_keep;
+  p.offsets = o.offsets;
+  p.tile_prefix = at<int32_t>(ws, L.tile_prefix);
+  p.route_pos = o.route_pos;
+  p.perm_src = o.perm_src;
+  p.x_perm = o.x_perm;
+  p.R_req = o.R_req;
+  p.R_keep = o.R_keep;
+  p.drop_stats = o.drops;
+  p.status = at<int32_t>(ws, L.status);
+  return cuda_status(launch_permute(p, st));
+}
+
+moe_status do_grouped(const moe_config& c, const Layout& L, void* ws, const void* x_perm,
+                      const int32_t* offsets, const void* Wg, const void* Wu, const void* Wd,
+                      void* f, bool tile_prefix_ready, cudaStream_t st) {
+  if (!offsets) return MOE_ERR_INVALID_ARG;
+  if (c.T == 0) return MOE_OK;
+  if (!x_perm || !Wg || !Wu || !Wd || !f) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(f))
+    return MOE_ERR_MISALIGNED;
+  int32_t* status = at<int32_t>(ws, L.status);
+  int32_t* tp = at<int32_t>(ws, L.tile_prefix);
+  if (!tile_prefix_ready) {
+    moe_status s = cuda_status(launch_tile_prefix(offsets, c.N, tp, status, st));
+    if (s != MOE_OK) return s;
+  }
+  MlpParams p{};
+  p.A = x_perm;
+  p.a_rows = c.T * c.K;
+  p.offsets = offsets;
+  p.tile_prefix = tp;
+  p.groups = c.N;
+  p.d = c.d_model;
+  p.width = c.d_expert;
+  p.W_gate = Wg;
+  p.W_up = Wu;
+  p.W_down = Wd;
+  p.h = at<void>(ws, L.h);
+  p.out = f;
+  p.status = status;
+  return cuda_status(c.dtype == MOE_F32 ? launch_mlp_f32(p, st) : launch_mlp_bf16(p, st));
+}
+
+moe_status do_shared(const moe_config& c, const Layout& L, void* ws, const void* x,
+                     const void* Wg, const void* Wu, const void* Wd, void* g, cudaStream_t st) {
+  if (c.d_shared == 0) return MOE_ERR_INVALID_ARG;
+  if (c.T == 0) return MOE_OK;
+  if (!x || !Wg || !Wu || !Wd || !g) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(g))
+    return MOE_ERR_MISALIGNED;
+  MlpParams p{};
+  p.A = x;
+  p.a_rows = c.T;
+  p.offsets = nullptr;
+  p.tile_prefix = nullptr;
+  p.dense_rows = c.T;
+  p.groups = 1;
+  p.d = c.d_model;
+  p.width = c.d_shared;
+  p.W_gate = Wg;
+  p.W_up = Wu;
+  p.W_down = Wd;
+  p.h = at<void>(ws, L.hs);
+  p.out = g;
+  p.status = at<int32_t>(ws, L.status);
+  return cuda_status(c.dtype == MOE_F32 ? launch_mlp_f32(p, st) : launch_mlp_bf16(p, st));
+}
+
+moe_status do_combine(const moe_config& c, const void* f, const int32_t* route_pos,
+                      const float* topk_w, const void* g, const float* s, float* y,
+                      int32_t* status, cudaStream_t st) {
+  if (c.T == 0) return MOE_OK;
+  if (!f || !route_pos || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+  if ((g == nullptr) != (s == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(f) || !aligned16(y) || (g && !aligned16(g))) return MOE_ERR_MISALIGNED;
+  CombineParams p{};
+  p.f = f;
+  p.route_pos = route_pos;
+  p.topk_w = topk_w;
+  p.g = g;
+  p.shared_coef = s;
+  p.y = y;
+  p.T = c.T;
+  p.d = c.d_model;
+  p.K = c.K;
+  p.f_rows = c.T * c.K;
+  p.status = status;
+  return cuda_status(launch_combine(p, c.dtype, st));
+}
+
+}  // namespace
+
+Layout make_layout(const moe_config& c) {
+  Layout L{};
+  const size_t T = static_cast<size_t>(c.T), N = c.N, K = c.K, d = c.d_model, dr = c.d_expert,
+               ds = c.d_shared, eb = elem_bytes(c), M = c.num_ranks;
+  L.hist_tiles = (c.T + kHistTile - 1) / kHistTile;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L.status = take(256);
+  L.hist = take(static_cast<size_t>(L.hist_tiles) * N * 4);
+  L.tile_prefix = take((N + 1) * 4);
+  L.topk_idx = take(T * K * 4);
+  L.topk_w = take(T * K * 4);
+  L.shared_coef = take(T * 4);
+  L.logits = take(T * N * 4);
+  L.counts_req = take(N * 4);
+  L.counts_keep = take(N * 4);
+  L.offsets = take((N + 1) * 4);
+  L.route_pos = take(T * K * 4);
+  L.perm_src = take(T * K * 4);
+  L.R_req = take(M * 4);
+  L.R_keep = take(M * 4);
+  L.drop_stats = take(16);
+  L.x_perm = take(T * K * d * eb);
+  L.h = take(T * K * dr * eb);
+  L.f = take(T * K * d * eb);
+  L.hs = take(T * ds * eb);
+  L.g = take(T * d * eb);
+  L.total = o;
+  return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_version(void) { return "moe_gb300 0.1 (sm_103a)"; }
+
+const char* moe_status_string(int32_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape for this build";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_BOUNDS: return "device index out of range";
+    case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    default: return "unknown status";
+  }
+}
+
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_config* cfg, const void* x, const void* W_router,
+                     const float* router_bias, const void* shared_gate_w, int32_t* topk_idx,
+                     float* topk_w, float* shared_coef, float* logits, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  Layout L;
+  if ((s = check_ws(*cfg, workspace, workspace_bytes, &L)) != MOE_OK) return s;
+  return do_route(*cfg, x, W_router, router_bias, shared_gate_w, topk_idx, topk_w, shared_coef,
+                  logits, at<int32_t>(workspace, L.status), stream);
+}
+
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                       int32_t* counts_req, int32_t* counts_keep, int32_t* offsets,
+                       int32_t* route_pos, int32_t* perm_src, void* x_perm, int32_t* R_req,
+                       int32_t* R_keep, int32_t* drop_stats, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  Layout L;
+  if ((s = check_ws(*cfg, workspace, workspace_bytes, &L)) != MOE_OK) return s;
+  PermOut o{counts_req, counts_keep, offsets, route_pos, perm_src, R_req, R_keep, drop_stats,
+            x_perm};
+  return do_permute(*cfg, L, workspace, x, topk_idx, o, stream);
+}
+
+moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                              const void* W_gate, const void* W_up, const void* W_down, void* f,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  Layout L;
+  if ((s = check_ws(*cfg, workspace, workspace_bytes, &L)) != MOE_OK) return s;
+  return do_grouped(*cfg, L, workspace, x_perm, offsets, W_gate, W_up, W_down, f, false, stream);
+}
+
+moe_status moe_shared_mlp(const moe_config* cfg, const void* x, const void* Ws_gate,
+                          const void* Ws_up, const void* Ws_down, void* g, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  Layout L;
+  if ((s = check_ws(*cfg, workspace, workspace_bytes, &L)) != MOE_OK) return s;
+  return do_shared(*cfg, L, workspace, x, Ws_gate, Ws_up, Ws_down, g, stream);
+}
+
+moe_status moe_combine(const moe_config* cfg, const void* f, const int32_t* route_pos,
+                       const float* topk_w, const void* g, const float* shared_coef, float* y,
+                       cudaStream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  return do_combine(*cfg, f, route_pos, topk_w, g, shared_coef, y, nullptr, stream);
+}
+
+moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x,
+                             const moe_outputs* out, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!w || !out || (!out->y && cfg->T > 0)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if ((s = check_ws(*cfg, workspace, workspace_bytes, &L)) != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  void* ws = workspace;
+  auto pick = [&](auto* user, size_t off) {
+    using P = std::remove_pointer_t<decltype(user)>;
+    return user ? user : at<P>(ws, off);
+  };
+  int32_t* idx = pick(out->topk_idx, L.topk_idx);
+  float* tw = pick(out->topk_w, L.topk_w);
+  float* sc = pick(out->shared_coef, L.shared_coef);
+  int32_t* status = at<int32_t>(ws, L.status);
+  if ((s = do_route(c, x, w->W_router, w->router_bias, w->shared_gate_w, idx, tw, sc, out->logits,
+                    status, stream)) != MOE_OK)
+    return s;
+  PermOut po{pick(out->counts_req, L.counts_req), pick(out->counts_keep, L.counts_keep),
+             pick(out->offsets, L.offsets),       pick(out->route_pos, L.route_pos),
+             pick(out->perm_src, L.perm_src),     pick(out->R_req, L.R_req),
+             pick(out->R_keep, L.R_keep),         pick(out->drop_stats, L.drop_stats),
+             at<void>(ws, L.x_perm)};
+  if ((s = do_permute(c, L, ws, x, idx, po, stream)) != MOE_OK) return s;
+  void* f = at<void>(ws, L.f);
+  if ((s = do_grouped(c, L, ws, po.x_perm, po.offsets, w->W_gate, w->W_up, w->W_down, f, true,
+                      stream)) != MOE_OK)
+    return s;
+  void* g = nullptr;
+  if (c.d_shared > 0) {
+    g = at<void>(ws, L.g);
+    if ((s = do_shared(c, L, ws, x, w->Ws_gate, w->Ws_up, w->Ws_down, g, stream)) != MOE_OK)
+      return s;
+  }
+  return do_combine(c, f, po.route_pos, tw, g, g ? sc : nullptr, out->y, status, stream);
+}
+
+moe_status moe_merge_shared(int32_t d_model, int32_t dtype, int32_t n_parts, const int32_t* widths,
+                            const void* const* gate_parts, const void* const* up_parts,
+                            const void* const* down_parts, void* Ws_gate, void* Ws_up,
+                            void* Ws_down, cudaStream_t stream) {
+  if (d_model < 1 || n_parts < 1 || !widths || !gate_parts || !up_parts || !down_parts ||
+      !Ws_gate || !Ws_up || !Ws_down)
+    return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_F32 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  const size_t eb = dtype == MOE_F32 ? 4 : 2;
+  size_t total = 0;
+  for (int j = 0; j < n_parts; ++j) {
+    if (widths[j] < 1 || !gate_parts[j] || !up_parts[j] || !down_parts[j])
+      return MOE_ERR_INVALID_ARG;
+    total += static_cast<size_t>(widths[j]);
+  }
+  size_t row = 0;
+  for (int j = 0; j < n_parts; ++j) {
+    const size_t w = static_cast<size_t>(widths[j]);
+    const size_t rows_bytes = w * d_model * eb;
+    cudaError_t e = cudaMemcpyAsync(static_cast<char*>(Ws_gate) + row * d_model * eb,
+                                    gate_parts[j], rows_bytes, cudaMemcpyDeviceToDevice, stream);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<char*>(Ws_up) + row * d_model * eb, up_parts[j], rows_bytes,
+                          cudaMemcpyDeviceToDevice, stream);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(static_cast<char*>(Ws_down) + row * eb, total * eb, down_parts[j],
+                            w * eb, w * eb, static_cast<size_t>(d_model),
+                            cudaMemcpyDeviceToDevice, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    row += w;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!workspace || workspace_bytes < 256) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_MISALIGNED;
+  return cudaMemsetAsync(workspace, 0, 256, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_read_status(void* workspace, int32_t* code, cudaStream_t stream) {
+  if (!workspace || !code) return MOE_ERR_INVALID_ARG;
+  int32_t host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  *code = host;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,117 @@
+// Internal declarations of the MoE layer library: the workspace layout and the
+// kernel launchers.  Every launcher enqueues on the given stream and returns the
+// CUDA error of the launch (cudaSuccess on success).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe_gb300.h"
+
+namespace moe {
+
+constexpr int kMaxExperts = 256;   // N limit (routing keeps up to 8 logits per lane of a warp)
+constexpr int kMaxTopK = 8;
+constexpr int kHistTile = 256;     // tokens per counting tile of the permutation
+constexpr int kTcRows = 128;       // rows per tensor-core tile (tcgen05 M)
+
+// Byte offsets of the regions of one workspace (each region 256-byte aligned).
+struct Layout {
+  size_t status, hist, tile_prefix, topk_idx, topk_w, shared_coef, logits, counts_req,
+      counts_keep, offsets, route_pos, perm_src, R_req, R_keep, drop_stats, x_perm, h, f, hs, g;
+  size_t total;
+  int64_t hist_tiles;
+};
+
+Layout make_layout(const moe_config& c);
+
+inline size_t elem_bytes(const moe_config& c) { return c.dtype == MOE_F32 ? 4 : 2; }
+
+// ---- routing -----------------------------------------------------------------
+struct RouteParams {
+  const void* x;
+  const void* W_router;
+  const float* router_bias;
+  const void* shared_gate_w;
+  int64_t T;
+  int32_t d, N, K, score, norm, shared_mode;
+  float alpha, shared_gain;
+  int32_t* topk_idx;
+  float* topk_w;
+  float* shared_coef;
+  float* logits;
+  int32_t* status;
+};
+cudaError_t launch_route(const RouteParams& p, int32_t dtype, cudaStream_t s);
+
+// ---- counting, capacity, permutation ----------------------------------------
+struct PermuteParams {
+  const void* x;
+  const int32_t* topk_idx;
+  int64_t T;
+  int32_t d, N, K;
+  int32_t cap_policy;
+  int32_t cap;            // per-expert budget b or per-rank budget B (ignored without capacity)
+  int32_t num_ranks;
+  int32_t rho[kMaxExperts];
+  int32_t elem_bytes;
+  int32_t* hist;          // [hist_tiles][N] workspace
+  int64_t hist_tiles;
+  int32_t* counts_req;
+  int32_t* counts_keep;
+  int32_t* offsets;
+  int32_t* tile_prefix;   // [N+1] m-tile prefix for the grouped GEMMs
+  int32_t* route_pos;
+  int32_t* perm_src;
+  void* x_perm;
+  int32_t* R_req;
+  int32_t* R_keep;
+  int32_t* drop_stats;
+  int32_t* status;
+};
+cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s);
+
+// m-tile prefix of packed segments: tile_prefix[e] = sum_{i<e} ceil((offsets[i+1]-offsets[i]) / 128).
+cudaError_t launch_tile_prefix(const int32_t* offsets, int32_t N, int32_t* tile_prefix,
+                               int32_t* status, cudaStream_t s);
+
+// ---- expert GEMMs -------------------------------------------------------------
+// One grouped SwiGLU MLP over packed segments (groups = N routed experts) or over
+// one dense block of rows (groups = 1, offsets == nullptr, rows = dense_rows).
+struct MlpParams {
+  const void* A;              // [a_rows][d] input rows
+  int64_t a_rows;             // rows of the A buffer (capacity, for TMA bounds)
+  const int32_t* offsets;     // [groups+1] device, or nullptr for one dense group
+  const int32_t* tile_prefix; // [groups+1] device, or nullptr for one dense group
+  int64_t dense_rows;
+  int32_t groups;
+  int32_t d;                  // model width (K of gate/up, N of down)
+  int32_t width;              // intermediate width per group
+  const void* W_gate;         // [groups][width][d]
+  const void* W_up;           // [groups][width][d]
+  const void* W_down;         // [groups][d][width]
+  void* h;                    // [a_rows][width] intermediate (workspace)
+  void* out;                  // [a_rows][d]
+  int32_t* status;
+};
+cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s);
+cudaError_t launch_mlp_f32(const MlpParams& p, cudaStream_t s);
+
+// ---- combine -------------------------------------------------------------------
+struct CombineParams {
+  const void* f;
+  const int32_t* route_pos;
+  const float* topk_w;
+  const void* g;
+  const float* shared_coef;
+  float* y;
+  int64_t T;
+  int32_t d, K;
+  int64_t f_rows;             // rows of f (positions must be below)
+  int32_t* status;
+};
+cudaError_t launch_combine(const CombineParams& p, int32_t dtype, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,242 @@
+// Requested and kept counts, capacity, packed offsets and the row permutation.
+//
+// Follows Section 10 "Routing, Capacity, and Load Balancing": Eq. 19 (requested
+// counts), Eq. 20-21 (destination totals, kept counts, drops), Eq. 23 / Eq. 25
+// (rank-wide and per-expert budgets), the admission order of Section 10.3
+// (local-expert-major, a prefix of each expert's requests in token order),
+// Eq. 26 (kept rows packed densely per expert, offsets o_e) and Eq. 27 (drops).
+//
+// A stable counting sort, four launches, no atomics on positions:
+//   1. count   - one CTA per tile of 256 tokens: per-tile histogram of experts.
+//   2. scan    - one CTA: per-expert exclusive prefix over tiles (C^req falls out),
+//                the capacity rule (C^keep), offsets, destination totals, the
+//                m-tile prefix the grouped GEMMs walk, and the dropped-route total.
+//   3. place   - one warp per tile: walks the tile's routes in (token, slot) order,
+//                ranks equal experts with __match_any_sync, and writes the packed
+//                position of every kept route (-1 if dropped) and its source token.
+//   4. gather  - one warp per packed row: copies x[perm_src[row]] into x_perm[row].
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(256) count_kernel(PermuteParams p) {
+  __shared__ int hist[kMaxExperts];
+  for (int e = threadIdx.x; e < p.N; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kHistTile;
+  const int64_t t1 = min(t0 + kHistTile, p.T);
+  const int64_t r0 = t0 * p.K, r1 = t1 * p.K;
+  for (int64_t r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+    const int e = p.topk_idx[r];
+    if (e < 0 || e >= p.N) {
+      set_status(p.status, MOE_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    atomicAdd(&hist[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < p.N; e += blockDim.x)
+    p.hist[blockIdx.x * static_cast<int64_t>(p.N) + e] = hist[e];
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(PermuteParams p) {
+  __shared__ int creq[kMaxExperts];
+  __shared__ int ckeep[kMaxExperts];
+  __shared__ int offs[kMaxExperts + 1];
+  __shared__ int tprefix[kMaxExperts + 1];
+  __shared__ int rreq[kMaxExperts];
+  __shared__ int rkeep[kMaxExperts];
+  __shared__ int dropped;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
+
+  // 1. per-expert exclusive prefix over tiles, in place; C^req is the total.
+  for (int e = warp; e < p.N; e += nwarps) {
+    int running = 0;
+    for (int64_t base = 0; base < p.hist_tiles; base += 32) {
+      const int64_t tile = base + lane;
+      const int v = tile < p.hist_tiles ? p.hist[tile * p.N + e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (tile < p.hist_tiles) p.hist[tile * p.N + e] = running + incl - v;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) creq[e] = running;
+  }
+  __syncthreads();
+
+  // 2. capacity, offsets, destination totals: sequential over experts, in ascending
+  //    expert index (the local-expert-major admission order of the rank-wide rule).
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < p.num_ranks; ++q) { rreq[q] = 0; rkeep[q] = 0; }
+    int total_drop = 0;
+    offs[0] = 0;
+    tprefix[0] = 0;
+    for (int e = 0; e < p.N; ++e) {
+      const int q = p.rho[e];
+      int keep = creq[e];
+      if (p.cap_policy == MOE_CAP_PER_EXPERT) {
+        keep = min(keep, p.cap);
+      } else if (p.cap_policy == MOE_CAP_RANK_WIDE) {
+        keep = min(keep, p.cap - rkeep[q]);
+      }
+      ckeep[e] = keep;
+      rreq[q] += creq[e];
+      rkeep[q] += keep;
+      total_drop += creq[e] - keep;
+      offs[e + 1] = offs[e] + keep;
+      tprefix[e + 1] = tprefix[e] + (keep + kTcRows - 1) / kTcRows;
+    }
+    dropped = total_drop;
+  }
+  __syncthreads();
+
+  for (int e = threadIdx.x; e < p.N; e += blockDim.x) {
+    if (p.counts_req) p.counts_req[e] = creq[e];
+    p.counts_keep[e] = ckeep[e];
+  }
+  for (int e = threadIdx.x; e <= p.N; e += blockDim.x) {
+    p.offsets[e] = offs[e];
+    p.tile_prefix[e] = tprefix[e];
+  }
+  for (int q = threadIdx.x; q < p.num_ranks; q += blockDim.x) {
+    if (p.R_req) p.R_req[q] = rreq[q];
+    if (p.R_keep) p.R_keep[q] = rkeep[q];
+  }
+  if (threadIdx.x == 0 && p.drop_stats) {
+    p.drop_stats[0] = dropped;
+    p.drop_stats[1] = 0;
+    p.drop_stats[2] = 0;
+    p.drop_stats[3] = 0;
+  }
+}
+
+__global__ void __launch_bounds__(32) place_kernel(PermuteParams p) {
+  __shared__ int cnt[kMaxExperts];
+  __shared__ int ckeep[kMaxExperts];
+  __shared__ int offs[kMaxExperts];
+  __shared__ int drops[kHistTile];
+  const int lane = threadIdx.x;
+  const int64_t tile = blockIdx.x;
+  for (int e = lane; e < p.N; e += 32) {
+    cnt[e] = p.hist[tile * p.N + e];      // routes to e from earlier tiles
+    ckeep[e] = p.counts_keep[e];
+    offs[e] = p.offsets[e];
+  }
+  for (int i = lane; i < kHistTile; i += 32) drops[i] = 0;
+  __syncwarp();
+
+  const int64_t t0 = tile * kHistTile;
+  const int64_t t1 = min(t0 + kHistTile, p.T);
+  const int64_t r0 = t0 * p.K, r1 = t1 * p.K;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int64_t base = r0; base < r1; base += 32) {
+    const int64_t r = base + lane;
+    int e = -1;
+    if (r < r1) {
+      e = p.topk_idx[r];
+      if (e < 0 || e >= p.N) e = -1;   // reported by the count kernel
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int rank_in_round = __popc(same & lt_mask);
+    const int g = (e >= 0) ? cnt[e] + rank_in_round : 0;
+    __syncwarp();
+    if (e >= 0 && rank_in_round == 0) cnt[e] += __popc(same);
+    __syncwarp();
+    if (r < r1) {
+      const int64_t t = r / p.K;
+      if (e >= 0 && g < ckeep[e]) {
+        const int pos = offs[e] + g;
+        p.route_pos[r] = pos;
+        p.perm_src[pos] = static_cast<int32_t>(t);
+      } else {
+        p.route_pos[r] = -1;
+        atomicAdd(&drops[t - t0], 1);
+      }
+    }
+  }
+  __syncwarp();
+  if (p.drop_stats) {
+    int lost_any = 0, lost_all = 0;
+    for (int64_t t = t0 + lane; t < t1; t += 32) {
+      const int d = drops[t - t0];
+      lost_any += d > 0;
+      lost_all += d == p.K;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      lost_any += __shfl_xor_sync(0xffffffffu, lost_any, off);
+      lost_all += __shfl_xor_sync(0xffffffffu, lost_all, off);
+    }
+    if (lane == 0) {
+      if (lost_any) atomicAdd(&p.drop_stats[1], lost_any);
+      if (lost_all) atomicAdd(&p.drop_stats[2], lost_all);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) gather_kernel(PermuteParams p) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  const int64_t rows = min(static_cast<int64_t>(p.offsets[p.N]), p.T * p.K);
+  if (row >= rows) return;
+  const int32_t src = p.perm_src[row];
+  if (src < 0 || src >= p.T) {
+    set_status(p.status, MOE_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int64_t nvec = static_cast<int64_t>(p.d) * p.elem_bytes / 16;
+  const int4* s = reinterpret_cast<const int4*>(static_cast<const char*>(p.x) + src * nvec * 16);
+  int4* dst = reinterpret_cast<int4*>(static_cast<char*>(p.x_perm) + row * nvec * 16);
+  for (int64_t v = lane; v < nvec; v += 32) dst[v] = s[v];
+}
+
+__global__ void tile_prefix_kernel(const int32_t* offsets, int32_t N, int32_t* tile_prefix,
+                                   int32_t* status) {
+  if (threadIdx.x != 0) return;
+  int acc = 0;
+  tile_prefix[0] = 0;
+  for (int e = 0; e < N; ++e) {
+    const int m = offsets[e + 1] - offsets[e];
+    if (m < 0) {
+      set_status(status, MOE_ERR_DEVICE_BOUNDS);
+      acc = 0x3fffffff;  // no valid tile walk exists; make every later prefix huge but finite
+    } else {
+      acc += (m + kTcRows - 1) / kTcRows;
+    }
+    tile_prefix[e + 1] = acc;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s) {
+  const unsigned tiles = static_cast<unsigned>(p.hist_tiles);
+  if (p.T > 0) {
+    count_kernel<<<tiles, 256, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  scan_kernel<<<1, 1024, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.T == 0) return e;
+  place_kernel<<<tiles, 32, 0, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t max_rows = p.T * p.K;
+  gather_kernel<<<static_cast<unsigned>((max_rows + 7) / 8), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_prefix(const int32_t* offsets, int32_t N, int32_t* tile_prefix,
+                               int32_t* status, cudaStream_t s) {
+  tile_prefix_kernel<<<1, 32, 0, s>>>(offsets, N, tile_prefix, status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

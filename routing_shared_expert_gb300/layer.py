@@ -1,0 +1,109 @@
+"""A convenience holder for one MoE layer on the device: config, weights, workspace, outputs.
+
+Marshalling only.  ``forward`` is one ``moe_layer_forward`` call; ``forward_staged``
+runs the same five entry points one by one (optionally recording CUDA events
+between them on the launching stream, which is how per-kernel times are taken).
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import torch
+
+from . import _native as nat
+
+
+def config_from_spec(spec, T: Optional[int] = None) -> nat.moe_config:
+    """A ``moe_config`` from any object with the layer's fields (T, d_model, N, K, ...)."""
+    return nat.make_config(
+        T=spec.T if T is None else T, d_model=spec.d_model, N=spec.N, K=spec.K,
+        d_expert=spec.d_expert, d_shared=spec.d_shared, dtype=spec.dtype, score=spec.score,
+        norm=spec.norm, alpha=spec.alpha, shared_mode=spec.shared_mode,
+        shared_gain=spec.shared_gain, cap_policy=spec.cap_policy,
+        capacity_factor=spec.capacity_factor, num_ranks=spec.num_ranks,
+        rho=[i % spec.num_ranks for i in range(spec.N)])
+
+
+STAGES = ("route", "permute", "grouped_swiglu", "shared_mlp", "combine")
+
+
+class MoELayer:
+    def __init__(self, cfg: nat.moe_config, weights: Dict[str, Optional[torch.Tensor]],
+                 device="cuda", staged_buffers: bool = True):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        self.weights = weights
+        self.w = nat.make_weights(weights["W_router"], weights.get("router_bias"),
+                                  weights.get("shared_gate_w"), weights["W_gate"], weights["W_up"],
+                                  weights["W_down"], weights.get("Ws_gate"), weights.get("Ws_up"),
+                                  weights.get("Ws_down"))
+        self.ws = nat.alloc_workspace(cfg, device)
+        T, d, N, K, M = cfg.T, cfg.d_model, cfg.N, cfg.K, cfg.num_ranks
+        i32 = dict(dtype=torch.int32, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.out = {
+            "y": torch.empty((T, d), **f32),
+            "topk_idx": torch.empty((T, K), **i32),
+            "topk_w": torch.empty((T, K), **f32),
+            "shared_coef": torch.empty((T,), **f32),
+            "logits": torch.empty((T, N), **f32),
+            "counts_req": torch.empty((N,), **i32),
+            "counts_keep": torch.empty((N,), **i32),
+            "offsets": torch.empty((N + 1,), **i32),
+            "route_pos": torch.empty((T, K), **i32),
+            "perm_src": torch.empty((T * K,), **i32),
+            "R_req": torch.empty((M,), **i32),
+            "R_keep": torch.empty((M,), **i32),
+            "drop_stats": torch.empty((4,), **i32),
+        }
+        self.outputs = nat.make_outputs(**self.out)
+        self.staged = None
+        if staged_buffers:
+            dt = torch.float32 if cfg.dtype == nat.DTYPES["f32"] else torch.bfloat16
+            self.staged = {
+                "x_perm": torch.empty((T * K, d), dtype=dt, device=device),
+                "f": torch.empty((T * K, d), dtype=dt, device=device),
+                "g": torch.empty((T, d), dtype=dt, device=device) if cfg.d_shared > 0 else None,
+            }
+
+    def forward(self, x: torch.Tensor, stream=None, logits: bool = True) -> torch.Tensor:
+        outs = self.outputs if logits else self._no_logits()
+        nat.moe_layer_forward(self.cfg, self.w, x, outs, self.ws, stream)
+        return self.out["y"]
+
+    def _no_logits(self):
+        if not hasattr(self, "_outputs_nolog"):
+            d = {k: v for k, v in self.out.items() if k != "logits"}
+            self._outputs_nolog = nat.make_outputs(**d)
+        return self._outputs_nolog
+
+    def forward_staged(self, x: torch.Tensor, events=None, stream=None) -> torch.Tensor:
+        """The five entry points in order; ``events`` (len 6) are recorded around them."""
+        c, o, s, w = self.cfg, self.out, self.staged, self.weights
+        st = stream if stream is not None else torch.cuda.current_stream()
+
+        def rec(i):
+            if events is not None:
+                events[i].record(st)
+
+        rec(0)
+        nat.moe_route(c, x, w["W_router"], w.get("router_bias"), w.get("shared_gate_w"),
+                      o["topk_idx"], o["topk_w"], o["shared_coef"], o["logits"], self.ws, st)
+        rec(1)
+        nat.moe_permute(c, x, o["topk_idx"], o["counts_req"], o["counts_keep"], o["offsets"],
+                        o["route_pos"], o["perm_src"], s["x_perm"], o["R_req"], o["R_keep"],
+                        o["drop_stats"], self.ws, st)
+        rec(2)
+        nat.moe_grouped_swiglu(c, s["x_perm"], o["offsets"], w["W_gate"], w["W_up"], w["W_down"],
+                               s["f"], self.ws, st)
+        rec(3)
+        if c.d_shared > 0:
+            nat.moe_shared_mlp(c, x, w["Ws_gate"], w["Ws_up"], w["Ws_down"], s["g"], self.ws, st)
+        rec(4)
+        nat.moe_combine(c, s["f"], o["route_pos"], o["topk_w"], s["g"],
+                        o["shared_coef"] if c.d_shared > 0 else None, o["y"], st)
+        rec(5)
+        return o["y"]
+
+    def status(self) -> int:
+        return nat.moe_read_status(self.ws)

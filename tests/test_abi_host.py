@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every function ``include/moe_gb300.h`` declares,
+and reject invalid layers on the host before touching CUDA.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def nat():
+    from routing_shared_expert_gb300 import build
+    build.build()
+    from routing_shared_expert_gb300 import _native
+    return _native
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|moe_status)\s+(moe_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("moe_route", "moe_permute", "moe_grouped_swiglu", "moe_shared_mlp", "moe_combine",
+              "moe_layer_forward", "moe_workspace_size", "moe_read_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(nat):
+    lib = nat.library()
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def _olmo(**kw):
+    from workloads import CONFIGS
+    from routing_shared_expert_gb300.layer import config_from_spec
+    spec = CONFIGS["olmo"]
+    c = config_from_spec(spec)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def test_workspace_size_valid_and_monotone(nat):
+    a = nat.moe_workspace_size(_olmo(T=1024))
+    b = nat.moe_workspace_size(_olmo(T=2048))
+    assert 0 < a < b
+    assert a % 256 == 0
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("K", 0, -1), ("K", 33, -1), ("N", 0, -1), ("N", 300, -1), ("T", -1, -1),
+    ("dtype", 7, -1), ("score", 3, -1), ("norm", 9, -1), ("shared_mode", 0, -1),
+    ("cap_policy", 5, -1), ("num_ranks", 0, -1), ("alpha", float("nan"), -1),
+    ("d_model", 100, -2), ("d_expert", 36, -2),
+])
+def test_invalid_layers_rejected_on_host(nat, field, value, status):
+    c = _olmo(**{field: value})
+    n = ctypes.c_size_t(0)
+    got = nat.library().moe_workspace_size(ctypes.byref(c), ctypes.byref(n))
+    assert got == status, (field, value, got)
+
+
+def test_capacity_factor_checked_only_with_a_policy(nat):
+    c = _olmo(capacity_factor=-1.0)
+    assert nat.moe_workspace_size(c) > 0
+    c = _olmo(capacity_factor=-1.0, cap_policy=1)
+    with pytest.raises(nat.MoEError):
+        nat.moe_workspace_size(c)
+
+
+def test_rho_out_of_range_rejected(nat):
+    c = nat.make_config(T=16, d_model=64, N=4, K=1, d_expert=64, d_shared=0, shared_mode="none",
+                        cap_policy="rank_wide", num_ranks=2, rho=[0, 1, 2, 0])
+    with pytest.raises(nat.MoEError):
+        nat.moe_workspace_size(c)
+
+
+def test_entry_points_reject_before_cuda(nat):
+    """Null workspace / null outputs are refused on the host; no CUDA call is made."""
+    lib = nat.library()
+    c = _olmo(T=64)
+    fake = ctypes.c_void_p(0x1000)
+    st = lib.moe_route(ctypes.byref(c), fake, fake, None, None, fake, fake, None, None, None, 0, None)
+    assert st == -1
+    st = lib.moe_route(ctypes.byref(c), fake, fake, None, None, fake, fake, None, None,
+                       ctypes.c_void_p(0x100100), 16, None)
+    assert st == -4   # workspace too small
+    st = lib.moe_route(ctypes.byref(c), fake, fake, None, None, fake, fake, None, None,
+                       ctypes.c_void_p(0x100101), 1 << 40, None)
+    assert st == -7   # misaligned workspace
+    w = nat.moe_weights()
+    o = nat.moe_outputs()
+    st = lib.moe_layer_forward(ctypes.byref(c), ctypes.byref(w), fake, ctypes.byref(o), None, 0, None)
+    assert st == -1   # y missing
+    # combine with g but no shared coefficient
+    st = lib.moe_combine(ctypes.byref(c), fake, fake, fake, fake, None, fake, None)
+    assert st == -1
+
+
+def test_status_strings(nat):
+    lib = nat.library()
+    for code in range(-7, 1):
+        assert lib.moe_status_string(code)
+    assert nat.version().startswith("moe_gb300")

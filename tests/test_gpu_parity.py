@@ -1,0 +1,191 @@
+"""Parity of the CUDA path (through the C ABI) against the oracle, on a GB300.
+
+Bars: top-K indices, counts, capacity decisions, offsets, positions and the
+permutation bit-exact given the device's router logits (lowest index on ties);
+y within max|y - y_ref| / rms(y_ref) <= 1e-5 (fp32 layers) or 1.5e-2 (bf16
+layers, fp32 accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests.gpu_helpers import TOL, check_logits, check_routing_exact, host, oracle_y, rel_err, run_layer
+from workloads import CONFIGS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+C = CONFIGS
+SMALL = {
+    # sizes the oracle finishes in seconds that still span several tiles and ragged tails:
+    # T not a multiple of the 256-token counting tile or the 128-row GEMM tile, d_r not a
+    # multiple of the 128-column gate/up tile, d not a multiple of the 256-column down tile.
+    "tiny": C["tiny"],
+    "olmo_s": C["olmo"].replace(T=1000, d_model=512, d_expert=384, d_shared=256),
+    "qwen2_s": C["qwen2"].replace(T=777, d_model=256, d_expert=200, d_shared=320),
+    "dsv3_s": C["dsv3"].replace(T=600, d_model=448, d_expert=128, d_shared=128),
+    "mixtral_s": C["mixtral"].replace(T=1500, d_model=320, d_expert=448),
+    "rankwide_s": C["dsv3"].replace(T=500, d_model=256, d_expert=128, d_shared=128,
+                                    cap_policy="rank_wide", capacity_factor=0.8,
+                                    logit_bias="zipf1.2"),
+    "olmo_k1": C["olmo"].replace(T=300, d_model=256, d_expert=128, d_shared=128, K=1, alpha=1.0),
+    "olmo_kN": C["olmo"].replace(T=300, d_model=256, d_expert=128, d_shared=128, N=4, K=4),
+    "tiny_cap": C["tiny"].replace(cap_policy="per_expert", capacity_factor=0.5,
+                                  logit_bias="zipf1.2"),
+    "mixtral_tightcap": C["mixtral"].replace(T=700, d_model=256, d_expert=256,
+                                             capacity_factor=0.3),
+}
+
+
+def _spec_and_inputs(name, **over):
+    spec = SMALL[name]
+    inp = make_inputs(spec, "cuda")
+    for k, v in over.items():
+        inp[k] = v
+    return spec, inp
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_layer_small(name):
+    spec, inp = _spec_and_inputs(name)
+    layer = run_layer(spec, inp)
+    assert layer.status() == 0
+    hin = host(inp)
+    check_logits(layer, spec, hin)
+    rt = check_routing_exact(layer, spec)
+    tokens = np.arange(spec.T)
+    y_ref, s_ref = oracle_y(spec, hin, rt, tokens)
+    np.testing.assert_allclose(layer.out["shared_coef"].cpu().double().numpy(), s_ref, rtol=1e-5,
+                               atol=1e-6)
+    err = rel_err(layer.out["y"].cpu().double().numpy(), y_ref)
+    assert err <= TOL[spec.dtype], f"{name}: rel err {err:.3e}"
+    if spec.cap_policy != "none":
+        assert rt.drops["dropped_routes"] > 0, "capacity case should drop routes"
+
+
+@pytest.mark.parametrize("name", ["olmo_s", "mixtral_s", "tiny", "qwen2_s"])
+def test_staged_entry_points_equal_fused(name):
+    spec, inp = _spec_and_inputs(name)
+    a = run_layer(spec, inp)
+    b = run_layer(spec, inp, staged=True)
+    for k in ("y", "topk_idx", "topk_w", "route_pos", "offsets", "counts_keep", "shared_coef"):
+        assert torch.equal(a.out[k], b.out[k]), k
+
+
+def test_equal_logits_ties_and_dense_reduction():
+    """All-zero router: every token ties on every expert; selection takes 0..K-1 and, under the
+    Olmo rule, r = 1, so the layer is one dense SwiGLU over the concatenated blocks (Eq. 81)."""
+    spec = SMALL["olmo_s"]
+    inp = make_inputs(spec, "cuda")
+    inp["W_router"] = torch.zeros_like(inp["W_router"])
+    layer = run_layer(spec, inp)
+    rt = check_routing_exact(layer, spec)
+    assert (rt.topk_idx == np.arange(spec.K)[None, :]).all()
+    np.testing.assert_allclose(layer.out["topk_w"].cpu().numpy(), 1.0, rtol=1e-6)
+    hin = host(inp)
+    K = spec.K
+    Wg = torch.cat([hin["W_gate"][e] for e in range(K)] + [hin["Ws_gate"]], 0)
+    Wu = torch.cat([hin["W_up"][e] for e in range(K)] + [hin["Ws_up"]], 0)
+    Wd = torch.cat([hin["W_down"][e] for e in range(K)] + [hin["Ws_down"]], 1)
+    dense = O.swiglu(hin["x"], Wg, Wu, Wd)
+    assert rel_err(layer.out["y"].cpu().double().numpy(), dense) <= TOL["bf16"]
+
+
+def test_empty_batch():
+    import routing_shared_expert_gb300 as moe
+    spec = SMALL["olmo_s"].replace(T=0)
+    inp = make_inputs(SMALL["olmo_s"].replace(T=1), "cuda")
+    inp["x"] = inp["x"][:0]
+    layer = moe.MoELayer(moe.config_from_spec(spec), inp, "cuda")
+    layer.forward(torch.empty((0, spec.d_model), dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    assert int(layer.out["counts_req"].sum()) == 0
+    assert int(layer.out["offsets"][-1]) == 0
+    assert layer.status() == 0
+
+
+def test_single_token_and_single_row_experts():
+    spec = SMALL["dsv3_s"].replace(T=1)
+    inp = make_inputs(spec, "cuda")
+    layer = run_layer(spec, inp)
+    rt = check_routing_exact(layer, spec)
+    assert (rt.counts_keep <= 1).all() and rt.counts_keep.sum() == spec.K
+    y_ref, _ = oracle_y(spec, host(inp), rt, np.arange(1))
+    assert rel_err(layer.out["y"].cpu().double().numpy(), y_ref) <= TOL["bf16"]
+
+
+def test_merge_shared_on_device():
+    """Eq. 75 on the device: the merged shared weights equal the concatenation, bit for bit,
+    and the layer with them matches the oracle's sum of the three parts (Eq. 76)."""
+    import routing_shared_expert_gb300 as moe
+    spec = C["tiny"]
+    inp = make_inputs(spec, "cuda", with_shared_parts=True)
+    parts = inp.pop("Ws_parts")
+    d = spec.d_model
+    g = torch.empty_like(inp["Ws_gate"])
+    u = torch.empty_like(inp["Ws_up"])
+    dn = torch.empty_like(inp["Ws_down"])
+    moe.moe_merge_shared(d, spec.dtype, [p[0] for p in parts], [p[1] for p in parts],
+                         [p[2] for p in parts], g, u, dn)
+    torch.cuda.synchronize()
+    assert torch.equal(g, inp["Ws_gate"]) and torch.equal(u, inp["Ws_up"])
+    assert torch.equal(dn, inp["Ws_down"])
+    inp["Ws_gate"], inp["Ws_up"], inp["Ws_down"] = g, u, dn
+    layer = run_layer(spec, inp)
+    hin = host(inp)
+    rt = check_routing_exact(layer, spec)
+    x = hin["x"]
+    y_ref = O.moe_outputs_for_tokens(np.arange(spec.T), x, rt,
+                                     lambda e: (hin["W_gate"][e], hin["W_up"][e], hin["W_down"][e]),
+                                     None, np.zeros(spec.T))
+    y_ref = y_ref + sum(O.swiglu(x, p[0].cpu(), p[1].cpu(), p[2].cpu()) for p in parts)
+    assert rel_err(layer.out["y"].cpu().double().numpy(), y_ref) <= TOL["f32"]
+
+
+def test_two_calls_reuse_workspace():
+    spec, inp = _spec_and_inputs("mixtral_s")
+    import routing_shared_expert_gb300 as moe
+    layer = moe.MoELayer(moe.config_from_spec(spec), inp, "cuda")
+    y1 = layer.forward(inp["x"]).clone()
+    y2 = layer.forward(inp["x"]).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+# ------------------------------------------------------------------- full sizes
+
+FULL = ["olmo", "qwen2", "dsv3", "mixtral"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_layer_full_size_sampled(name):
+    """The benchmark workloads at full size, in the launch configuration the bench times:
+    routing, counts and permutation checked for every token; logits and y on a sample."""
+    spec = C[name]
+    inp = make_inputs(spec, "cuda")
+    layer = run_layer(spec, inp)
+    assert layer.status() == 0
+    rt = check_routing_exact(layer, spec)
+    gen = np.random.default_rng(0)
+    n = 24 if name in ("dsv3", "mixtral") else 48
+    tokens = np.sort(gen.choice(spec.T, size=n, replace=False))
+    x_rows = inp["x"][torch.as_tensor(tokens, device="cuda")].cpu()
+    # logits of the sampled rows
+    z_ref = O.router_logits(x_rows, inp["W_router"].cpu(),
+                            None if inp["router_bias"] is None else inp["router_bias"].cpu())
+    z_dev = layer.out["logits"].cpu().double().numpy()[tokens]
+    assert np.abs(z_dev - z_ref).max() / np.sqrt((z_ref ** 2).mean()) < 1e-4
+    W = inp
+    s = O.shared_coefficient(x_rows, spec.shared_mode, spec.shared_gain,
+                             None if W["shared_gate_w"] is None else W["shared_gate_w"].cpu())
+    shared = None
+    if spec.d_shared > 0:
+        shared = (W["Ws_gate"].cpu(), W["Ws_up"].cpu(), W["Ws_down"].cpu())
+    y_ref = O.moe_outputs_for_tokens(
+        tokens, x_rows, rt, lambda e: (W["W_gate"][e].cpu(), W["W_up"][e].cpu(), W["W_down"][e].cpu()),
+        shared, s)
+    y_dev = layer.out["y"][torch.as_tensor(tokens, device="cuda")].cpu().double().numpy()
+    err = rel_err(y_dev, y_ref)
+    assert err <= TOL["bf16"], f"{name}: rel err {err:.3e}"
+    if spec.cap_policy != "none":
+        assert rt.drops["dropped_routes"] > 0
