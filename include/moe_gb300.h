@@ -20,7 +20,9 @@
  *   at least moe_workspace_size() bytes, 256-byte aligned.
  * - Tensors are dense row-major.  Element type of activations and weights is
  *   cfg->dtype (fp32 or bf16).  Router logits, coefficients, the shared
- *   coefficient and y are fp32.  Indices and counts are int32.
+ *   coefficient, the expert outputs f, the shared output g and y are fp32
+ *   for every dtype (the bf16 path rounds only the expert inputs and the
+ *   intermediate h, which feed the tensor cores).  Indices and counts are int32.
  * - Weight storage: W_router [N][d] (one row per expert, z = x W_router^T);
  *   W_gate, W_up [N][d_expert][d] (one row per intermediate unit, the columns
  *   of W_g / W_u of Eq. 74); W_down [N][d][d_expert] (one row per output
@@ -168,7 +170,7 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
 /* Routed experts over densely packed segments (Section 20.1 Eq. 74 per segment; Section 10.3,
  * Eq. 26: rows [offsets[e], offsets[e+1]) of x_perm belong to expert e, nothing else is computed).
  *   x_perm [K*T][d]; offsets [N+1] (device; read on the device, never copied to the host).
- * Out: f [K*T][d] (dtype): f[row] = SwiGLU_e(x_perm[row]) for rows < offsets[N].
+ * Out: f [K*T][d] fp32: f[row] = SwiGLU_e(x_perm[row]) for rows < offsets[N].
  * The intermediate h = SiLU(x W_g) * (x W_u) is kept in the workspace (dtype). */
 moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
                               const void* W_gate, const void* W_up, const void* W_down,
@@ -177,14 +179,14 @@ moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const i
 
 /* The one (merged) shared expert over all tokens (Section 20.1, Eq. 74-76).
  *   x [T][d]; Ws_gate, Ws_up [d_shared][d]; Ws_down [d][d_shared].
- * Out: g [T][d] (dtype).  Requires d_shared > 0. */
+ * Out: g [T][d] fp32.  Requires d_shared > 0. */
 moe_status moe_shared_mlp(const moe_config* cfg, const void* x, const void* Ws_gate,
                           const void* Ws_up, const void* Ws_down, void* g,
                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Weighted combine, Eq. 80: y_t = sum_{k: route_pos[t][k] >= 0} topk_w[t][k] * f[route_pos[t][k]]
  *   + shared_coef[t] * g_t, accumulated in fp32 in slot order, then the shared term.
- *   f [K*T][d]; route_pos, topk_w [T][K]; g [T][d] and shared_coef [T] may both be NULL
+ *   f [K*T][d] fp32; route_pos, topk_w [T][K]; g [T][d] fp32 and shared_coef [T] may both be NULL
  *   (no shared term).  Out: y [T][d] fp32.  Dropped routes add nothing and the kept
  *   coefficients are not renormalised. */
 moe_status moe_combine(const moe_config* cfg, const void* f, const int32_t* route_pos,

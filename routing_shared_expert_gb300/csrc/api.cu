@@ -176,7 +176,7 @@ moe_status do_grouped(const moe_config& c, const Layout& L, void* ws, const void
   p.W_up = Wu;
   p.W_down = Wd;
   p.h = at<void>(ws, L.h);
-  p.out = f;
+  p.out = static_cast<float*>(f);
   p.status = status;
   return cuda_status(c.dtype == MOE_F32 ? launch_mlp_f32(p, st) : launch_mlp_bf16(p, st));
 }
@@ -201,7 +201,7 @@ moe_status do_shared(const moe_config& c, const Layout& L, void* ws, const void*
   p.W_up = Wu;
   p.W_down = Wd;
   p.h = at<void>(ws, L.hs);
-  p.out = g;
+  p.out = static_cast<float*>(g);
   p.status = at<int32_t>(ws, L.status);
   return cuda_status(c.dtype == MOE_F32 ? launch_mlp_f32(p, st) : launch_mlp_bf16(p, st));
 }
@@ -225,7 +225,7 @@ moe_status do_combine(const moe_config& c, const void* f, const int32_t* route_p
   p.K = c.K;
   p.f_rows = c.T * c.K;
   p.status = status;
-  return cuda_status(launch_combine(p, c.dtype, st));
+  return cuda_status(launch_combine(p, st));
 }
 
 }  // namespace
@@ -258,9 +258,9 @@ Layout make_layout(const moe_config& c) {
   L.drop_stats = take(16);
   L.x_perm = take(T * K * d * eb);
   L.h = take(T * K * dr * eb);
-  L.f = take(T * K * d * eb);
+  L.f = take(T * K * d * 4);
   L.hs = take(T * ds * eb);
-  L.g = take(T * d * eb);
+  L.g = take(T * d * 4);
   L.total = o;
   return L;
 }

@@ -3,7 +3,7 @@
 // What is computed (Section 20 "One Shared Expert Is All You Need", Eq. 74, per
 // packed segment of Section 10 "Routing, Capacity, and Load Balancing", Eq. 26):
 //   gate/up:  h[row] = SiLU(x[row] W_g^e) * (x[row] W_u^e)      rows of expert e's segment
-//   down:     f[row] = h[row] W_d^e
+//   down:     f[row] = h[row] W_d^e        (fp32 output)
 // Only rows [offsets[e], offsets[e+1]) are written; the offsets are read on the
 // device, so no count ever travels to the host.  The shared expert is the same
 // kernel over one dense group of T rows.
@@ -15,7 +15,7 @@
 //               fp32 accumulate in TMEM), M = 128; commits free ring stages and
 //               publish finished accumulators.
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator rows (one TMEM lane per
-//               thread), SiLU(gate) * up or plain bf16 conversion, row-masked stores.
+//               thread), SiLU(gate) * up to bf16 h, or the fp32 rows of f; row-masked stores.
 // The accumulator is double buffered in TMEM (2 x 256 columns), so the epilogue
 // of one tile overlaps the MMAs of the next.
 //   SwiGLU mode: a tile is 128 rows x 128 h columns; the gate and up weight tiles
@@ -54,7 +54,7 @@ struct TcArgs {
   int32_t n_out;               // output columns per group
   int32_t b_rows_per_group;    // rows between groups in the 2-D view of B
   int64_t out_rows;            // rows of the output buffer (stores beyond are dropped)
-  void* out;
+  void* out;                   // SwiGLU mode: bf16 h; plain mode: fp32 f
   int64_t ldo;
   int32_t* status;
 };
@@ -283,23 +283,24 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       } else {
+        // plain mode: fp32 output rows (the expert outputs f stay in fp32 up to the combine)
+        float* out_f = static_cast<float*>(args.out) + (valid ? row : 0) * args.ldo;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t ar[32], br[32];
           tmem_ld32x2(taddr + c * 64, taddr + c * 64 + 32, ar, br);
           const int col0 = tl.n * 256 + c * 64;
           if (valid) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              pk[i] = pack_bf16x2(__uint_as_float(ar[2 * i]), __uint_as_float(ar[2 * i + 1]));
-              pk[16 + i] = pack_bf16x2(__uint_as_float(br[2 * i]), __uint_as_float(br[2 * i + 1]));
-            }
 #pragma unroll
             for (int v = 0; v < 8; ++v)
-              if (col0 + v * 8 + 8 <= args.n_out)
-                *reinterpret_cast<uint4*>(out_row + col0 + v * 8) =
-                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+              if (col0 + v * 4 + 4 <= args.n_out)
+                *reinterpret_cast<uint4*>(out_f + col0 + v * 4) =
+                    make_uint4(ar[4 * v], ar[4 * v + 1], ar[4 * v + 2], ar[4 * v + 3]);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              if (col0 + 32 + v * 4 + 4 <= args.n_out)
+                *reinterpret_cast<uint4*>(out_f + col0 + 32 + v * 4) =
+                    make_uint4(br[4 * v], br[4 * v + 1], br[4 * v + 2], br[4 * v + 3]);
           }
         }
       }

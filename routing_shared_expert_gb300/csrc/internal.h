@@ -92,8 +92,8 @@ struct MlpParams {
   const void* W_gate;         // [groups][width][d]
   const void* W_up;           // [groups][width][d]
   const void* W_down;         // [groups][d][width]
-  void* h;                    // [a_rows][width] intermediate (workspace)
-  void* out;                  // [a_rows][d]
+  void* h;                    // [a_rows][width] intermediate (workspace), layer dtype
+  float* out;                 // [a_rows][d] fp32
   int32_t* status;
 };
 cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s);
@@ -112,6 +112,6 @@ struct CombineParams {
   int64_t f_rows;             // rows of f (positions must be below)
   int32_t* status;
 };
-cudaError_t launch_combine(const CombineParams& p, int32_t dtype, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 
 }  // namespace moe

@@ -62,8 +62,8 @@ class MoELayer:
             dt = torch.float32 if cfg.dtype == nat.DTYPES["f32"] else torch.bfloat16
             self.staged = {
                 "x_perm": torch.empty((T * K, d), dtype=dt, device=device),
-                "f": torch.empty((T * K, d), dtype=dt, device=device),
-                "g": torch.empty((T, d), dtype=dt, device=device) if cfg.d_shared > 0 else None,
+                "f": torch.empty((T * K, d), dtype=torch.float32, device=device),
+                "g": torch.empty((T, d), dtype=torch.float32, device=device) if cfg.d_shared > 0 else None,
             }
 
     def forward(self, x: torch.Tensor, stream=None, logits: bool = True) -> torch.Tensor:

@@ -10,6 +10,16 @@ if ROOT not in sys.path:
 GOLDEN = os.path.join(ROOT, "tests", "golden")
 
 
+def ensure_built():
+    """Compile the CUDA library if it is missing or stale (nvcc cross-compiles without a GPU)."""
+    import importlib.util
+    path = os.path.join(ROOT, "routing_shared_expert_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("_moe_gb300_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
 

@@ -4,6 +4,9 @@ import numpy as np
 import torch
 
 import oracle as O
+from tests.conftest import ensure_built
+
+ensure_built()
 
 TOL = {"f32": 1e-5, "bf16": 1.5e-2}
 
@@ -72,3 +75,21 @@ def oracle_y(spec, inp_host, rt, tokens):
 
 def rel_err(y, y_ref):
     return float(np.abs(y - y_ref).max() / (np.sqrt((y_ref ** 2).mean()) + 1e-30))
+
+
+def layer_error(spec, y, y_ref, route_pos):
+    """max|y - y_ref| / rms(y_ref).
+
+    Rows that receive no contribution at all (every route dropped and no shared
+    expert) are exact zeros on both sides: they are checked for equality and
+    left out of the rms, which they would only shrink.
+    """
+    y = np.asarray(y)
+    if spec.d_shared == 0 or spec.shared_mode == "none":
+        empty = (np.asarray(route_pos) < 0).all(axis=1)
+        assert (y[empty] == 0).all(), "a row with every route dropped must be exactly zero"
+        assert (y_ref[empty] == 0).all()
+        if (~empty).any():
+            return rel_err(y[~empty], y_ref[~empty])
+        return 0.0
+    return rel_err(y, y_ref)

@@ -9,15 +9,14 @@ import re
 
 import pytest
 
-from tests.conftest import ROOT
+from tests.conftest import ROOT, ensure_built
 
 HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
 
 
 @pytest.fixture(scope="module")
 def nat():
-    from routing_shared_expert_gb300 import build
-    build.build()
+    ensure_built()
     from routing_shared_expert_gb300 import _native
     return _native
 
