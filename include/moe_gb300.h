@@ -167,6 +167,24 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
                        int32_t* R_req, int32_t* R_keep, int32_t* drop_stats,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* moe_permute without a workspace, for callers that cannot allocate device memory (a process
+ * whose device memory is fully planned up front, or a plugin host that passes only inputs and
+ * outputs).  The pages have no counterpart: this is a packaging variant of moe_permute with the
+ * same arguments minus the workspace, and the same results, bit for bit.
+ * Its scratch is one static device array built into the library (every GPU that loads the
+ * library holds it, 258 KiB, until the process exits): it fits ceil(T / 256) * N <= 65536
+ * (for example T <= 65536 at N = 256, T <= 524288 at N = 32); larger layers return
+ * MOE_ERR_UNSUPPORTED before anything is enqueued.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current, so make that first
+ * call before any stream capture.  All calls share the array: calls that overlap on the GPU
+ * race and must be serialised.  Calls no cudaMalloc / cudaFree.  Device-side index errors are
+ * not reported (there is no status word); out-of-range expert ids are skipped. */
+moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                               int32_t* counts_req, int32_t* counts_keep, int32_t* offsets,
+                               int32_t* route_pos, int32_t* perm_src, void* x_perm,
+                               int32_t* R_req, int32_t* R_keep, int32_t* drop_stats,
+                               cudaStream_t stream);
+
 /* Routed experts over densely packed segments (Section 20.1 Eq. 74 per segment; Section 10.3,
  * Eq. 26: rows [offsets[e], offsets[e+1]) of x_perm belong to expert e, nothing else is computed).
  *   x_perm [K*T][d]; offsets [N+1] (device; read on the device, never copied to the host).

@@ -56,7 +56,7 @@ class moe_outputs(ctypes.Structure):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it first "
-                          "(python -m routing_shared_expert_gb300.build)")
+                          "(python routing_shared_expert_gb300/build.py)")
     lib = ctypes.CDLL(LIB_PATH)
     P = c_void_p
     C = POINTER(moe_config)
@@ -67,6 +67,7 @@ def _load():
         "moe_workspace_init": ([P, c_size_t, P], c_int32),
         "moe_route": ([C, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
         "moe_permute": ([C, P, P, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
+        "moe_permute_noalloc": ([C, P, P, P, P, P, P, P, P, P, P, P, P], c_int32),
         "moe_grouped_swiglu": ([C, P, P, P, P, P, P, P, c_size_t, P], c_int32),
         "moe_shared_mlp": ([C, P, P, P, P, P, P, c_size_t, P], c_int32),
         "moe_combine": ([C, P, P, P, P, P, P, P], c_int32),
@@ -177,6 +178,15 @@ def moe_permute(cfg, x, topk_idx, counts_req, counts_keep, offsets, route_pos, p
         ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts_req), _ptr(counts_keep),
         _ptr(offsets), _ptr(route_pos), _ptr(perm_src), _ptr(x_perm), _ptr(R_req), _ptr(R_keep),
         _ptr(drop_stats), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def moe_permute_noalloc(cfg, x, topk_idx, counts_req, counts_keep, offsets, route_pos, perm_src,
+                        x_perm, R_req, R_keep, drop_stats, stream=None):
+    """moe_permute for callers that cannot allocate: no workspace (see the C header)."""
+    _check("moe_permute_noalloc", _lib.moe_permute_noalloc(
+        ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts_req), _ptr(counts_keep),
+        _ptr(offsets), _ptr(route_pos), _ptr(perm_src), _ptr(x_perm), _ptr(R_req), _ptr(R_keep),
+        _ptr(drop_stats), _stream(stream)))
 
 
 def moe_grouped_swiglu(cfg, x_perm, offsets, W_gate, W_up, W_down, f, workspace, stream=None):

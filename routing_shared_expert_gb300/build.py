@@ -3,7 +3,7 @@
 Each ``csrc/*.cu`` translation unit is compiled in parallel with nvcc
 (``-gencode arch=compute_103a,code=sm_103a``), then linked into one shared
 library next to this file.  A stamp of the sources and flags skips the work
-when nothing changed.  Usable as ``python -m routing_shared_expert_gb300.build``.
+when nothing changed.  Run with ``python routing_shared_expert_gb300/build.py`` (importing the package needs the library).
 """
 from __future__ import annotations
 

@@ -51,16 +51,6 @@ moe_status check_cfg(const moe_config* c) {
   return MOE_OK;
 }
 
-int32_t capacity_budget(const moe_config& c) {
-  if (c.cap_policy == MOE_CAP_NONE) return 0;
-  const double routes = static_cast<double>(c.K) * static_cast<double>(c.T);
-  const double denom = c.cap_policy == MOE_CAP_PER_EXPERT ? c.N : c.num_ranks;
-  const double b = std::ceil(c.capacity_factor * routes / denom);
-  if (b < 1.0) return 1;
-  if (b > 2147483647.0) return 2147483647;
-  return static_cast<int32_t>(b);
-}
-
 template <typename T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
@@ -229,6 +219,16 @@ moe_status do_combine(const moe_config& c, const void* f, const int32_t* route_p
 }
 
 }  // namespace
+
+int32_t capacity_budget(const moe_config& c) {
+  if (c.cap_policy == MOE_CAP_NONE) return 0;
+  const double routes = static_cast<double>(c.K) * static_cast<double>(c.T);
+  const double denom = c.cap_policy == MOE_CAP_PER_EXPERT ? c.N : c.num_ranks;
+  const double b = std::ceil(c.capacity_factor * routes / denom);
+  if (b < 1.0) return 1;
+  if (b > 2147483647.0) return 2147483647;
+  return static_cast<int32_t>(b);
+}
 
 Layout make_layout(const moe_config& c) {
   Layout L{};

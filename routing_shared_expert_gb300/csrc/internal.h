@@ -27,6 +27,9 @@ struct Layout {
 
 Layout make_layout(const moe_config& c);
 
+// Capacity budget of the layer: b (per expert, Eq. 25) or B (per rank, Eq. 23); 0 without capacity.
+int32_t capacity_budget(const moe_config& c);
+
 inline size_t elem_bytes(const moe_config& c) { return c.dtype == MOE_F32 ? 4 : 2; }
 
 // ---- routing -----------------------------------------------------------------
