@@ -168,7 +168,9 @@ moe_status do_grouped(const moe_config& c, const Layout& L, void* ws, const void
   p.h = at<void>(ws, L.h);
   p.out = static_cast<float*>(f);
   p.status = status;
-  return cuda_status(c.dtype == MOE_F32 ? launch_mlp_f32(p, st) : launch_mlp_bf16(p, st));
+  if (c.dtype == MOE_F32) return cuda_status(launch_mlp_f32(p, st));
+  return cuda_status(use_pair_tiles(c.T * c.K, c.N) ? launch_mlp_bf16_pair(p, st)
+                                                    : launch_mlp_bf16(p, st));
 }
 
 moe_status do_shared(const moe_config& c, const Layout& L, void* ws, const void* x,
@@ -193,7 +195,8 @@ moe_status do_shared(const moe_config& c, const Layout& L, void* ws, const void*
   p.h = at<void>(ws, L.hs);
   p.out = static_cast<float*>(g);
   p.status = at<int32_t>(ws, L.status);
-  return cuda_status(c.dtype == MOE_F32 ? launch_mlp_f32(p, st) : launch_mlp_bf16(p, st));
+  if (c.dtype == MOE_F32) return cuda_status(launch_mlp_f32(p, st));
+  return cuda_status(use_pair_tiles(c.T, 1) ? launch_mlp_bf16_pair(p, st) : launch_mlp_bf16(p, st));
 }
 
 moe_status do_combine(const moe_config& c, const void* f, const int32_t* route_pos,

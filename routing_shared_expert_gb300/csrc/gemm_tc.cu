@@ -339,19 +339,6 @@ EncodeFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [rows][inner] (row-major, dense), box 64 x box_rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
-  EncodeFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int sm_count() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -379,6 +366,19 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
 
 }  // namespace
 
+// 2-D bf16 tensor [rows][inner] (row-major, dense), box 64 x box_rows, 128-byte swizzle.
+bool make_bf16_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {
   const bool dense = p.offsets == nullptr;
   const int64_t rows_cap = p.a_rows;
@@ -387,11 +387,11 @@ cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {
   const int64_t mt_ub = dense ? (p.dense_rows + BM - 1) / BM : (rows_cap + BM - 1) / BM + p.groups;
 
   CUtensorMap mA, mG, mU, mH, mD;
-  if (!make_map(&mA, p.A, p.d, rows_cap, BM) ||
-      !make_map(&mG, p.W_gate, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
-      !make_map(&mU, p.W_up, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
-      !make_map(&mH, p.h, p.width, rows_cap, BM) ||
-      !make_map(&mD, p.W_down, p.width, static_cast<uint64_t>(p.groups) * p.d, 256))
+  if (!make_bf16_map(&mA, p.A, p.d, rows_cap, BM) ||
+      !make_bf16_map(&mG, p.W_gate, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
+      !make_bf16_map(&mU, p.W_up, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
+      !make_bf16_map(&mH, p.h, p.width, rows_cap, BM) ||
+      !make_bf16_map(&mD, p.W_down, p.width, static_cast<uint64_t>(p.groups) * p.d, 256))
     return cudaErrorInvalidValue;
 
   TcArgs a{};

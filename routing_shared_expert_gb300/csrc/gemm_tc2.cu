@@ -1,0 +1,409 @@
+// Grouped SwiGLU expert GEMMs on CTA pairs: tcgen05 with cta_group::2 (2-SM MMA).
+//
+// Computes the same as gemm_tc.cu (Section 20 "One Shared Expert Is All You
+// Need", Eq. 74, per packed segment of Section 10, Eq. 26):
+//   gate/up:  h[row] = SiLU(x[row] W_g^e) * (x[row] W_u^e)     (bf16 h)
+//   down:     f[row] = h[row] W_d^e                            (fp32 f)
+// but a cluster of two CTAs on two SMs computes each 256-row tile together.
+// The even CTA issues tcgen05.mma with M = 256, N = 256: A rows 0-127 come from
+// its own shared memory and rows 128-255 from its partner's; B columns 0-127
+// from its own and 128-255 from its partner's.  Each CTA therefore loads only
+// 16 KB of A and 16 KB of B per 64-wide K step (half the bytes per multiply-add
+// of a one-SM 128 x 256 tile), which lets six stages sit in shared memory and
+// keeps the tensor pipe fed from L2.  Each CTA's TMEM holds the fp32
+// accumulator rows of its own 128 rows for all 256 columns.
+//   SwiGLU mode: the even CTA loads the gate weight rows, the odd CTA the up
+//                rows of the same 128 h columns, so TMEM columns [0,128) hold
+//                x W_g and [128,256) hold x W_u for the CTA's rows.
+//   Plain mode:  each CTA loads 128 of the 256 output columns' weight rows.
+// Roles per CTA (192 threads): warp 0 TMA producer (both CTAs; completions are
+// counted on the even CTA's barrier), warp 1 TMEM allocation and, in the even
+// CTA only, the MMA issuer; warps 2-5 epilogue.  The epilogue stages each
+// 32 x 32 block through shared memory so that global stores are row-contiguous.
+// Every wait is bounded by %globaltimer; a wait that runs out records
+// MOE_ERR_TIMEOUT and the CTA drains what it issued before the final cluster
+// barrier and TMEM release.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;                    // rows per CTA
+constexpr int PM = 256;                    // rows per pair tile
+constexpr int BK = 64;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;       // 16 KB
+constexpr int B_BYTES = 128 * BK * 2;      // 16 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_LD = 36;                 // 32-bit words per staged row (16-byte aligned)
+constexpr int EPI_WARP_WORDS = 32 * EPI_LD;
+constexpr int EPI_BYTES = 4 * EPI_WARP_WORDS * 4;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+
+struct PairArgs {
+  const int32_t* offsets;    // [groups+1] device, or nullptr for one dense group
+  int32_t dense_rows;
+  int32_t groups;
+  int32_t k_dim;
+  int32_t n_out;             // output columns per group
+  int32_t b_rows_per_group;  // rows between groups in the 2-D view of B
+  int64_t out_rows;          // rows of the output buffer
+  void* out;                 // SwiGLU: bf16 h; plain: fp32 f
+  int64_t ldo;
+  int32_t* status;
+};
+
+struct Tile {
+  int g, m, n, seg_start, seg_end;
+};
+
+__device__ __forceinline__ bool pair_tile(const int* s_tp, const int* s_off, int G, int n_tiles,
+                                          int64_t t, Tile& o) {
+  if (t >= static_cast<int64_t>(s_tp[G]) * n_tiles) return false;
+  int lo = 0, hi = G;   // s_tp[lo] * n_tiles <= t < s_tp[hi] * n_tiles
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (static_cast<int64_t>(s_tp[mid]) * n_tiles <= t) lo = mid; else hi = mid;
+  }
+  const int mt = s_tp[lo + 1] - s_tp[lo];
+  const int64_t local = t - static_cast<int64_t>(s_tp[lo]) * n_tiles;
+  o.g = lo;
+  o.n = static_cast<int>(local / mt);
+  o.m = static_cast<int>(local % mt);
+  o.seg_start = s_off[lo];
+  o.seg_end = s_off[lo + 1];
+  return true;
+}
+
+template <bool SWIGLU>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    tc_pair_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                 const __grid_constant__ CUtensorMap tmB1, const PairArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint32_t* epi = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* never = const_cast<int*>(abort_flag) + 1;
+  const int G = args.offsets ? args.groups : 1;
+  int* s_off = never + 1;       // [G+1]
+  int* s_tp = s_off + (G + 1);  // [G+1] pair-tile prefix
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  constexpr int BN_OUT = SWIGLU ? 128 : 256;
+  const int n_tiles = (args.n_out + BN_OUT - 1) / BN_OUT;
+  const int k_blocks = (args.k_dim + BK - 1) / BK;
+  const uint32_t smem_base = smem_u32(smem);
+  const int64_t pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 8);   // 4 epilogue warps in each CTA of the pair
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    *never = 0;
+    mbar_fence_init();
+  }
+  if (warp == 3) {
+    // segment table and prefix of 256-row tiles per group
+    if (args.offsets == nullptr) {
+      if (lane == 0) {
+        s_off[0] = 0;
+        s_off[1] = args.dense_rows;
+        s_tp[0] = 0;
+        s_tp[1] = (args.dense_rows + PM - 1) / PM;
+      }
+    } else {
+      for (int i = lane; i <= G; i += 32) s_off[i] = args.offsets[i];
+      __syncwarp();
+      int running = 0;
+      for (int base = 0; base < G; base += 32) {
+        const int g = base + lane;
+        int v = 0;
+        if (g < G) {
+          const int len = s_off[g + 1] - s_off[g];
+          if (len < 0) set_status(args.status, MOE_ERR_DEVICE_BOUNDS);
+          v = len > 0 ? (len + PM - 1) / PM : 0;
+        }
+        int incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        if (g < G) s_tp[g + 1] = running + incl;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) s_tp[0] = 0;
+    }
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB0);
+    if (SWIGLU) tma_prefetch_map(&tmB1);
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_holder), TMEM_COLS);
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync_all();   // barriers initialised and TMEM allocated in both CTAs
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      const CUtensorMap* mapB = (SWIGLU && !leader) ? &tmB1 : &tmB0;
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued_parity[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+      bool ok = true;
+      Tile tl;
+      for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl); t += n_pairs) {
+        const int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * BM;
+        const int b_row = SWIGLU ? tl.g * args.b_rows_per_group + tl.n * 128
+                                 : tl.g * args.b_rows_per_group + tl.n * 256 + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
+                                 kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb_local = smem_u32(&full[stage]);
+          const uint32_t fb_leader = mapa_shared(fb_local, 0);
+          if (leader) mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
+          const uint32_t sA = smem_base + stage * STAGE_BYTES;
+          tma_load_2d_pair(sA, &tmA, kb * BK, a_row, fb_leader);
+          tma_load_2d_pair(sA + A_BYTES, mapB, kb * BK, b_row, fb_leader);
+          issued_parity[stage] = static_cast<int>(phase);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok && leader) {
+        // The even CTA's full barriers count both CTAs' copies: wait for them to land.
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_parity[s] >= 0)
+            mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>(issued_parity[s]), never,
+                              nullptr, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (leader && lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(PM, 256);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      Tile tl;
+      int64_t local = 0;
+      for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl);
+           t += n_pairs, ++local) {
+        const int buf = static_cast<int>(local & 1);
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        if (!mbar_wait_bounded(smem_u32(&tempty[buf]), (use & 1u) ^ 1u, abort_flag, args.status,
+                               kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_acc = tmem_base + static_cast<uint32_t>(buf * 256);
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, args.status,
+                                 kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_base + stage * STAGE_BYTES;
+          const uint64_t a_desc = sw128_kmajor_desc(sA);
+          const uint64_t b_desc = sw128_kmajor_desc(sA + A_BYTES);
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j)
+            tc_mma_bf16_pair(d_acc, a_desc + 2 * j, b_desc + 2 * j, idesc,
+                             (kb > 0 || j > 0) ? 1u : 0u);
+          tc_commit_pair(smem_u32(&empty[stage]), 0x3);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_pair(smem_u32(&tfull[buf]), 0x3);
+      }
+      if (!ok) {
+        tc_commit_pair(smem_u32(drain), 0x1);
+        mbar_wait_bounded(smem_u32(drain), 0, never, nullptr, kDrainLimitNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    uint32_t* stg = epi + (warp - 2) * EPI_WARP_WORDS;
+    Tile tl;
+    int64_t local = 0;
+    for (int64_t t = pair_id; pair_tile(s_tp, s_off, G, n_tiles, t, tl); t += n_pairs, ++local) {
+      const int buf = static_cast<int>(local & 1);
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      bool ready = true;
+      if (lane == 0)
+        ready = mbar_wait_bounded(smem_u32(&tfull[buf]), use & 1u, abort_flag, args.status,
+                                  kWaitLimitNs);
+      ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+      if (!ready) break;
+      tc_fence_after();
+      const int64_t row0 = static_cast<int64_t>(tl.seg_start) + tl.m * PM + rank * BM + q * 32;
+      const int64_t row_end = tl.seg_end < args.out_rows ? tl.seg_end : args.out_rows;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(buf * 256);
+      if (SWIGLU) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t gr[32], ur[32];
+          tmem_ld32x2(taddr + c * 32, taddr + 128 + c * 32, gr, ur);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int e = 8 * v + 2 * i;
+              w4[i] = pack_bf16x2(silu(__uint_as_float(gr[e])) * __uint_as_float(ur[e]),
+                                  silu(__uint_as_float(gr[e + 1])) * __uint_as_float(ur[e + 1]));
+            }
+            *reinterpret_cast<uint4*>(stg + lane * EPI_LD + 4 * v) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+          __syncwarp();
+          // four lanes per row (16 bytes each), eight rows per pass
+#pragma unroll
+          for (int pass = 0; pass < 4; ++pass) {
+            const int r = pass * 8 + lane / 4;
+            const int64_t row = row0 + r;
+            const int col = tl.n * 128 + c * 32 + (lane % 4) * 8;
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + r * EPI_LD + (lane % 4) * 4);
+            if (row < row_end && col + 8 <= args.n_out)
+              *reinterpret_cast<uint4*>(out + row * args.ldo + col) = val;
+          }
+          __syncwarp();
+        }
+      } else {
+        float* out = static_cast<float*>(args.out);
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t ar[32];
+          tmem_ld32(taddr + c * 32, ar);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<uint4*>(stg + lane * EPI_LD + 4 * v) =
+                make_uint4(ar[4 * v], ar[4 * v + 1], ar[4 * v + 2], ar[4 * v + 3]);
+          __syncwarp();
+          // eight lanes per row (16 bytes each), four rows per pass
+#pragma unroll
+          for (int pass = 0; pass < 8; ++pass) {
+            const int r = pass * 4 + lane / 8;
+            const int64_t row = row0 + r;
+            const int col = tl.n * 256 + c * 32 + (lane % 8) * 4;
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + r * EPI_LD + (lane % 8) * 4);
+            if (row < row_end && col + 4 <= args.n_out)
+              *reinterpret_cast<uint4*>(out + row * args.ldo + col) = val;
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync_all();   // no CTA leaves while its partner may still use its memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+int sm_count_pair() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n >= 2 ? n : 2;
+}
+
+size_t pair_smem_bytes(int groups) {
+  return 1024 + STAGES * STAGE_BYTES + EPI_BYTES + 8 * (2 * STAGES + 5) + 16 +
+         8 * (static_cast<size_t>(groups) + 1) + 64;
+}
+
+template <bool SWIGLU>
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                        const PairArgs& args, int64_t max_pair_tiles, cudaStream_t s) {
+  if (max_pair_tiles <= 0) return cudaSuccess;
+  const size_t smem = pair_smem_bytes(args.offsets ? args.groups : 1);
+  auto kern = tc_pair_gemm<SWIGLU>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int64_t pairs_max = sm_count_pair() / 2;
+  const int64_t pairs = max_pair_tiles < pairs_max ? max_pair_tiles : pairs_max;
+  kern<<<static_cast<unsigned>(2 * pairs), THREADS, smem, s>>>(a, b0, b1, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
+  const bool dense = p.offsets == nullptr;
+  const int64_t rows_cap = p.a_rows;
+  if (rows_cap == 0 || (dense && p.dense_rows == 0)) return cudaSuccess;
+  const int64_t mt_ub = dense ? (p.dense_rows + PM - 1) / PM : (rows_cap + PM - 1) / PM + p.groups;
+
+  CUtensorMap mA, mG, mU, mH, mD;
+  if (!make_bf16_map(&mA, p.A, p.d, rows_cap, BM) ||
+      !make_bf16_map(&mG, p.W_gate, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
+      !make_bf16_map(&mU, p.W_up, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
+      !make_bf16_map(&mH, p.h, p.width, rows_cap, BM) ||
+      !make_bf16_map(&mD, p.W_down, p.width, static_cast<uint64_t>(p.groups) * p.d, 128))
+    return cudaErrorInvalidValue;
+
+  PairArgs a{};
+  a.offsets = p.offsets;
+  a.dense_rows = static_cast<int32_t>(p.dense_rows);
+  a.groups = p.groups;
+  a.out_rows = rows_cap;
+  a.status = p.status;
+
+  a.k_dim = p.d;
+  a.n_out = p.width;
+  a.b_rows_per_group = p.width;
+  a.out = p.h;
+  a.ldo = p.width;
+  cudaError_t e = launch_pair<true>(mA, mG, mU, a, mt_ub * ((p.width + 127) / 128), s);
+  if (e != cudaSuccess) return e;
+
+  a.k_dim = p.width;
+  a.n_out = p.d;
+  a.b_rows_per_group = p.d;
+  a.out = p.out;
+  a.ldo = p.d;
+  return launch_pair<false>(mH, mD, mD, a, mt_ub * ((p.d + 255) / 256), s);
+}
+
+}  // namespace moe

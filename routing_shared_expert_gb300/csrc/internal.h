@@ -48,6 +48,12 @@ struct RouteParams {
   int32_t* status;
 };
 cudaError_t launch_route(const RouteParams& p, int32_t dtype, cudaStream_t s);
+// bf16 router on the tensor cores (route_tc.cu); launch_route dispatches to it.
+cudaError_t launch_route_tc(const RouteParams& p, cudaStream_t s);
+
+// 2-D bf16 tensor map of a dense row-major [rows][inner] tensor: box 64 x box_rows,
+// 128-byte swizzle, zero fill out of bounds.  False if the driver rejects it.
+bool make_bf16_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 
 // ---- counting, capacity, permutation ----------------------------------------
 struct PermuteParams {
@@ -99,7 +105,13 @@ struct MlpParams {
   float* out;                 // [a_rows][d] fp32
   int32_t* status;
 };
-cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s);
+cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s);        // 1-SM, 128-row tiles
+cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s);   // CTA pairs, 256-row tiles
+
+// Tile shape choice for the bf16 expert GEMMs: 256-row pair tiles pay off when
+// segments are long; short segments (a few hundred rows per expert) waste less
+// on 128-row tiles.
+inline bool use_pair_tiles(int64_t rows, int32_t groups) { return rows >= 384LL * groups; }
 cudaError_t launch_mlp_f32(const MlpParams& p, cudaStream_t s);
 
 // ---- combine -------------------------------------------------------------------

@@ -7,7 +7,8 @@
 // the selected logits, learned sigmoid shared gate) and Section 21 "Merging
 // Routed and Shared Expert Activations" (Eq. 80 coefficients r and s).
 //
-// One CTA handles 32 tokens.  Phase 1 computes the fp32 logits of its tokens for
+// This file holds the CUDA-core router, used for fp32 layers (bf16 layers use the
+// tensor-core router in route_tc.cu).  One CTA handles 32 tokens.  Phase 1 computes the fp32 logits of its tokens for
 // all N experts (plus the shared-gate column w_s when the layer has one) with a
 // register-tiled dot product over d staged through shared memory.  Phase 2 gives
 // each warp four tokens: the warp holds a token's N logits (8 per lane at most),
@@ -226,7 +227,7 @@ cudaError_t launch_dt(const RouteParams& p, cudaStream_t s) {
 
 cudaError_t launch_route(const RouteParams& p, int32_t dtype, cudaStream_t s) {
   if (p.T == 0) return cudaSuccess;
-  return dtype == MOE_F32 ? launch_dt<float>(p, s) : launch_dt<__nv_bfloat16>(p, s);
+  return dtype == MOE_F32 ? launch_dt<float>(p, s) : launch_route_tc(p, s);
 }
 
 }  // namespace moe

@@ -1,0 +1,309 @@
+// Router on the tensor cores for bf16 layers: logits, scores, top-K and coefficients.
+//
+// Same step as route.cu (Section 10 "Routing, Capacity, and Load Balancing",
+// Table 16 and Eq. 35; Appendix E "Expert-Merge Normalization in Public MoE
+// Models", Table 52; Section 21, Eq. 80 coefficients), organised for sm_103a:
+//   - one CTA per 128 tokens; warp 0 streams x and W_router K-blocks with TMA
+//     (128-byte swizzle) through a shared-memory ring, warp 1 issues
+//     tcgen05.mma (M = 128 tokens, N = N rounded up to 16, fp32 accumulators in
+//     TMEM), plus an N = 16 MMA against the shared-gate vector w_s when the layer
+//     has a learned shared gate (its logit lands in TMEM column N_pad);
+//   - warps 2-5 read the accumulators with tcgen05.ld, one token row per
+//     thread, so the selection runs in registers: a sorted top-8 list with
+//     strict comparisons (an equal later expert never displaces an earlier one,
+//     which gives the lower-index tie rule), then the scores of the selected
+//     experts, the selected weights and r = alpha * w.
+// Every wait is bounded; a wait that runs out records MOE_ERR_TIMEOUT.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int G_BYTES = 16 * BK * 2;
+constexpr int SMEM_RING = 200 * 1024;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+
+struct RouteTcArgs {
+  RouteParams p;
+  int32_t n_pad;       // N rounded up to 16
+  int32_t gated;       // 1 when the shared gate column is computed
+  int32_t stages;
+  int32_t stage_bytes;
+};
+
+__global__ void __launch_bounds__(THREADS, 1)
+    route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                    const __grid_constant__ CUtensorMap tmG, const RouteTcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const RouteParams& p = a.p;
+  const int S = a.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * a.stage_bytes);
+  uint64_t* empty = full + 8;
+  uint64_t* acc_full = empty + 8;
+  uint64_t* drain = acc_full + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* never = const_cast<int*>(abort_flag) + 1;
+  float* s_bias = reinterpret_cast<float*>(never + 1);   // [kMaxExperts]
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int k_blocks = (p.d + BK - 1) / BK;
+  const uint32_t smem_base = smem_u32(smem);
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * BM;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(acc_full), 1);
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    *never = 0;
+    mbar_fence_init();
+  }
+  for (int i = threadIdx.x; i < p.N; i += THREADS) s_bias[i] = p.router_bias ? p.router_bias[i] : 0.f;
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmX);
+    tma_prefetch_map(&tmW);
+    if (a.gated) tma_prefetch_map(&tmG);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const uint32_t tx_bytes = static_cast<uint32_t>(A_BYTES + a.n_pad * BK * 2 + (a.gated ? G_BYTES : 0));
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued_parity[8];
+      for (int s = 0; s < 8; ++s) issued_parity[s] = -1;
+      bool ok = true;
+      for (int kb = 0; kb < k_blocks; ++kb) {
+        if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p.status,
+                               kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full[stage]);
+        mbar_arrive_expect_tx(fb, tx_bytes);
+        const uint32_t sA = smem_base + stage * a.stage_bytes;
+        const uint32_t sB = sA + A_BYTES;
+        tma_load_2d(sA, &tmX, kb * BK, static_cast<int32_t>(t0), fb);
+        tma_load_2d(sB, &tmW, kb * BK, 0, fb);
+        if (a.gated) tma_load_2d(sB + a.n_pad * BK * 2, &tmG, kb * BK, 0, fb);
+        issued_parity[stage] = static_cast<int>(phase);
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok)
+        for (int s = 0; s < S; ++s)
+          if (issued_parity[s] >= 0)
+            mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>(issued_parity[s]), never,
+                              nullptr, kDrainLimitNs);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, a.n_pad);
+      const uint32_t idesc_g = idesc_bf16_f32(BM, 16);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = 0; kb < k_blocks; ++kb) {
+        if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, p.status, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sA = smem_base + stage * a.stage_bytes;
+        const uint32_t sB = sA + A_BYTES;
+        const uint64_t a_desc = sw128_kmajor_desc(sA);
+        const uint64_t b_desc = sw128_kmajor_desc(sB);
+        const uint64_t g_desc = sw128_kmajor_desc(sB + a.n_pad * BK * 2);
+#pragma unroll
+        for (int j = 0; j < BK / 16; ++j) {
+          const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+          tc_mma_bf16(tmem_base, a_desc + 2 * j, b_desc + 2 * j, idesc, acc);
+          if (a.gated)
+            tc_mma_bf16(tmem_base + a.n_pad, a_desc + 2 * j, g_desc + 2 * j, idesc_g, acc);
+        }
+        tc_commit(smem_u32(&empty[stage]));
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+      if (ok) {
+        tc_commit(smem_u32(acc_full));
+      } else {
+        tc_commit(smem_u32(drain));
+        mbar_wait_bounded(smem_u32(drain), 0, never, nullptr, kDrainLimitNs);
+      }
+    }
+  } else {
+    // ---------------- epilogue: one token row per thread ----------------
+    const int q = warp & 3;
+    bool ready = true;
+    if (lane == 0)
+      ready = mbar_wait_bounded(smem_u32(acc_full), 0, abort_flag, p.status, kWaitLimitNs);
+    ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+    if (ready) {
+      tc_fence_after();
+      const int64_t t = t0 + q * 32 + lane;
+      const bool valid = t < p.T;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      constexpr int EMPTY = 0x7fffffff;
+      float bv[kMaxTopK];
+      int bi[kMaxTopK];
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) { bv[j] = 0.f; bi[j] = EMPTY; }
+      float* lrow = (p.logits && valid) ? p.logits + t * p.N : nullptr;
+      // pass 1: keys, logits output, top-8 list
+      for (int c0 = 0; c0 < p.N; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c0, r);
+        float z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = __uint_as_float(r[i]) + (c0 + i < p.N ? s_bias[c0 + i] : 0.f);
+        if (lrow) {
+          if (c0 + 32 <= p.N && (p.N & 3) == 0 && (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              *reinterpret_cast<float4*>(lrow + c0 + 4 * v) =
+                  make_float4(z[4 * v], z[4 * v + 1], z[4 * v + 2], z[4 * v + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c0 + i < p.N) lrow[c0 + i] = z[i];
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (c0 + i >= p.N) break;
+          float cv = z[i];
+          int ci = c0 + i;
+          if (bi[kMaxTopK - 1] == EMPTY || cv > bv[kMaxTopK - 1]) {
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+              const bool take = bi[j] == EMPTY || cv > bv[j];
+              const float tv = take ? bv[j] : cv;
+              const int ti = take ? bi[j] : ci;
+              bv[j] = take ? cv : bv[j];
+              bi[j] = take ? ci : bi[j];
+              cv = tv;
+              ci = ti;
+            }
+          }
+        }
+      }
+      // scores and weights of the selected experts
+      float w[kMaxTopK];
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) w[j] = 0.f;
+      if (p.norm == MOE_NORM_SOFTMAX_SELECTED) {
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+          if (j < p.K) { w[j] = expf(bv[j] - bv[0]); s += w[j]; }
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+          if (j < p.K) w[j] /= s;
+      } else {
+        if (p.score == MOE_SCORE_SOFTMAX) {
+          // pass 2: softmax denominator over all N experts (the maximum is bv[0])
+          const float m = bv[0];
+          float s = 0.f;
+          for (int c0 = 0; c0 < p.N; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c0, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c0 + i < p.N) s += expf(__uint_as_float(r[i]) + s_bias[c0 + i] - m);
+          }
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j)
+            if (j < p.K) w[j] = expf(bv[j] - m) / s;
+        } else {
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j)
+            if (j < p.K) w[j] = 1.f / (1.f + expf(-bv[j]));
+        }
+        if (p.norm == MOE_NORM_L1_SELECTED) {
+          float s = 0.f;
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j)
+            if (j < p.K) s += w[j];
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j)
+            if (j < p.K) w[j] /= s;
+        }
+      }
+      float shared = 0.f;
+      if (p.shared_mode == MOE_SHARED_CONST) {
+        shared = p.shared_gain;
+      } else if (p.shared_mode == MOE_SHARED_SIGMOID_GATE) {
+        uint32_t r[32];
+        tmem_ld32(taddr + a.n_pad, r);
+        shared = 1.f / (1.f + expf(-__uint_as_float(r[0])));
+      }
+      if (valid) {
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+          if (j < p.K) {
+            p.topk_idx[t * p.K + j] = bi[j];
+            p.topk_w[t * p.K + j] = p.alpha * w[j];
+          }
+        if (p.shared_coef) p.shared_coef[t] = shared;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route_tc(const RouteParams& p, cudaStream_t s) {
+  if (p.T == 0) return cudaSuccess;
+  const bool gated = p.shared_mode == MOE_SHARED_SIGMOID_GATE;
+  const int n_pad = (p.N + 15) / 16 * 16;
+  CUtensorMap mX, mW, mG;
+  if (!make_bf16_map(&mX, p.x, p.d, p.T, BM) || !make_bf16_map(&mW, p.W_router, p.d, p.N, n_pad))
+    return cudaErrorInvalidValue;
+  if (gated) {
+    if (!make_bf16_map(&mG, p.shared_gate_w, p.d, 1, 16)) return cudaErrorInvalidValue;
+  } else {
+    mG = mW;
+  }
+  RouteTcArgs a{};
+  a.p = p;
+  a.n_pad = n_pad;
+  a.gated = gated ? 1 : 0;
+  a.stage_bytes = A_BYTES + n_pad * BK * 2 + (gated ? G_BYTES : 0);
+  a.stages = SMEM_RING / a.stage_bytes;
+  if (a.stages > 8) a.stages = 8;
+  if (a.stages < 2) a.stages = 2;
+  const size_t smem = 1024 + static_cast<size_t>(a.stages) * a.stage_bytes + 8 * 20 + 16 +
+                      sizeof(float) * kMaxExperts + 64;
+  cudaError_t e = cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>((p.T + BM - 1) / BM);
+  route_tc_kernel<<<grid, THREADS, smem, s>>>(mX, mW, mG, a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

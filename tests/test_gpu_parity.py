@@ -40,6 +40,10 @@ SMALL = {
                                   logit_bias="zipf1.2"),
     "mixtral_tightcap": C["mixtral"].replace(T=700, d_model=4096, d_expert=256,
                                              capacity_factor=0.6),
+    # long segments (>= 384 rows per expert): the expert GEMMs take 256-row CTA-pair tiles
+    "pair_s": C["olmo"].replace(T=1100, d_model=448, N=4, K=2, alpha=2.0, d_expert=320,
+                                d_shared=192),
+    "pair_cap_s": C["mixtral"].replace(T=1600, d_model=4096, d_expert=448, capacity_factor=1.0),
 }
 
 
@@ -69,7 +73,7 @@ def test_layer_small(name):
         assert rt.drops["dropped_routes"] > 0, "capacity case should drop routes"
 
 
-@pytest.mark.parametrize("name", ["olmo_s", "mixtral_s", "tiny", "qwen2_s"])
+@pytest.mark.parametrize("name", ["olmo_s", "mixtral_s", "tiny", "qwen2_s", "pair_s"])
 def test_staged_entry_points_equal_fused(name):
     spec, inp = _spec_and_inputs(name)
     a = run_layer(spec, inp)
