@@ -157,9 +157,10 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* W_router,
  * (Section 10.1, Eq. 19-21; Section 10.3, Eq. 23, 25, 26, 27).
  *   x [T][d]; topk_idx [T][K] as produced by moe_route (values in [0, N)).
  * Out: counts_req [N], counts_keep [N], offsets [N+1], route_pos [T][K], perm_src [K*T],
- *   x_perm [K*T][d] (rows [0, offsets[N]) hold x[perm_src[row]], the rest unspecified),
- *   R_req / R_keep [num_ranks], drop_stats [4].  counts_req, R_req, R_keep and drop_stats may
- *   be NULL; the others are required.
+ *   R_req / R_keep [num_ranks], drop_stats [4], and optionally x_perm [K*T][d] (rows
+ *   [0, offsets[N]) hold x[perm_src[row]], the rest unspecified).  counts_req, R_req, R_keep,
+ *   drop_stats and x_perm may be NULL; without x_perm no rows are copied and x may be NULL
+ *   (moe_grouped_swiglu can read the rows of x through perm_src instead).
  * Within one expert, packed rows ascend with the token index.  Deterministic. */
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
                        int32_t* counts_req, int32_t* counts_keep, int32_t* offsets,
@@ -186,14 +187,20 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32
                                cudaStream_t stream);
 
 /* Routed experts over densely packed segments (Section 20.1 Eq. 74 per segment; Section 10.3,
- * Eq. 26: rows [offsets[e], offsets[e+1]) of x_perm belong to expert e, nothing else is computed).
- *   x_perm [K*T][d]; offsets [N+1] (device; read on the device, never copied to the host).
- * Out: f [K*T][d] fp32: f[row] = SwiGLU_e(x_perm[row]) for rows < offsets[N].
+ * Eq. 26: packed rows [offsets[e], offsets[e+1]) belong to expert e, nothing else is computed).
+ *   offsets [N+1] (device; read on the device, never copied to the host).
+ *   perm_src NULL:  x_rows is x_perm [K*T][d], packed row r is x_rows[r].
+ *   perm_src [K*T]: x_rows is x [T][d] and packed row r is x[perm_src[r]]; the rows are
+ *                   gathered inside the GEMM's operand load, so no K*T x d buffer is
+ *                   needed.  Same results bit for bit; on a GB300 this form measured about
+ *                   2.7x slower on bf16 layers (32 four-row TMA gathers per K step), so
+ *                   moe_layer_forward uses the packed form.
+ * Out: f [K*T][d] fp32: f[row] = SwiGLU_e(packed row) for rows < offsets[N].
  * The intermediate h = SiLU(x W_g) * (x W_u) is kept in the workspace (dtype). */
-moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
-                              const void* W_gate, const void* W_up, const void* W_down,
-                              void* f, void* workspace, size_t workspace_bytes,
-                              cudaStream_t stream);
+moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_rows, const int32_t* offsets,
+                              const int32_t* perm_src, const void* W_gate, const void* W_up,
+                              const void* W_down, void* f, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
 
 /* The one (merged) shared expert over all tokens (Section 20.1, Eq. 74-76).
  *   x [T][d]; Ws_gate, Ws_up [d_shared][d]; Ws_down [d][d_shared].

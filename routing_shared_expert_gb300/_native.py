@@ -68,7 +68,7 @@ def _load():
         "moe_route": ([C, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
         "moe_permute": ([C, P, P, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
         "moe_permute_noalloc": ([C, P, P, P, P, P, P, P, P, P, P, P, P], c_int32),
-        "moe_grouped_swiglu": ([C, P, P, P, P, P, P, P, c_size_t, P], c_int32),
+        "moe_grouped_swiglu": ([C, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
         "moe_shared_mlp": ([C, P, P, P, P, P, P, c_size_t, P], c_int32),
         "moe_combine": ([C, P, P, P, P, P, P, P], c_int32),
         "moe_layer_forward": ([C, POINTER(moe_weights), P, POINTER(moe_outputs), P, c_size_t, P], c_int32),
@@ -189,10 +189,12 @@ def moe_permute_noalloc(cfg, x, topk_idx, counts_req, counts_keep, offsets, rout
         _ptr(drop_stats), _stream(stream)))
 
 
-def moe_grouped_swiglu(cfg, x_perm, offsets, W_gate, W_up, W_down, f, workspace, stream=None):
+def moe_grouped_swiglu(cfg, x_rows, offsets, perm_src, W_gate, W_up, W_down, f, workspace,
+                       stream=None):
+    """x_rows is x_perm when perm_src is None, else x (rows gathered through perm_src)."""
     _check("moe_grouped_swiglu", _lib.moe_grouped_swiglu(
-        ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
-        _ptr(f), _ptr(workspace), workspace.numel(), _stream(stream)))
+        ctypes.byref(cfg), _ptr(x_rows), _ptr(offsets), _ptr(perm_src), _ptr(W_gate), _ptr(W_up),
+        _ptr(W_down), _ptr(f), _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def moe_shared_mlp(cfg, x, Ws_gate, Ws_up, Ws_down, g, workspace, stream=None):

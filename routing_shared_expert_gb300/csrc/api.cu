@@ -108,8 +108,8 @@ struct PermOut {
 
 moe_status do_permute(const moe_config& c, const Layout& L, void* ws, const void* x,
                       const int32_t* topk_idx, const PermOut& o, cudaStream_t st) {
-  if (c.T > 0 && (!x || !topk_idx || !o.route_pos || !o.perm_src || !o.x_perm))
-    return MOE_ERR_INVALID_ARG;
+  if (c.T > 0 && (!topk_idx || !o.route_pos || !o.perm_src)) return MOE_ERR_INVALID_ARG;
+  if (c.T > 0 && o.x_perm && !x) return MOE_ERR_INVALID_ARG;
   if (!o.counts_keep || !o.offsets) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(o.x_perm)) return MOE_ERR_MISALIGNED;
   PermuteParams p{};
@@ -140,13 +140,14 @@ moe_status do_permute(const moe_config& c, const Layout& L, void* ws, const void
   return cuda_status(launch_permute(p, st));
 }
 
-moe_status do_grouped(const moe_config& c, const Layout& L, void* ws, const void* x_perm,
-                      const int32_t* offsets, const void* Wg, const void* Wu, const void* Wd,
-                      void* f, bool tile_prefix_ready, cudaStream_t st) {
+moe_status do_grouped(const moe_config& c, const Layout& L, void* ws, const void* x_rows,
+                      const int32_t* offsets, const int32_t* perm_src, const void* Wg,
+                      const void* Wu, const void* Wd, void* f, bool tile_prefix_ready,
+                      cudaStream_t st) {
   if (!offsets) return MOE_ERR_INVALID_ARG;
   if (c.T == 0) return MOE_OK;
-  if (!x_perm || !Wg || !Wu || !Wd || !f) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x_perm) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(f))
+  if (!x_rows || !Wg || !Wu || !Wd || !f) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_rows) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(f))
     return MOE_ERR_MISALIGNED;
   int32_t* status = at<int32_t>(ws, L.status);
   int32_t* tp = at<int32_t>(ws, L.tile_prefix);
@@ -155,8 +156,10 @@ moe_status do_grouped(const moe_config& c, const Layout& L, void* ws, const void
     if (s != MOE_OK) return s;
   }
   MlpParams p{};
-  p.A = x_perm;
+  p.A = x_rows;
   p.a_rows = c.T * c.K;
+  p.gather_src = perm_src;
+  p.src_rows = c.T;
   p.offsets = offsets;
   p.tile_prefix = tp;
   p.groups = c.N;
@@ -324,14 +327,16 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
   return do_permute(*cfg, L, workspace, x, topk_idx, o, stream);
 }
 
-moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
-                              const void* W_gate, const void* W_up, const void* W_down, void* f,
-                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_rows, const int32_t* offsets,
+                              const int32_t* perm_src, const void* W_gate, const void* W_up,
+                              const void* W_down, void* f, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
   moe_status s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   Layout L;
   if ((s = check_ws(*cfg, workspace, workspace_bytes, &L)) != MOE_OK) return s;
-  return do_grouped(*cfg, L, workspace, x_perm, offsets, W_gate, W_up, W_down, f, false, stream);
+  return do_grouped(*cfg, L, workspace, x_rows, offsets, perm_src, W_gate, W_up, W_down, f, false,
+                    stream);
 }
 
 moe_status moe_shared_mlp(const moe_config* cfg, const void* x, const void* Ws_gate,
@@ -380,8 +385,10 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
              at<void>(ws, L.x_perm)};
   if ((s = do_permute(c, L, ws, x, idx, po, stream)) != MOE_OK) return s;
   void* f = at<void>(ws, L.f);
-  if ((s = do_grouped(c, L, ws, po.x_perm, po.offsets, w->W_gate, w->W_up, w->W_down, f, true,
-                      stream)) != MOE_OK)
+  // Packed rows: one copy pass, then plain tile loads in the GEMM (a gathered A-load
+  // through perm_src needs 32 four-row TMA gathers per stage and runs far slower).
+  if ((s = do_grouped(c, L, ws, po.x_perm, po.offsets, nullptr, w->W_gate, w->W_up, w->W_down, f,
+                      true, stream)) != MOE_OK)
     return s;
   void* g = nullptr;
   if (c.d_shared > 0) {

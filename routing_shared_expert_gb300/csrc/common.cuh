@@ -115,6 +115,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const CUtensorMap
       : "memory");
 }
 
+// Gather of four rows (row indices r0..r3, 64 elements from column c0 each) of a
+// 2-D tensor whose map has a one-row box; the rows land 128 bytes apart at
+// smem_dst with the map's swizzle, completing on an mbarrier of this CTA.
+__device__ __forceinline__ void tma_gather4(uint32_t smem_dst, const CUtensorMap* map, int32_t c0,
+                                            const int32_t (&r)[4], uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]),
+      "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -253,6 +266,37 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const CUtens
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
+}
+
+// Four-row gather (see tma_gather4) completing on an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_gather4_pair(uint32_t smem_dst, const CUtensorMap* map, int32_t c0,
+                                                 const int32_t (&r)[4], uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]),
+      "r"(bar)
+      : "memory");
+}
+
+// Source rows of four consecutive packed rows starting at `row` (gathered GEMM A-load).
+// Rows past the segment (or the table) read the segment's first row; their results
+// are never stored.  A source index outside [0, src_rows) is reported and replaced by 0.
+__device__ __forceinline__ void gather_rows4(const int32_t* src, int64_t cap, int64_t row,
+                                             int64_t seg_start, int64_t seg_end, int64_t src_rows,
+                                             int32_t* status, int32_t (&r)[4]) {
+  const int64_t fallback = seg_start < cap ? seg_start : -1;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t pr = row + i;
+    const int64_t at = (pr < seg_end && pr < cap) ? pr : fallback;
+    int32_t v = at >= 0 ? src[at] : 0;
+    if (v < 0 || v >= src_rows) {
+      set_status(status, MOE_ERR_DEVICE_BOUNDS);
+      v = 0;
+    }
+    r[i] = v;
+  }
 }
 
 // One warp in each CTA of the pair allocates together; each CTA receives the address.

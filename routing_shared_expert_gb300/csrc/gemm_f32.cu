@@ -20,7 +20,9 @@ constexpr int KC = 32;    // K chunk
 constexpr int THREADS = 256;
 
 struct F32Args {
-  const float* A;            // [rows][k_dim]
+  const float* A;            // [rows][k_dim], or x when gathering
+  const int32_t* gather_src; // packed row -> row of x, or nullptr
+  int64_t src_rows;
   const int32_t* offsets;    // [groups+1] or nullptr (dense)
   int32_t groups;
   int64_t dense_rows;
@@ -79,7 +81,19 @@ __global__ void __launch_bounds__(THREADS) f32_mlp_kernel(F32Args a) {
     for (int i = threadIdx.x; i < RB * KC; i += THREADS) {
       const int r = i / KC, c = i % KC;
       const int64_t row = r0 + r;
-      As[r][c] = (row < rend && k0 + c < a.k_dim) ? a.A[row * a.k_dim + k0 + c] : 0.f;
+      float v = 0.f;
+      if (row < rend && k0 + c < a.k_dim) {
+        int64_t src = row;
+        if (a.gather_src) {
+          src = a.gather_src[row];
+          if (src < 0 || src >= a.src_rows) {
+            set_status(a.status, MOE_ERR_DEVICE_BOUNDS);
+            src = -1;
+          }
+        }
+        if (src >= 0) v = a.A[src * a.k_dim + k0 + c];
+      }
+      As[r][c] = v;
     }
     for (int i = threadIdx.x; i < CB * KC; i += THREADS) {
       const int r = i / KC, c = i % KC;
@@ -135,6 +149,8 @@ cudaError_t launch_mlp_f32(const MlpParams& p, cudaStream_t s) {
   a.status = p.status;
 
   a.A = static_cast<const float*>(p.A);
+  a.gather_src = p.gather_src;
+  a.src_rows = p.src_rows;
   a.k_dim = p.d;
   a.n_out = p.width;
   a.B0 = static_cast<const float*>(p.W_gate);
@@ -146,6 +162,7 @@ cudaError_t launch_mlp_f32(const MlpParams& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
 
   a.A = static_cast<const float*>(p.h);
+  a.gather_src = nullptr;
   a.k_dim = p.width;
   a.n_out = p.d;
   a.B0 = static_cast<const float*>(p.W_down);

@@ -57,6 +57,9 @@ struct TcArgs {
   void* out;                   // SwiGLU mode: bf16 h; plain mode: fp32 f
   int64_t ldo;
   int32_t* status;
+  const int32_t* gather_src;   // non-null: A rows are gathered from x through this table
+  int64_t gather_cap;
+  int64_t src_rows;
 };
 
 struct Tile {
@@ -151,42 +154,54 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued_parity[STAGES];
+    // Lane 0 waits for free stages, arms the barrier and loads B (and A when A is
+    // packed); when A is gathered every lane loads four of the tile's 128 rows.
+    const bool gather = args.gather_src != nullptr;
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued_parity[STAGES];
 #pragma unroll
-      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
-      bool ok = true;
-      Tile tl;
-      for (int64_t t = blockIdx.x; ok && tile_coords(args, s_tp, s_off, n_tiles, t, tl);
-           t += gridDim.x) {
-        const int a_row = tl.seg_start + tl.m * BM;
-        const int b_row = tl.g * args.b_rows_per_group + tl.n * BN_OUT;
-        for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
-                                 kWaitLimitNs)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = smem_u32(&full[stage]);
+    for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+    bool ok = true;
+    Tile tl;
+    for (int64_t t = blockIdx.x; (gather || lane == 0) && ok && tile_coords(args, s_tp, s_off, n_tiles, t, tl);
+         t += gridDim.x) {
+      const int a_row = tl.seg_start + tl.m * BM;
+      const int b_row = tl.g * args.b_rows_per_group + tl.n * BN_OUT;
+      int32_t src[4] = {0, 0, 0, 0};
+      if (gather)
+        gather_rows4(args.gather_src, args.gather_cap, a_row + 4 * lane, tl.seg_start, tl.seg_end,
+                     args.src_rows, args.status, src);
+      for (int kb = 0; kb < k_blocks; ++kb) {
+        bool go = true;
+        if (lane == 0)
+          go = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
+                                 kWaitLimitNs);
+        if (gather) go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+        if (!go) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full[stage]);
+        const uint32_t sA = smem_base + stage * STAGE_BYTES;
+        const uint32_t sB = sA + A_BYTES;
+        if (lane == 0) {
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          const uint32_t sA = smem_base + stage * STAGE_BYTES;
-          const uint32_t sB = sA + A_BYTES;
-          tma_load_2d(sA, &tmA, kb * BK, a_row, fb);
+          if (!gather) tma_load_2d(sA, &tmA, kb * BK, a_row, fb);
           tma_load_2d(sB, &tmB0, kb * BK, b_row, fb);
           if (SWIGLU) tma_load_2d(sB + B_BYTES / 2, &tmB1, kb * BK, b_row, fb);
           issued_parity[stage] = static_cast<int>(phase);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
+        if (gather) tma_gather4(sA + lane * 512, &tmA, kb * BK, src, fb);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
-      if (!ok) {
-        // Let every copy this thread started land before the CTA can exit.
-        for (int s = 0; s < STAGES; ++s)
-          if (issued_parity[s] >= 0)
-            mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>(issued_parity[s]), never,
-                              nullptr, kDrainLimitNs);
-      }
+    }
+    if (!ok && lane == 0) {
+      // Let every copy this warp started land before the CTA can exit.
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_parity[s] >= 0)
+          mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>(issued_parity[s]), never,
+                            nullptr, kDrainLimitNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -387,7 +402,8 @@ cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {
   const int64_t mt_ub = dense ? (p.dense_rows + BM - 1) / BM : (rows_cap + BM - 1) / BM + p.groups;
 
   CUtensorMap mA, mG, mU, mH, mD;
-  if (!make_bf16_map(&mA, p.A, p.d, rows_cap, BM) ||
+  const bool gather = p.gather_src != nullptr;
+  if (!make_bf16_map(&mA, p.A, p.d, gather ? p.src_rows : rows_cap, gather ? 1 : BM) ||
       !make_bf16_map(&mG, p.W_gate, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
       !make_bf16_map(&mU, p.W_up, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
       !make_bf16_map(&mH, p.h, p.width, rows_cap, BM) ||
@@ -401,6 +417,9 @@ cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {
   a.groups = p.groups;
   a.status = p.status;
   a.out_rows = rows_cap;
+  a.gather_src = p.gather_src;
+  a.gather_cap = rows_cap;
+  a.src_rows = p.src_rows;
 
   // gate/up + SiLU -> h
   a.k_dim = p.d;
@@ -411,7 +430,8 @@ cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {
   cudaError_t e = launch_one<true>(mA, mG, mU, a, mt_ub * ((p.width + 127) / 128), s);
   if (e != cudaSuccess) return e;
 
-  // down -> out
+  // down -> out (h is packed)
+  a.gather_src = nullptr;
   a.k_dim = p.width;
   a.n_out = p.d;
   a.b_rows_per_group = p.d;

@@ -16,6 +16,10 @@
 //                rows of the same 128 h columns, so TMEM columns [0,128) hold
 //                x W_g and [128,256) hold x W_u for the CTA's rows.
 //   Plain mode:  each CTA loads 128 of the 256 output columns' weight rows.
+// The gate/up A rows are either read from a packed buffer (one TMA tile load) or
+// gathered straight from x through the packed-row source table: each lane of the
+// producer warp issues one tile::gather4 of four rows, so the row permutation of
+// Section 10.3 costs no extra pass over memory.
 // Roles per CTA (192 threads): warp 0 TMA producer (both CTAs; completions are
 // counted on the even CTA's barrier), warp 1 TMEM allocation and, in the even
 // CTA only, the MMA issuer; warps 2-5 epilogue.  The epilogue stages each
@@ -55,6 +59,9 @@ struct PairArgs {
   void* out;                 // SwiGLU: bf16 h; plain: fp32 f
   int64_t ldo;
   int32_t* status;
+  const int32_t* gather_src; // non-null: A rows are gathered from x through this table
+  int64_t gather_cap;        // entries of gather_src
+  int64_t src_rows;          // rows of x
 };
 
 struct Tile {
@@ -169,42 +176,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
-    if (lane == 0) {
-      const CUtensorMap* mapB = (SWIGLU && !leader) ? &tmB1 : &tmB0;
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued_parity[STAGES];
+    // Lane 0 waits for free stages, arms the even CTA's barrier and loads B (and A when
+    // A is packed); when A is gathered every lane loads four of the 128 rows.
+    const CUtensorMap* mapB = (SWIGLU && !leader) ? &tmB1 : &tmB0;
+    const bool gather = args.gather_src != nullptr;
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued_parity[STAGES];
 #pragma unroll
-      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
-      bool ok = true;
-      Tile tl;
-      for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl); t += n_pairs) {
-        const int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * BM;
-        const int b_row = SWIGLU ? tl.g * args.b_rows_per_group + tl.n * 128
-                                 : tl.g * args.b_rows_per_group + tl.n * 256 + static_cast<int>(rank) * 128;
-        for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
-                                 kWaitLimitNs)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb_local = smem_u32(&full[stage]);
-          const uint32_t fb_leader = mapa_shared(fb_local, 0);
+    for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+    bool ok = true;
+    Tile tl;
+    for (int64_t t = pair_id; (gather || lane == 0) && ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl);
+         t += n_pairs) {
+      const int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * BM;
+      const int b_row = SWIGLU ? tl.g * args.b_rows_per_group + tl.n * 128
+                               : tl.g * args.b_rows_per_group + tl.n * 256 + static_cast<int>(rank) * 128;
+      int32_t src[4] = {0, 0, 0, 0};
+      if (gather)
+        gather_rows4(args.gather_src, args.gather_cap, a_row + 4 * lane, tl.seg_start, tl.seg_end,
+                     args.src_rows, args.status, src);
+      for (int kb = 0; kb < k_blocks; ++kb) {
+        bool go = true;
+        if (lane == 0)
+          go = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
+                                 kWaitLimitNs);
+        if (gather) go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+        if (!go) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb_local = smem_u32(&full[stage]);
+        const uint32_t fb_leader = mapa_shared(fb_local, 0);
+        const uint32_t sA = smem_base + stage * STAGE_BYTES;
+        if (lane == 0) {
           if (leader) mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
-          const uint32_t sA = smem_base + stage * STAGE_BYTES;
-          tma_load_2d_pair(sA, &tmA, kb * BK, a_row, fb_leader);
+          if (!gather) tma_load_2d_pair(sA, &tmA, kb * BK, a_row, fb_leader);
           tma_load_2d_pair(sA + A_BYTES, mapB, kb * BK, b_row, fb_leader);
           issued_parity[stage] = static_cast<int>(phase);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
+        if (gather) tma_gather4_pair(sA + lane * 512, &tmA, kb * BK, src, fb_leader);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
-      if (!ok && leader) {
-        // The even CTA's full barriers count both CTAs' copies: wait for them to land.
-        for (int s = 0; s < STAGES; ++s)
-          if (issued_parity[s] >= 0)
-            mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>(issued_parity[s]), never,
-                              nullptr, kDrainLimitNs);
-      }
+    }
+    if (!ok && leader && lane == 0) {
+      // The even CTA's full barriers count both CTAs' copies: wait for them to land.
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_parity[s] >= 0)
+          mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>(issued_parity[s]), never,
+                            nullptr, kDrainLimitNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
@@ -376,7 +396,8 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   const int64_t mt_ub = dense ? (p.dense_rows + PM - 1) / PM : (rows_cap + PM - 1) / PM + p.groups;
 
   CUtensorMap mA, mG, mU, mH, mD;
-  if (!make_bf16_map(&mA, p.A, p.d, rows_cap, BM) ||
+  const bool gather = p.gather_src != nullptr;
+  if (!make_bf16_map(&mA, p.A, p.d, gather ? p.src_rows : rows_cap, gather ? 1 : BM) ||
       !make_bf16_map(&mG, p.W_gate, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
       !make_bf16_map(&mU, p.W_up, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
       !make_bf16_map(&mH, p.h, p.width, rows_cap, BM) ||
@@ -389,6 +410,9 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.groups = p.groups;
   a.out_rows = rows_cap;
   a.status = p.status;
+  a.gather_src = p.gather_src;
+  a.gather_cap = rows_cap;
+  a.src_rows = p.src_rows;
 
   a.k_dim = p.d;
   a.n_out = p.width;
@@ -403,6 +427,7 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.b_rows_per_group = p.d;
   a.out = p.out;
   a.ldo = p.d;
+  a.gather_src = nullptr;    // h is packed
   return launch_pair<false>(mH, mD, mD, a, mt_ub * ((p.d + 255) / 256), s);
 }
 

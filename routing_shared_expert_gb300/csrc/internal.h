@@ -90,8 +90,10 @@ cudaError_t launch_tile_prefix(const int32_t* offsets, int32_t N, int32_t* tile_
 // One grouped SwiGLU MLP over packed segments (groups = N routed experts) or over
 // one dense block of rows (groups = 1, offsets == nullptr, rows = dense_rows).
 struct MlpParams {
-  const void* A;              // [a_rows][d] input rows
-  int64_t a_rows;             // rows of the A buffer (capacity, for TMA bounds)
+  const void* A;              // [a_rows][d] input rows, or x [src_rows][d] when gathering
+  int64_t a_rows;             // packed rows (capacity of h and out, and of gather_src)
+  const int32_t* gather_src;  // [a_rows] source row of each packed row, or nullptr (A is packed)
+  int64_t src_rows;           // rows of x when gathering
   const int32_t* offsets;     // [groups+1] device, or nullptr for one dense group
   const int32_t* tile_prefix; // [groups+1] device, or nullptr for one dense group
   int64_t dense_rows;

@@ -11,10 +11,12 @@
 //   2. scan    - one CTA: per-expert exclusive prefix over tiles (C^req falls out),
 //                the capacity rule (C^keep), offsets, destination totals, the
 //                m-tile prefix the grouped GEMMs walk, and the dropped-route total.
-//   3. place   - one warp per tile: walks the tile's routes in (token, slot) order,
-//                ranks equal experts with __match_any_sync, and writes the packed
-//                position of every kept route (-1 if dropped) and its source token.
-//   4. gather  - one warp per packed row: copies x[perm_src[row]] into x_perm[row].
+//   3. place   - one CTA per tile: ranks each route among the requests to its expert
+//                in (token, slot) order (warp-level __match_any_sync, then a prefix
+//                over the tile's warps), and writes the packed position of every
+//                kept route (-1 if dropped) and its source token.
+//   4. gather  - one warp per token: copies x[t] into the packed rows of t's kept
+//                routes (only when the caller passes x_perm).
 #include "common.cuh"
 #include "internal.h"
 
@@ -116,52 +118,86 @@ __global__ void __launch_bounds__(1024) scan_kernel(PermuteParams p) {
   }
 }
 
-__global__ void __launch_bounds__(32) place_kernel(PermuteParams p) {
-  __shared__ int cnt[kMaxExperts];
+// One CTA (8 warps) per 256-token tile.  Warp w owns tokens [32w, 32w+32) of the
+// tile; its 32*K routes in (token, slot) order are ranked within the warp with
+// __match_any_sync (round k holds routes [32k, 32k+32) of the warp's range).  A
+// per-expert exclusive prefix over the warps, seeded with the routes to that
+// expert from earlier tiles, then gives every route its rank among all requests
+// to its expert in token order.
+__global__ void __launch_bounds__(256) place_kernel(PermuteParams p) {
+  __shared__ int wcnt[8][kMaxExperts];   // per-warp counts, then per-warp bases
   __shared__ int ckeep[kMaxExperts];
   __shared__ int offs[kMaxExperts];
   __shared__ int drops[kHistTile];
-  const int lane = threadIdx.x;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t tile = blockIdx.x;
-  for (int e = lane; e < p.N; e += 32) {
-    cnt[e] = p.hist[tile * p.N + e];      // routes to e from earlier tiles
+  for (int e = threadIdx.x; e < p.N; e += blockDim.x) {
     ckeep[e] = p.counts_keep[e];
     offs[e] = p.offsets[e];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) wcnt[w][e] = 0;
   }
-  for (int i = lane; i < kHistTile; i += 32) drops[i] = 0;
-  __syncwarp();
+  for (int i = threadIdx.x; i < kHistTile; i += blockDim.x) drops[i] = 0;
+  __syncthreads();
 
   const int64_t t0 = tile * kHistTile;
   const int64_t t1 = min(t0 + kHistTile, p.T);
-  const int64_t r0 = t0 * p.K, r1 = t1 * p.K;
+  const int64_t w0 = min(t0 + 32 * warp, t1), w1 = min(w0 + 32, t1);
+  const int64_t r0 = w0 * p.K, r1 = w1 * p.K;
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int64_t base = r0; base < r1; base += 32) {
-    const int64_t r = base + lane;
+  int my_e[kMaxTopK], my_rank[kMaxTopK];
+#pragma unroll
+  for (int k = 0; k < kMaxTopK; ++k) {
+    my_e[k] = -1;
+    my_rank[k] = 0;
+    if (k >= p.K) continue;
+    const int64_t r = r0 + 32 * k + lane;
     int e = -1;
     if (r < r1) {
       e = p.topk_idx[r];
       if (e < 0 || e >= p.N) e = -1;   // reported by the count kernel
     }
     const unsigned same = __match_any_sync(0xffffffffu, e);
-    const int rank_in_round = __popc(same & lt_mask);
-    const int g = (e >= 0) ? cnt[e] + rank_in_round : 0;
+    const int rank = __popc(same & lt_mask);
+    int base = 0;
+    if (e >= 0) base = wcnt[warp][e];
     __syncwarp();
-    if (e >= 0 && rank_in_round == 0) cnt[e] += __popc(same);
+    if (e >= 0 && rank == 0) wcnt[warp][e] = base + __popc(same);
     __syncwarp();
-    if (r < r1) {
-      const int64_t t = r / p.K;
-      if (e >= 0 && g < ckeep[e]) {
-        const int pos = offs[e] + g;
-        p.route_pos[r] = pos;
-        p.perm_src[pos] = static_cast<int32_t>(t);
-      } else {
-        p.route_pos[r] = -1;
-        atomicAdd(&drops[t - t0], 1);
-      }
+    my_e[k] = e;
+    my_rank[k] = base + rank;
+  }
+  __syncthreads();
+  // exclusive prefix over warps, seeded with the routes from earlier tiles
+  for (int e = threadIdx.x; e < p.N; e += blockDim.x) {
+    int run = p.hist[tile * p.N + e];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int c = wcnt[w][e];
+      wcnt[w][e] = run;
+      run += c;
     }
   }
-  __syncwarp();
-  if (p.drop_stats) {
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kMaxTopK; ++k) {
+    if (k >= p.K) continue;
+    const int64_t r = r0 + 32 * k + lane;
+    if (r >= r1) continue;
+    const int e = my_e[k];
+    const int64_t t = r / p.K;
+    const int g = e >= 0 ? wcnt[warp][e] + my_rank[k] : 0;
+    if (e >= 0 && g < ckeep[e]) {
+      const int pos = offs[e] + g;
+      p.route_pos[r] = pos;
+      p.perm_src[pos] = static_cast<int32_t>(t);
+    } else {
+      p.route_pos[r] = -1;
+      atomicAdd(&drops[t - t0], 1);
+    }
+  }
+  __syncthreads();
+  if (p.drop_stats && warp == 0) {
     int lost_any = 0, lost_all = 0;
     for (int64_t t = t0 + lane; t < t1; t += 32) {
       const int d = drops[t - t0];
@@ -180,20 +216,33 @@ __global__ void __launch_bounds__(32) place_kernel(PermuteParams p) {
   }
 }
 
+// One warp per token: each 16-byte piece of x[t] is read once and written to the
+// packed rows of all of t's kept routes.
 __global__ void __launch_bounds__(256) gather_kernel(PermuteParams p) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
-  const int64_t rows = min(static_cast<int64_t>(p.offsets[p.N]), p.T * p.K);
-  if (row >= rows) return;
-  const int32_t src = p.perm_src[row];
-  if (src < 0 || src >= p.T) {
-    set_status(p.status, MOE_ERR_DEVICE_BOUNDS);
-    return;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (t >= p.T) return;
+  const int64_t cap = p.T * p.K;
+  int64_t dst[kMaxTopK];
+  int n = 0;
+#pragma unroll
+  for (int k = 0; k < kMaxTopK; ++k) {
+    dst[k] = -1;
+    if (k < p.K) {
+      const int32_t pos = p.route_pos[t * p.K + k];
+      if (pos >= cap) set_status(p.status, MOE_ERR_DEVICE_BOUNDS);
+      else if (pos >= 0) dst[n++] = pos;
+    }
   }
   const int64_t nvec = static_cast<int64_t>(p.d) * p.elem_bytes / 16;
-  const int4* s = reinterpret_cast<const int4*>(static_cast<const char*>(p.x) + src * nvec * 16);
-  int4* dst = reinterpret_cast<int4*>(static_cast<char*>(p.x_perm) + row * nvec * 16);
-  for (int64_t v = lane; v < nvec; v += 32) dst[v] = s[v];
+  const int4* src = reinterpret_cast<const int4*>(static_cast<const char*>(p.x) + t * nvec * 16);
+  int4* out = static_cast<int4*>(p.x_perm);
+  for (int64_t v = lane; v < nvec; v += 32) {
+    const int4 val = src[v];
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k)
+      if (k < n) out[dst[k] * nvec + v] = val;
+  }
 }
 
 __global__ void tile_prefix_kernel(const int32_t* offsets, int32_t N, int32_t* tile_prefix,
@@ -225,11 +274,11 @@ cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s) {
   scan_kernel<<<1, 1024, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.T == 0) return e;
-  place_kernel<<<tiles, 32, 0, s>>>(p);
+  place_kernel<<<tiles, 256, 0, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t max_rows = p.T * p.K;
-  gather_kernel<<<static_cast<unsigned>((max_rows + 7) / 8), 256, 0, s>>>(p);
+  if (p.x_perm == nullptr) return cudaSuccess;   // the expert GEMM gathers rows itself
+  gather_kernel<<<static_cast<unsigned>((p.T + 7) / 8), 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

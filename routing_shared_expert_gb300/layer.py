@@ -94,8 +94,8 @@ class MoELayer:
                         o["route_pos"], o["perm_src"], s["x_perm"], o["R_req"], o["R_keep"],
                         o["drop_stats"], self.ws, st)
         rec(2)
-        nat.moe_grouped_swiglu(c, s["x_perm"], o["offsets"], w["W_gate"], w["W_up"], w["W_down"],
-                               s["f"], self.ws, st)
+        nat.moe_grouped_swiglu(c, s["x_perm"], o["offsets"], None, w["W_gate"], w["W_up"],
+                               w["W_down"], s["f"], self.ws, st)
         rec(3)
         if c.d_shared > 0:
             nat.moe_shared_mlp(c, x, w["Ws_gate"], w["Ws_up"], w["Ws_down"], s["g"], self.ws, st)

@@ -82,6 +82,33 @@ def test_staged_entry_points_equal_fused(name):
         assert torch.equal(a.out[k], b.out[k]), k
 
 
+@pytest.mark.parametrize("name", ["olmo_s", "pair_s", "tiny", "mixtral_tightcap"])
+def test_gathered_rows_equal_packed_rows(name):
+    """The expert GEMM reading rows of x through perm_src gives exactly what it gives on the
+    explicitly permuted copy x_perm (both tile shapes, and the fp32 path)."""
+    import routing_shared_expert_gb300 as moe
+    spec, inp = _spec_and_inputs(name)
+    layer = run_layer(spec, inp)
+    c, o = layer.cfg, layer.out
+    T, K, d = spec.T, spec.K, spec.d_model
+    x_perm = torch.zeros((T * K, d), dtype=spec.torch_dtype, device="cuda")
+    moe.moe_permute(c, inp["x"], o["topk_idx"], None, o["counts_keep"], o["offsets"],
+                    o["route_pos"], o["perm_src"], x_perm, None, None, None, layer.ws)
+    f_packed = torch.zeros((T * K, d), dtype=torch.float32, device="cuda")
+    f_gather = torch.zeros((T * K, d), dtype=torch.float32, device="cuda")
+    moe.moe_grouped_swiglu(c, x_perm, o["offsets"], None, inp["W_gate"], inp["W_up"],
+                           inp["W_down"], f_packed, layer.ws)
+    moe.moe_grouped_swiglu(c, inp["x"], o["offsets"], o["perm_src"], inp["W_gate"], inp["W_up"],
+                           inp["W_down"], f_gather, layer.ws)
+    torch.cuda.synchronize()
+    kept = int(o["offsets"][-1])
+    assert kept > 0
+    src = o["perm_src"][:kept].long()
+    assert torch.equal(x_perm[:kept], inp["x"][src])
+    assert torch.equal(f_packed[:kept], f_gather[:kept])
+    assert layer.status() == 0
+
+
 def test_equal_logits_ties_and_dense_reduction():
     """All-zero router: every token ties on every expert; selection takes 0..K-1 and, under the
     Olmo rule, r = 1, so the layer is one dense SwiGLU over the concatenated blocks (Eq. 81)."""
