@@ -109,6 +109,83 @@ def time_oracle(spec, inp_host, budget_s: float, min_tokens: int = 64):
     return S, t
 
 
+# ----------------------------------------------------------------- entropy sweep
+
+def histograms(N: int, R: int):
+    """Kept-count histograms over N experts with R routes in total (fixed work).
+
+    Families: uniform; one hot expert holding a share s of the routes ("spike");
+    three hot experts sharing s ("three-hot"), the rest spread evenly.  Pairs of
+    spike / three-hot histograms with the same maximum load are included.
+    """
+    def spread(hot):
+        rest = R - sum(hot)
+        k = N - len(hot)
+        base = [rest // k + (1 if i < rest % k else 0) for i in range(k)]
+        return hot + base
+    out = [("uniform", spread([]))]
+    for s in (0.1, 0.2, 0.3, 0.45, 0.6, 0.8):
+        out.append((f"spike s={s}", spread([int(R * s)])))
+        out.append((f"three-hot s={s}", spread([int(R * s / 3)] * 3)))
+    # same maximum load as the spike with share s: three experts at that load
+    for s in (0.1, 0.2, 0.3):
+        m = int(R * s)
+        out.append((f"three-hot max={m}", spread([m, m, m])))
+    return out
+
+
+def entropy_deficit(counts):
+    import math
+    tot = float(sum(counts))
+    H = -sum((c / tot) * math.log(c / tot) for c in counts if c > 0)
+    return 1.0 - H / math.log(len(counts))
+
+
+def sweep_entropy(args, spec):
+    """Grouped-GEMM throughput vs the kept-count entropy deficit at fixed total work
+    (Section 10.2's fixed-work microbenchmark of local expert compute)."""
+    import torch
+    import routing_shared_expert_gb300 as moe
+    from workloads import make_inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = make_inputs(spec, dev)
+    cfg = moe.config_from_spec(spec)
+    ws = moe.alloc_workspace(cfg, dev)
+    R = spec.T * spec.K
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    x_perm = torch.randn((R, spec.d_model), generator=g, device=dev).to(spec.torch_dtype)
+    f = torch.empty((R, spec.d_model), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flops = 6.0 * spec.d_model * spec.d_expert * R
+    rows = []
+    for name, counts in histograms(spec.N, R):
+        assert sum(counts) == R and len(counts) == spec.N
+        offs = torch.tensor([0] + list(__import__("itertools").accumulate(counts)), dtype=torch.int32, device=dev)
+        for _ in range(3):
+            moe.moe_grouped_swiglu(cfg, x_perm, offs, None, inp["W_gate"], inp["W_up"], inp["W_down"], f, ws)
+        torch.cuda.synchronize()
+        ms = 0.0
+        for _ in range(args.steps):
+            flush.add_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            moe.moe_grouped_swiglu(cfg, x_perm, offs, None, inp["W_gate"], inp["W_up"], inp["W_down"], f, ws)
+            b.record()
+            torch.cuda.synchronize()
+            ms += a.elapsed_time(b)
+        ms /= args.steps
+        rows.append({"histogram": name, "max_load": max(counts), "entropy_deficit": round(entropy_deficit(counts), 4),
+                     "ms": round(ms, 4), "tflops": round(flops / ms / 1e9, 1)})
+    assert moe.moe_read_status(ws) == 0
+    base = rows[0]["tflops"]
+    for r in rows:
+        r["normalized"] = round(r["tflops"] / base, 4)
+        print(json.dumps(r), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------- main
 
 def main():
@@ -120,6 +197,8 @@ def main():
     ap.add_argument("--config", default="olmo")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--sweep", choices=["entropy"], default=None,
+                    help="instead of the benchmark line: grouped-GEMM throughput vs entropy deficit")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -128,6 +207,8 @@ def main():
 
     from workloads import CONFIGS, make_inputs
     spec = CONFIGS[args.config]
+    if args.sweep == "entropy":
+        return sweep_entropy(args, spec)
     cores = len(os.sched_getaffinity(0))
     config = {"workload": spec.name, "T": spec.T, "d_model": spec.d_model, "N": spec.N,
               "d_expert": spec.d_expert, "K": spec.K, "d_shared": spec.d_shared,
