@@ -27,7 +27,9 @@ Sources (page title, then section / equation / table):
   kept counts, destination totals), Eq. 22 (max/mean), Eq. 23 and 25
   (rank-wide and per-expert capacity), Eq. 26 (packed offsets), the admission
   order of Section 10.3, Eq. 27 (route-drop fraction), Eq. 28-29 (drop totals),
-  Eq. 35 (selection on logits for softmax routing).
+  Eq. 35 (selection on logits for softmax routing, selection-only bias),
+  Eq. 36-37 (bias controller), Eq. 30 / 38 (load-balancing loss statistics),
+  Eq. 39 (requested max/mean), the entropy deficit of Section 10.2.
 
 Readings where the pages are silent or ambiguous are stated beside the code
 that takes them.  Parity unpinned: the exact expert and shared outputs f_i, g
@@ -336,18 +338,33 @@ class Routing:
     drops: dict
 
 
-def route(logits, cfg, rho=None) -> Routing:
+def selection_keys(logits, selection_bias=None) -> np.ndarray:
+    """a_t,i + b_i of Eq. 35: the key the selection ranks, with the persistent
+    selection-only bias b ("Section 10.6", Eq. 35).  The bias moves the selection
+    only; the mixture weights come from the unbiased logits.
+
+    The key is formed in float32 (the precision of the device's logits), so the
+    comparisons that decide the selection are the same on both sides.
+    """
+    z = np.asarray(logits)
+    if selection_bias is None:
+        return f64(z)
+    return (z.astype(np.float32) + np.asarray(selection_bias, np.float32)[None, :]).astype(F64)
+
+
+def route(logits, cfg, rho=None, selection_bias=None) -> Routing:
     """Steps from the logits to the packed layout, for a whole batch.
 
     ``cfg`` needs N, K, T, score, norm, alpha, cap_policy, capacity_factor,
-    num_ranks.  ``rho`` defaults to i mod num_ranks.
+    num_ranks.  ``rho`` defaults to i mod num_ranks.  ``selection_bias`` is the
+    optional Eq. 35 bias b (selection only).
     """
     z = f64(logits)
     T, N = z.shape
     K = cfg.K
     if rho is None:
         rho = [i % cfg.num_ranks for i in range(N)]
-    idx = select_topk(z, K)
+    idx = select_topk(selection_keys(logits, selection_bias), K)
     r = cfg.alpha * selected_weights(z, idx, cfg.score, cfg.norm)
     C_req = requested_counts(idx, N)
     C_keep = kept_counts(C_req, cfg.cap_policy, cfg.capacity_factor, K, T, rho, cfg.num_ranks)
@@ -408,3 +425,67 @@ def moe_forward(cfg, inputs: dict, logits=None):
     y = moe_outputs_for_tokens(np.arange(T), x, routing, lambda e: (Wg[e], Wu[e], Wd[e]),
                                shared, s)
     return y, routing, s
+
+
+# --------------------------------------------------------------------------- #
+# Load-balancing statistics and the bias controller                           #
+# --------------------------------------------------------------------------- #
+
+def normalized_scores(z, score: str) -> np.ndarray:
+    """p_t,i: router scores normalised across the N experts of each token.
+
+    Softmax scores are already normalised; sigmoid scores are divided by their
+    sum over the experts ("Section 10.7.1": for sigmoid routing the scores the
+    loss uses are normalised across experts).
+    """
+    if score == "softmax":
+        return softmax_all(z)
+    q = sigmoid(z)
+    return q / q.sum(axis=1, keepdims=True)
+
+
+def lbl_statistics(p, idx, N: int):
+    """f_i = C_i^req / (K T), P_i = mean_t p_t,i and L = N sum_i f_i P_i
+    ("Section 10.5", Eq. 30; Eq. 38)."""
+    p = f64(p)
+    idx = np.asarray(idx)
+    T, K = idx.shape
+    C = requested_counts(idx, N).astype(F64)
+    f = C / (K * T)
+    P = p.mean(axis=0)
+    return f, P, float(N * (f * P).sum())
+
+
+def max_mean_imbalance(x) -> float:
+    """I_max(x) = n ||x||_inf / ||x||_1 for a nonzero load vector ("Section 10.2", Eq. 22)."""
+    x = f64(x)
+    return float(len(x) * x.max() / x.sum())
+
+
+def entropy_deficit(x) -> float:
+    """I_H(x) = 1 - H(pi) / log n with pi = x / sum x ("Section 10.2")."""
+    x = f64(x)
+    pi = x / x.sum()
+    nz = pi[pi > 0]
+    return float(1.0 + (nz * np.log(nz)).sum() / np.log(len(x)))
+
+
+def coefficient_of_variation(x) -> float:
+    """Standard deviation over mean of a load vector ("Section 10.2")."""
+    x = f64(x)
+    return float(x.std() / x.mean())
+
+
+def never_selected(x) -> int:
+    """Experts with zero load ("Section 10.2": never-selected experts)."""
+    return int((np.asarray(x) == 0).sum())
+
+
+def bias_update(bias, counts, gamma: float) -> np.ndarray:
+    """b_i <- b_i + gamma sign(mean(C) - C_i) ("Section 10.6", Eq. 36-37).
+
+    Computed in float32, the precision of the stored bias.
+    """
+    C = f64(counts)
+    step = np.sign(C.mean() - C).astype(np.float32)
+    return np.asarray(bias, np.float32) + np.float32(gamma) * step

@@ -363,3 +363,106 @@ def test_shared_gate_closed_form():
     x = np.array([[math.log(3.0), 0.0]])
     s = O.shared_coefficient(x, "gate", 1.0, np.array([1.0, 7.0]))
     assert abs(s[0] - 0.75) < 1e-15
+
+
+# ----------------------------------------------- Section 10.5-10.7: balancing --
+
+def test_eq45_six_token_lbl(golden):
+    """Eq. 43-45: f = (1/3, 2/3), P = (3/5, 2/5), L = 14/15, and the centered form (Eq. 41)."""
+    g = read_golden("eq43_six_token_example.txt")
+    p = np.array(g["scores"])
+    idx = O.select_topk(p, 1)
+    f, P, L = O.lbl_statistics(p, idx, 2)
+    np.testing.assert_allclose(f, g["f"], rtol=1e-15)
+    np.testing.assert_allclose(P, g["P"], rtol=1e-15)
+    assert abs(L - g["L_LBL"][0]) < 1e-15
+    u = np.full(2, 0.5)
+    assert abs(L - (1 + 2 * (f - u) @ (P - u))) < 1e-15
+    assert abs(O.max_mean_imbalance(O.requested_counts(idx, 2)) - g["I_max"][0]) < 1e-15
+
+
+def test_eq40_eq42_lbl_identities():
+    """Eq. 42: P = u gives L = 1 for any f; Eq. 40: P = f gives L = 1 + N ||f - u||^2; Eq. 41 in general."""
+    rng = np.random.default_rng(8)
+    for N, K, T in [(4, 1, 50), (16, 2, 200), (64, 4, 300)]:
+        idx = np.stack([rng.choice(N, size=K, replace=False) for _ in range(T)])
+        f, _, _ = O.lbl_statistics(np.full((T, N), 1.0 / N), idx, N)
+        assert abs(O.lbl_statistics(np.full((T, N), 1.0 / N), idx, N)[2] - 1.0) < 1e-12
+        # a score table whose column means equal f
+        p = np.tile(f, (T, 1))
+        L = O.lbl_statistics(p, idx, N)[2]
+        u = np.full(N, 1.0 / N)
+        assert abs(L - (1 + N * ((f - u) ** 2).sum())) < 1e-12
+        z = rng.normal(size=(T, N))
+        p = O.softmax_all(z)
+        f, P, L = O.lbl_statistics(p, idx, N)
+        assert abs(L - (1 + N * (f - u) @ (P - u))) < 1e-12
+
+
+def test_eq48_two_expert_infimum(golden):
+    """Eq. 47-49: with expert-1 routes scoring (1, 0) and expert-2 routes (1/2 - e, 1/2 + e),
+    L approaches 1 - x + 2 x^2 as e -> 0: 7/8 at x = 1/4, 8/9 for the 2:4 split."""
+    g = read_golden("eq48_52_lbl_limits.txt")
+    for xk, lk in (("two_expert_x", "two_expert_inf"), ("two_expert_x_split", "two_expert_inf_split")):
+        x = g[xk][0]
+        T = 12
+        n1 = int(round(x * T))
+        eps = 1e-9
+        p = np.array([[1.0, 0.0]] * n1 + [[0.5 - eps, 0.5 + eps]] * (T - n1))
+        idx = O.select_topk(p, 1)
+        assert (idx[:n1, 0] == 0).all() and (idx[n1:, 0] == 1).all()
+        L = O.lbl_statistics(p, idx, 2)[2]
+        assert abs(L - g[lk][0]) < 1e-8
+        assert abs(g[lk][0] - (1 - x + 2 * x * x)) < 1e-15
+
+
+def test_eq52_many_expert_limit(golden):
+    """Eq. 50-52: A active experts win uniformly; winners score (1 + D e)/(D + K), dead experts
+    (1 - K e)/(D + K), other active experts ~0; L -> N K / (A (N - A + K))."""
+    g = read_golden("eq48_52_lbl_limits.txt")
+    N, A, K = int(g["many_N"][0]), int(g["many_A"][0]), int(g["many_K"][0])
+    for (N, A, K, want) in [(N, A, K, g["many_limit"][0]), (64, 16, 4, None), (32, 8, 2, None)]:
+        D = N - A
+        eps = 1e-10
+        T = A * 10
+        p = np.zeros((T, N))
+        for t in range(T):
+            win = [(t * K + j) % A for j in range(K)]
+            p[t, A:] = (1 - K * eps) / (D + K)
+            p[t, win] = (1 + D * eps) / (D + K)
+        idx = O.select_topk(p, K)
+        L = O.lbl_statistics(p, idx, N)[2]
+        limit = N * K / (A * (N - A + K))
+        if want is not None:
+            assert abs(limit - want) < 1e-15
+        assert abs(L - limit) < 1e-8
+        assert abs(O.max_mean_imbalance(O.requested_counts(idx, N)) - N / A) < 1e-12
+        assert O.never_selected(O.requested_counts(idx, N)) == D
+
+
+def test_entropy_deficit_and_cv_closed_forms():
+    assert O.entropy_deficit(np.full(8, 5)) == 0.0
+    assert abs(O.entropy_deficit(np.eye(8)[3]) - 1.0) < 1e-15
+    x = np.array([1, 1, 0, 0])
+    assert abs(O.entropy_deficit(x) - 0.5) < 1e-15            # log 2 / log 4
+    assert O.coefficient_of_variation(np.full(5, 3)) == 0.0
+    assert abs(O.coefficient_of_variation(np.array([0, 2])) - 1.0) < 1e-15
+    assert O.max_mean_imbalance(np.full(6, 7)) == 1.0
+
+
+def test_eq37_bias_update_by_hand():
+    """Eq. 36-37: b_i <- b_i + gamma sign(mean C - C_i)."""
+    b = O.bias_update(np.array([0.0, 0.5, -0.25, 1.0]), np.array([5, 1, 3, 3]), 0.125)
+    np.testing.assert_array_equal(b, np.array([-0.125, 0.625, -0.25, 1.0], np.float32))
+
+
+def test_eq35_selection_bias_moves_selection_not_weights():
+    """Eq. 35: the bias enters the selection key only; weights come from the unbiased logits."""
+    z = np.array([[1.0, 0.9, -1.0, 0.0]])
+    cfg = Cfg(N=4, K=2, T=1, alpha=1.0)
+    plain = O.route(z, cfg)
+    assert sorted(plain.topk_idx[0].tolist()) == [0, 1]
+    biased = O.route(z, cfg, selection_bias=[0.0, 0.0, 0.0, 1.5])
+    assert biased.topk_idx[0].tolist() == [3, 0]           # keys (1.0, 0.9, -1.0, 1.5)
+    e = np.exp(np.array([0.0, 1.0]))
+    np.testing.assert_allclose(biased.topk_w[0], e / e.sum(), rtol=1e-15)
