@@ -100,11 +100,12 @@ typedef struct moe_config {
   const int32_t* rho;     /* HOST [N], values in [0, num_ranks); NULL means rho(i) = i mod num_ranks */
 } moe_config;
 
-/* Weights of one layer (device pointers, layouts above).  router_bias [N] fp32 and
+/* Weights of one layer (device pointers, layouts above).  router_bias, selection_bias and
  * shared_gate_w [d] may be NULL; shared weights are ignored when d_shared == 0. */
 typedef struct moe_weights {
   const void* W_router;
-  const float* router_bias;
+  const float* router_bias;       /* [N] fp32 logit bias (enters selection and scores), or NULL */
+  const float* selection_bias;    /* [N] fp32 Eq. 35 bias b (enters the selection key only), or NULL */
   const void* shared_gate_w;
   const void* W_gate;
   const void* W_up;
@@ -144,14 +145,18 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Router, scores, top-K and coefficients for every token (Section 10, Table 16 first row;
  * Appendix E, Table 52; Eq. 80 coefficients r and s).
- *   x [T][d]; W_router [N][d]; router_bias [N] fp32 or NULL; shared_gate_w [d] or NULL
- *   (required iff shared_mode is the sigmoid gate).
- * Out: topk_idx [T][K]; topk_w [T][K]; shared_coef [T] (may be NULL); logits [T][N] (may be NULL).
- * The selection key is the fp32 logit z + bias; ties go to the lower expert index. */
+ *   x [T][d]; W_router [N][d]; router_bias [N] fp32 or NULL (a logit bias: part of z);
+ *   selection_bias [N] fp32 or NULL (Section 10.6, Eq. 35: added to the selection key only,
+ *   the weights come from the unbiased logits); shared_gate_w [d] or NULL (required iff
+ *   shared_mode is the sigmoid gate).
+ * Out: topk_idx [T][K]; topk_w [T][K]; shared_coef [T] (may be NULL); logits [T][N] (may be
+ * NULL) = z, the logits with router_bias and without selection_bias.
+ * The selection key is the fp32 value z (+ selection_bias); ties go to the lower expert index. */
 moe_status moe_route(const moe_config* cfg, const void* x, const void* W_router,
-                     const float* router_bias, const void* shared_gate_w,
-                     int32_t* topk_idx, float* topk_w, float* shared_coef, float* logits,
-                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                     const float* router_bias, const float* selection_bias,
+                     const void* shared_gate_w, int32_t* topk_idx, float* topk_w,
+                     float* shared_coef, float* logits, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
 
 /* Requested and kept counts, capacity, packed offsets and the row permutation
  * (Section 10.1, Eq. 19-21; Section 10.3, Eq. 23, 25, 26, 27).
@@ -232,6 +237,38 @@ moe_status moe_merge_shared(int32_t d_model, int32_t dtype, int32_t n_parts, con
                             const void* const* gate_parts, const void* const* up_parts,
                             const void* const* down_parts, void* Ws_gate, void* Ws_up,
                             void* Ws_down, cudaStream_t stream);
+
+/* Indices into the stats array of moe_balance_stats. */
+typedef enum {
+  MOE_STAT_LBL = 0,            /* L = N sum_i f_i P_i (Eq. 30); NaN without logits */
+  MOE_STAT_IMAX_REQ = 1,       /* I_max of C^req (Eq. 22, 39) */
+  MOE_STAT_IMAX_KEEP = 2,      /* I_max of C^keep; NaN without counts_keep */
+  MOE_STAT_IMAX_RANK_REQ = 3,  /* I_max of R^req; NaN without R_req */
+  MOE_STAT_IMAX_RANK_KEEP = 4, /* I_max of R^keep; NaN without R_keep */
+  MOE_STAT_IH_REQ = 5,         /* entropy deficit 1 - H(pi)/log N of C^req (Section 10.2) */
+  MOE_STAT_IH_KEEP = 6,        /* entropy deficit of C^keep; NaN without counts_keep */
+  MOE_STAT_CV_REQ = 7,         /* coefficient of variation of C^req */
+  MOE_STAT_NEVER_SELECTED = 8, /* experts with C^req = 0 */
+  MOE_STAT_DROP_FRACTION = 9,  /* delta_route = sum D / (K T) (Eq. 27); NaN without counts_keep */
+  MOE_STAT_COUNT = 10
+} moe_stat;
+
+/* Load-balancing statistics of one routed batch (Section 10.5, Eq. 30 and 38; Section 10.2,
+ * Eq. 22; Eq. 27).  logits [T][N] fp32 as moe_route wrote them (may be NULL: no P, no LBL);
+ * counts_req [N] (required), counts_keep [N], R_req / R_keep [num_ranks] (may be NULL).
+ * Out (device, each may be NULL): P [N] = mean over tokens of the scores normalised across
+ * experts (softmax probabilities; sigmoid scores divided by their sum, Section 10.7.1);
+ * f [N] = C_req / (K T); stats [MOE_STAT_COUNT] fp32.  Deterministic (fixed summation order). */
+moe_status moe_balance_stats(const moe_config* cfg, const float* logits, const int32_t* counts_req,
+                             const int32_t* counts_keep, const int32_t* R_req,
+                             const int32_t* R_keep, float* P, float* f, float* stats,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Post-batch bias controller (Section 10.6, Eq. 36-37): bias[i] += gamma * sign(mean(C) - C[i])
+ * for the selection-only bias of Eq. 35.  counts [N] int32 (requested counts of the feedback
+ * window), bias [N] fp32 updated in place; both device.  Asynchronous on the stream. */
+moe_status moe_bias_update(int32_t N, const int32_t* counts, float gamma, float* bias,
+                           cudaStream_t stream);
 
 /* Prepare a fresh workspace: zero its device status word (the first 256 bytes).  Call once
  * after allocating a workspace, before its first use.  Asynchronous on the stream. */

@@ -41,8 +41,8 @@ class moe_config(ctypes.Structure):
 
 
 class moe_weights(ctypes.Structure):
-    _fields_ = [(n, c_void_p) for n in ("W_router", "router_bias", "shared_gate_w", "W_gate", "W_up",
-                                        "W_down", "Ws_gate", "Ws_up", "Ws_down")]
+    _fields_ = [(n, c_void_p) for n in ("W_router", "router_bias", "selection_bias", "shared_gate_w",
+                                        "W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down")]
 
 
 OUTPUT_FIELDS = ("y", "topk_idx", "topk_w", "shared_coef", "logits", "counts_req", "counts_keep",
@@ -65,7 +65,9 @@ def _load():
         "moe_status_string": ([c_int32], c_char_p),
         "moe_workspace_size": ([C, POINTER(c_size_t)], c_int32),
         "moe_workspace_init": ([P, c_size_t, P], c_int32),
-        "moe_route": ([C, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
+        "moe_route": ([C, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
+        "moe_balance_stats": ([C, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
+        "moe_bias_update": ([c_int32, P, c_float, P, P], c_int32),
         "moe_permute": ([C, P, P, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
         "moe_permute_noalloc": ([C, P, P, P, P, P, P, P, P, P, P, P, P], c_int32),
         "moe_grouped_swiglu": ([C, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
@@ -164,12 +166,30 @@ def alloc_workspace(cfg: moe_config, device="cuda", stream=None):
     return ws
 
 
-def moe_route(cfg, x, W_router, router_bias, shared_gate_w, topk_idx, topk_w, shared_coef, logits,
-              workspace, stream=None):
+def moe_route(cfg, x, W_router, router_bias, selection_bias, shared_gate_w, topk_idx, topk_w,
+              shared_coef, logits, workspace, stream=None):
     _check("moe_route", _lib.moe_route(
-        ctypes.byref(cfg), _ptr(x), _ptr(W_router), _ptr(router_bias), _ptr(shared_gate_w),
-        _ptr(topk_idx), _ptr(topk_w), _ptr(shared_coef), _ptr(logits), _ptr(workspace),
-        workspace.numel(), _stream(stream)))
+        ctypes.byref(cfg), _ptr(x), _ptr(W_router), _ptr(router_bias), _ptr(selection_bias),
+        _ptr(shared_gate_w), _ptr(topk_idx), _ptr(topk_w), _ptr(shared_coef), _ptr(logits),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+STATS = ("lbl", "imax_req", "imax_keep", "imax_rank_req", "imax_rank_keep", "ih_req", "ih_keep",
+         "cv_req", "never_selected", "drop_fraction")
+
+
+def moe_balance_stats(cfg, logits, counts_req, counts_keep, R_req, R_keep, P, f, stats, workspace,
+                      stream=None):
+    """stats: float32 [len(STATS)] device tensor, indexed as STATS."""
+    _check("moe_balance_stats", _lib.moe_balance_stats(
+        ctypes.byref(cfg), _ptr(logits), _ptr(counts_req), _ptr(counts_keep), _ptr(R_req),
+        _ptr(R_keep), _ptr(P), _ptr(f), _ptr(stats), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
+
+
+def moe_bias_update(N, counts, gamma, bias, stream=None):
+    _check("moe_bias_update", _lib.moe_bias_update(int(N), _ptr(counts), float(gamma), _ptr(bias),
+                                                    _stream(stream)))
 
 
 def moe_permute(cfg, x, topk_idx, counts_req, counts_keep, offsets, route_pos, perm_src, x_perm,
@@ -210,10 +230,11 @@ def moe_combine(cfg, f, route_pos, topk_w, g, shared_coef, y, stream=None):
 
 
 def make_weights(W_router, router_bias, shared_gate_w, W_gate, W_up, W_down, Ws_gate=None,
-                 Ws_up=None, Ws_down=None) -> moe_weights:
+                 Ws_up=None, Ws_down=None, selection_bias=None) -> moe_weights:
     w = moe_weights()
     keep = []
     for name, t in (("W_router", W_router), ("router_bias", router_bias),
+                    ("selection_bias", selection_bias),
                     ("shared_gate_w", shared_gate_w), ("W_gate", W_gate), ("W_up", W_up),
                     ("W_down", W_down), ("Ws_gate", Ws_gate), ("Ws_up", Ws_up), ("Ws_down", Ws_down)):
         p = _ptr(t)

@@ -67,12 +67,13 @@ moe_status check_ws(const moe_config& c, void* ws, size_t bytes, Layout* L) {
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 RouteParams route_params(const moe_config& c, const void* x, const void* W_router,
-                         const float* bias, const void* gate_w, int32_t* idx, float* w,
-                         float* s, float* logits, int32_t* status) {
+                         const float* bias, const float* sel_bias, const void* gate_w,
+                         int32_t* idx, float* w, float* s, float* logits, int32_t* status) {
   RouteParams p{};
   p.x = x;
   p.W_router = W_router;
   p.router_bias = bias;
+  p.selection_bias = sel_bias;
   p.shared_gate_w = gate_w;
   p.T = c.T;
   p.d = c.d_model;
@@ -92,13 +93,12 @@ RouteParams route_params(const moe_config& c, const void* x, const void* W_route
 }
 
 moe_status do_route(const moe_config& c, const void* x, const void* W_router, const float* bias,
-                    const void* gate_w, int32_t* idx, float* w, float* s, float* logits,
-                    int32_t* status, cudaStream_t st) {
+                    const float* sel_bias, const void* gate_w, int32_t* idx, float* w, float* s,
+                    float* logits, int32_t* status, cudaStream_t st) {
   if (c.T > 0 && (!x || !W_router || !idx || !w)) return MOE_ERR_INVALID_ARG;
   if (c.shared_mode == MOE_SHARED_SIGMOID_GATE && !gate_w) return MOE_ERR_INVALID_ARG;
-  return cuda_status(
-      launch_route(route_params(c, x, W_router, bias, gate_w, idx, w, s, logits, status), c.dtype,
-                   st));
+  return cuda_status(launch_route(
+      route_params(c, x, W_router, bias, sel_bias, gate_w, idx, w, s, logits, status), c.dtype, st));
 }
 
 struct PermOut {
@@ -262,6 +262,7 @@ Layout make_layout(const moe_config& c) {
   L.R_req = take(M * 4);
   L.R_keep = take(M * 4);
   L.drop_stats = take(16);
+  L.score_partial = take(static_cast<size_t>(L.hist_tiles) * N * 4);
   L.x_perm = take(T * K * d * eb);
   L.h = take(T * K * dr * eb);
   L.f = take(T * K * d * 4);
@@ -302,15 +303,16 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
 }
 
 moe_status moe_route(const moe_config* cfg, const void* x, const void* W_router,
-                     const float* router_bias, const void* shared_gate_w, int32_t* topk_idx,
-                     float* topk_w, float* shared_coef, float* logits, void* workspace,
-                     size_t workspace_bytes, cudaStream_t stream) {
+                     const float* router_bias, const float* selection_bias,
+                     const void* shared_gate_w, int32_t* topk_idx, float* topk_w,
+                     float* shared_coef, float* logits, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
   moe_status s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   Layout L;
   if ((s = check_ws(*cfg, workspace, workspace_bytes, &L)) != MOE_OK) return s;
-  return do_route(*cfg, x, W_router, router_bias, shared_gate_w, topk_idx, topk_w, shared_coef,
-                  logits, at<int32_t>(workspace, L.status), stream);
+  return do_route(*cfg, x, W_router, router_bias, selection_bias, shared_gate_w, topk_idx, topk_w,
+                  shared_coef, logits, at<int32_t>(workspace, L.status), stream);
 }
 
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
@@ -375,8 +377,8 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
   float* tw = pick(out->topk_w, L.topk_w);
   float* sc = pick(out->shared_coef, L.shared_coef);
   int32_t* status = at<int32_t>(ws, L.status);
-  if ((s = do_route(c, x, w->W_router, w->router_bias, w->shared_gate_w, idx, tw, sc, out->logits,
-                    status, stream)) != MOE_OK)
+  if ((s = do_route(c, x, w->W_router, w->router_bias, w->selection_bias, w->shared_gate_w, idx,
+                    tw, sc, out->logits, status, stream)) != MOE_OK)
     return s;
   PermOut po{pick(out->counts_req, L.counts_req), pick(out->counts_keep, L.counts_keep),
              pick(out->offsets, L.offsets),       pick(out->route_pos, L.route_pos),
@@ -431,6 +433,27 @@ moe_status moe_merge_shared(int32_t d_model, int32_t dtype, int32_t n_parts, con
     row += w;
   }
   return MOE_OK;
+}
+
+moe_status moe_balance_stats(const moe_config* cfg, const float* logits, const int32_t* counts_req,
+                             const int32_t* counts_keep, const int32_t* R_req,
+                             const int32_t* R_keep, float* P, float* f, float* stats,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  Layout L;
+  if ((s = check_ws(*cfg, workspace, workspace_bytes, &L)) != MOE_OK) return s;
+  if (!counts_req) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_balance_stats(*cfg, logits, at<float>(workspace, L.score_partial),
+                                          counts_req, counts_keep, R_req, R_keep, P, f, stats,
+                                          stream));
+}
+
+moe_status moe_bias_update(int32_t N, const int32_t* counts, float gamma, float* bias,
+                           cudaStream_t stream) {
+  if (N < 1 || N > kMaxExperts || !counts || !bias || !std::isfinite(gamma))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_bias_update(N, counts, gamma, bias, stream));
 }
 
 moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream) {

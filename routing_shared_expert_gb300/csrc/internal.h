@@ -20,7 +20,8 @@ constexpr int kTcRows = 128;       // rows per tensor-core tile (tcgen05 M)
 // Byte offsets of the regions of one workspace (each region 256-byte aligned).
 struct Layout {
   size_t status, hist, tile_prefix, topk_idx, topk_w, shared_coef, logits, counts_req,
-      counts_keep, offsets, route_pos, perm_src, R_req, R_keep, drop_stats, x_perm, h, f, hs, g;
+      counts_keep, offsets, route_pos, perm_src, R_req, R_keep, drop_stats, score_partial, x_perm, h, f,
+      hs, g;
   size_t total;
   int64_t hist_tiles;
 };
@@ -37,6 +38,7 @@ struct RouteParams {
   const void* x;
   const void* W_router;
   const float* router_bias;
+  const float* selection_bias;   // Eq. 35 b_i: added to the selection key only (nullable)
   const void* shared_gate_w;
   int64_t T;
   int32_t d, N, K, score, norm, shared_mode;
@@ -130,5 +132,13 @@ struct CombineParams {
   int32_t* status;
 };
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+
+// ---- balancing statistics ------------------------------------------------------
+cudaError_t launch_balance_stats(const moe_config& c, const float* logits, float* partial,
+                                 const int32_t* counts_req, const int32_t* counts_keep,
+                                 const int32_t* R_req, const int32_t* R_keep, float* P, float* f,
+                                 float* stats, cudaStream_t s);
+cudaError_t launch_bias_update(int32_t N, const int32_t* counts, float gamma, float* bias,
+                               cudaStream_t s);
 
 }  // namespace moe

@@ -95,14 +95,19 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     const int64_t t = t0 + r;
     if (t >= p.T) break;
     const float* z = zl + r * (ncols + 1);
-    float v[8];
+    float v[8], key[8];   // unbiased logit z, and the selection key z + b_sel
     bool live[8];
+    float zmax = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int e = lane + 32 * j;
       live[j] = e < p.N;
       v[j] = live[j] ? z[e] : 0.f;
+      key[j] = (live[j] && p.selection_bias) ? v[j] + p.selection_bias[e] : v[j];
+      if (live[j]) zmax = fmaxf(zmax, v[j]);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, off));
     if (p.logits) {
 #pragma unroll
       for (int j = 0; j < 8; ++j)
@@ -116,24 +121,25 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     for (int k = 0; k < kMaxTopK; ++k) {
       if (k >= p.K) break;
       // this lane's best remaining candidate: larger key, then lower index
-      float bv = 0.f;
+      float bv = 0.f, bz = 0.f;
       int bi = 0x7fffffff;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int e = lane + 32 * j;
-        if (live[j] && (bi == 0x7fffffff || v[j] > bv)) { bv = v[j]; bi = e; }
+        if (live[j] && (bi == 0x7fffffff || key[j] > bv)) { bv = key[j]; bz = v[j]; bi = e; }
       }
       // warp arg-max (ties to the lower index; lanes without candidates carry bi = INT_MAX)
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const float oz = __shfl_xor_sync(0xffffffffu, bz, off);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
         const bool take = (oi != 0x7fffffff) &&
                           (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-        if (take) { bv = ov; bi = oi; }
+        if (take) { bv = ov; bz = oz; bi = oi; }
       }
       sel_i[k] = bi;
-      sel_z[k] = bv;
+      sel_z[k] = bz;
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         if (bi == lane + 32 * j) live[j] = false;
@@ -144,17 +150,20 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
 #pragma unroll
     for (int k = 0; k < kMaxTopK; ++k) w[k] = 0.f;
     if (p.norm == MOE_NORM_SOFTMAX_SELECTED) {
-      float s = 0.f;
+      float s = 0.f, msel = sel_z[0];
+#pragma unroll
+      for (int k = 1; k < kMaxTopK; ++k)
+        if (k < p.K) msel = fmaxf(msel, sel_z[k]);
 #pragma unroll
       for (int k = 0; k < kMaxTopK; ++k)
-        if (k < p.K) { w[k] = expf(sel_z[k] - sel_z[0]); s += w[k]; }
+        if (k < p.K) { w[k] = expf(sel_z[k] - msel); s += w[k]; }
 #pragma unroll
       for (int k = 0; k < kMaxTopK; ++k)
         if (k < p.K) w[k] /= s;
     } else {
       if (p.score == MOE_SCORE_SOFTMAX) {
-        // full softmax over all N: the maximum logit is the first selected one
-        const float m = sel_z[0];
+        // full softmax over all N (unbiased logits)
+        const float m = zmax;
         float s = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {

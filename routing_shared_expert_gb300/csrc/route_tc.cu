@@ -11,8 +11,9 @@
 //   - warps 2-5 read the accumulators with tcgen05.ld, one token row per
 //     thread, so the selection runs in registers: a sorted top-8 list with
 //     strict comparisons (an equal later expert never displaces an earlier one,
-//     which gives the lower-index tie rule), then the scores of the selected
-//     experts, the selected weights and r = alpha * w.
+//     which gives the lower-index tie rule) on the key z (+ the Eq. 35
+//     selection-only bias), then the scores of the selected experts from the
+//     unbiased logits, the selected weights and r = alpha * w.
 // Every wait is bounded; a wait that runs out records MOE_ERR_TIMEOUT.
 #include "common.cuh"
 #include "internal.h"
@@ -53,7 +54,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* never = const_cast<int*>(abort_flag) + 1;
-  float* s_bias = reinterpret_cast<float*>(never + 1);   // [kMaxExperts]
+  float* s_bias = reinterpret_cast<float*>(never + 1);   // [kMaxExperts] logit bias
+  float* s_sel = s_bias + kMaxExperts;                    // [kMaxExperts] selection-only bias
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int k_blocks = (p.d + BK - 1) / BK;
@@ -71,7 +73,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     *never = 0;
     mbar_fence_init();
   }
-  for (int i = threadIdx.x; i < p.N; i += THREADS) s_bias[i] = p.router_bias ? p.router_bias[i] : 0.f;
+  for (int i = threadIdx.x; i < p.N; i += THREADS) {
+    s_bias[i] = p.router_bias ? p.router_bias[i] : 0.f;
+    s_sel[i] = p.selection_bias ? p.selection_bias[i] : 0.f;
+  }
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&tmX);
     tma_prefetch_map(&tmW);
@@ -161,10 +166,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool valid = t < p.T;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
       constexpr int EMPTY = 0x7fffffff;
-      float bv[kMaxTopK];
+      float bv[kMaxTopK], bz[kMaxTopK];   // selection key and unbiased logit of each slot
       int bi[kMaxTopK];
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) { bv[j] = 0.f; bi[j] = EMPTY; }
+      for (int j = 0; j < kMaxTopK; ++j) { bv[j] = 0.f; bz[j] = 0.f; bi[j] = EMPTY; }
+      float zmax = -INFINITY;
+      const bool sel = p.selection_bias != nullptr;
       float* lrow = (p.logits && valid) ? p.logits + t * p.N : nullptr;
       // pass 1: keys, logits output, top-8 list
       for (int c0 = 0; c0 < p.N; c0 += 32) {
@@ -188,17 +195,22 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           if (c0 + i >= p.N) break;
-          float cv = z[i];
+          zmax = fmaxf(zmax, z[i]);
+          float cv = sel ? z[i] + s_sel[c0 + i] : z[i];
+          float cz = z[i];
           int ci = c0 + i;
           if (bi[kMaxTopK - 1] == EMPTY || cv > bv[kMaxTopK - 1]) {
 #pragma unroll
             for (int j = 0; j < kMaxTopK; ++j) {
               const bool take = bi[j] == EMPTY || cv > bv[j];
               const float tv = take ? bv[j] : cv;
+              const float tz = take ? bz[j] : cz;
               const int ti = take ? bi[j] : ci;
               bv[j] = take ? cv : bv[j];
+              bz[j] = take ? cz : bz[j];
               bi[j] = take ? ci : bi[j];
               cv = tv;
+              cz = tz;
               ci = ti;
             }
           }
@@ -209,17 +221,20 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int j = 0; j < kMaxTopK; ++j) w[j] = 0.f;
       if (p.norm == MOE_NORM_SOFTMAX_SELECTED) {
-        float s = 0.f;
+        float s = 0.f, msel = bz[0];
+#pragma unroll
+        for (int j = 1; j < kMaxTopK; ++j)
+          if (j < p.K) msel = fmaxf(msel, bz[j]);
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j)
-          if (j < p.K) { w[j] = expf(bv[j] - bv[0]); s += w[j]; }
+          if (j < p.K) { w[j] = expf(bz[j] - msel); s += w[j]; }
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j)
           if (j < p.K) w[j] /= s;
       } else {
         if (p.score == MOE_SCORE_SOFTMAX) {
-          // pass 2: softmax denominator over all N experts (the maximum is bv[0])
-          const float m = bv[0];
+          // pass 2: softmax denominator over all N experts (unbiased logits)
+          const float m = zmax;
           float s = 0.f;
           for (int c0 = 0; c0 < p.N; c0 += 32) {
             uint32_t r[32];
@@ -230,11 +245,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
 #pragma unroll
           for (int j = 0; j < kMaxTopK; ++j)
-            if (j < p.K) w[j] = expf(bv[j] - m) / s;
+            if (j < p.K) w[j] = expf(bz[j] - m) / s;
         } else {
 #pragma unroll
           for (int j = 0; j < kMaxTopK; ++j)
-            if (j < p.K) w[j] = 1.f / (1.f + expf(-bv[j]));
+            if (j < p.K) w[j] = 1.f / (1.f + expf(-bz[j]));
         }
         if (p.norm == MOE_NORM_L1_SELECTED) {
           float s = 0.f;
@@ -297,7 +312,7 @@ cudaError_t launch_route_tc(const RouteParams& p, cudaStream_t s) {
   if (a.stages > 8) a.stages = 8;
   if (a.stages < 2) a.stages = 2;
   const size_t smem = 1024 + static_cast<size_t>(a.stages) * a.stage_bytes + 8 * 20 + 16 +
-                      sizeof(float) * kMaxExperts + 64;
+                      2 * sizeof(float) * kMaxExperts + 64;
   cudaError_t e = cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;

@@ -36,7 +36,7 @@ class MoELayer:
         self.w = nat.make_weights(weights["W_router"], weights.get("router_bias"),
                                   weights.get("shared_gate_w"), weights["W_gate"], weights["W_up"],
                                   weights["W_down"], weights.get("Ws_gate"), weights.get("Ws_up"),
-                                  weights.get("Ws_down"))
+                                  weights.get("Ws_down"), weights.get("selection_bias"))
         self.ws = nat.alloc_workspace(cfg, device)
         T, d, N, K, M = cfg.T, cfg.d_model, cfg.N, cfg.K, cfg.num_ranks
         i32 = dict(dtype=torch.int32, device=device)
@@ -87,8 +87,9 @@ class MoELayer:
                 events[i].record(st)
 
         rec(0)
-        nat.moe_route(c, x, w["W_router"], w.get("router_bias"), w.get("shared_gate_w"),
-                      o["topk_idx"], o["topk_w"], o["shared_coef"], o["logits"], self.ws, st)
+        nat.moe_route(c, x, w["W_router"], w.get("router_bias"), w.get("selection_bias"),
+                      w.get("shared_gate_w"), o["topk_idx"], o["topk_w"], o["shared_coef"],
+                      o["logits"], self.ws, st)
         rec(1)
         nat.moe_permute(c, x, o["topk_idx"], o["counts_req"], o["counts_keep"], o["offsets"],
                         o["route_pos"], o["perm_src"], s["x_perm"], o["R_req"], o["R_keep"],

@@ -26,11 +26,12 @@ def host(inp):
     return {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp.items()}
 
 
-def check_routing_exact(layer, spec):
+def check_routing_exact(layer, spec, selection_bias=None):
     """Indices, counts, capacity, offsets, positions and permutation: bit-exact against the
     oracle fed the device's fp32 logits.  Returns the oracle Routing."""
     out = {k: v.cpu() for k, v in layer.out.items()}
-    rt = O.route(out["logits"].double().numpy(), spec)
+    sb = None if selection_bias is None else selection_bias.cpu().numpy()
+    rt = O.route(out["logits"].numpy(), spec, selection_bias=sb)
     T, K, N = spec.T, spec.K, spec.N
     np.testing.assert_array_equal(out["topk_idx"].numpy(), rt.topk_idx)
     np.testing.assert_array_equal(out["counts_req"].numpy(), rt.counts_req)

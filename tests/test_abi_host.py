@@ -90,12 +90,13 @@ def test_entry_points_reject_before_cuda(nat):
     lib = nat.library()
     c = _olmo(T=64)
     fake = ctypes.c_void_p(0x1000)
-    st = lib.moe_route(ctypes.byref(c), fake, fake, None, None, fake, fake, None, None, None, 0, None)
+    st = lib.moe_route(ctypes.byref(c), fake, fake, None, None, None, fake, fake, None, None, None,
+                       0, None)
     assert st == -1
-    st = lib.moe_route(ctypes.byref(c), fake, fake, None, None, fake, fake, None, None,
+    st = lib.moe_route(ctypes.byref(c), fake, fake, None, None, None, fake, fake, None, None,
                        ctypes.c_void_p(0x100100), 16, None)
     assert st == -4   # workspace too small
-    st = lib.moe_route(ctypes.byref(c), fake, fake, None, None, fake, fake, None, None,
+    st = lib.moe_route(ctypes.byref(c), fake, fake, None, None, None, fake, fake, None, None,
                        ctypes.c_void_p(0x100101), 1 << 40, None)
     assert st == -7   # misaligned workspace
     w = nat.moe_weights()
@@ -105,6 +106,17 @@ def test_entry_points_reject_before_cuda(nat):
     # combine with g but no shared coefficient
     st = lib.moe_combine(ctypes.byref(c), fake, fake, fake, fake, None, fake, None)
     assert st == -1
+
+
+def test_bias_update_and_stats_reject_bad_args(nat):
+    lib = nat.library()
+    fake = ctypes.c_void_p(0x1000)
+    assert lib.moe_bias_update(0, fake, 0.1, fake, None) == -1
+    assert lib.moe_bias_update(4, None, 0.1, fake, None) == -1
+    assert lib.moe_bias_update(4, fake, float("inf"), fake, None) == -1
+    c = _olmo(T=64)
+    assert lib.moe_balance_stats(ctypes.byref(c), None, None, None, None, None, None, None, None,
+                                 None, 0, None) == -1
 
 
 def test_status_strings(nat):

@@ -1,0 +1,113 @@
+"""Aux-loss-free selection bias (Eq. 35), the bias controller (Eq. 36-37) and the
+load-balancing statistics (Eq. 22, 27, 30, 38, 39; entropy deficit), on a GB300,
+against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests.gpu_helpers import TOL, check_routing_exact, host, layer_error, oracle_y, run_layer
+from workloads import CONFIGS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+C = CONFIGS
+SHAPES = {
+    "tiny": C["tiny"],                                                          # CUDA-core router
+    "dsv3_s": C["dsv3"].replace(T=600, d_model=448, d_expert=128, d_shared=128),  # sigmoid, tensor cores
+    "olmo_s": C["olmo"].replace(T=1000, d_model=512, d_expert=384, d_shared=256),
+    "mixtral_s": C["mixtral"].replace(T=900, d_model=4096, d_expert=1024),     # selected softmax, capacity
+}
+
+
+def _bias(N, scale, seed=3):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(N, generator=g) * scale).to("cuda")
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_selection_bias_moves_selection_only(name):
+    spec = SHAPES[name]
+    inp = make_inputs(spec, "cuda")
+    b = _bias(spec.N, 0.75)
+    inp["selection_bias"] = b
+    layer = run_layer(spec, inp)
+    assert layer.status() == 0
+    rt = check_routing_exact(layer, spec, selection_bias=b)
+    # the bias changed some selections, and the weights are those of the unbiased logits
+    rt0 = O.route(layer.out["logits"].cpu().numpy(), spec)
+    assert (rt.topk_idx != rt0.topk_idx).any()
+    hin = host(inp)
+    y_ref, _ = oracle_y(spec, hin, rt, np.arange(spec.T))
+    err = layer_error(spec, layer.out["y"].cpu().double().numpy(), y_ref, rt.route_pos)
+    assert err <= TOL[spec.dtype]
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_balance_statistics(name):
+    import routing_shared_expert_gb300 as moe
+    spec = SHAPES[name]
+    inp = make_inputs(spec, "cuda")
+    layer = run_layer(spec, inp)
+    o = layer.out
+    P = torch.empty(spec.N, dtype=torch.float32, device="cuda")
+    f = torch.empty(spec.N, dtype=torch.float32, device="cuda")
+    st = torch.empty(len(moe.STATS), dtype=torch.float32, device="cuda")
+    moe.moe_balance_stats(layer.cfg, o["logits"], o["counts_req"], o["counts_keep"], o["R_req"],
+                          o["R_keep"], P, f, st, layer.ws)
+    torch.cuda.synchronize()
+    rt = check_routing_exact(layer, spec)
+    p = O.normalized_scores(o["logits"].cpu().numpy(), spec.score)
+    f_ref, P_ref, L_ref = O.lbl_statistics(p, rt.topk_idx, spec.N)
+    np.testing.assert_allclose(P.cpu().numpy(), P_ref, rtol=2e-5, atol=1e-7)
+    np.testing.assert_allclose(f.cpu().numpy(), f_ref, rtol=1e-6)
+    s = dict(zip(moe.STATS, st.cpu().numpy().tolist()))
+    assert abs(s["lbl"] - L_ref) <= 1e-5 * L_ref
+    assert abs(s["imax_req"] - O.max_mean_imbalance(rt.counts_req)) < 1e-5
+    assert abs(s["imax_keep"] - O.max_mean_imbalance(rt.counts_keep)) < 1e-5
+    assert abs(s["imax_rank_req"] - O.max_mean_imbalance(rt.R_req)) < 1e-5
+    assert abs(s["imax_rank_keep"] - O.max_mean_imbalance(rt.R_keep)) < 1e-5
+    assert abs(s["ih_req"] - O.entropy_deficit(rt.counts_req)) < 1e-5
+    assert abs(s["ih_keep"] - O.entropy_deficit(rt.counts_keep)) < 1e-5
+    assert abs(s["cv_req"] - O.coefficient_of_variation(rt.counts_req)) < 1e-5
+    assert s["never_selected"] == O.never_selected(rt.counts_req)
+    assert abs(s["drop_fraction"] - rt.drops["delta_route"]) < 1e-6
+
+
+def test_bias_update_matches_oracle_bit_for_bit():
+    import routing_shared_expert_gb300 as moe
+    g = torch.Generator().manual_seed(11)
+    for N in (8, 60, 256):
+        counts = torch.randint(0, 50, (N,), generator=g, dtype=torch.int32)
+        counts[: N // 8] = int(counts.float().mean().round())   # some exactly-average experts... maybe
+        bias = torch.randn(N, generator=g)
+        want = O.bias_update(bias.numpy(), counts.numpy(), 0.001)
+        b = bias.to("cuda")
+        moe.moe_bias_update(N, counts.to("cuda"), 0.001, b)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(b.cpu().numpy(), want)
+
+
+def test_bias_controller_feedback_loop_balances_requests():
+    """Eq. 35-37 closed loop on a skewed router: repeated batches with the post-batch sign update
+    reduce the requested max/mean imbalance, and every step matches the oracle exactly."""
+    import routing_shared_expert_gb300 as moe
+    spec = C["mixtral"].replace(T=1024, d_model=256, d_expert=128, cap_policy="none",
+                                capacity_factor=1.0)
+    inp = make_inputs(spec, "cuda")
+    b = torch.zeros(spec.N, dtype=torch.float32, device="cuda")
+    inp["selection_bias"] = b
+    layer = moe.MoELayer(moe.config_from_spec(spec), inp, "cuda")
+    first = last = None
+    for step in range(40):
+        layer.forward(inp["x"])
+        torch.cuda.synchronize()
+        counts = layer.out["counts_req"].cpu().numpy()
+        imax = O.max_mean_imbalance(counts)
+        first = imax if first is None else first
+        last = imax
+        before = b.cpu().numpy().copy()
+        moe.moe_bias_update(spec.N, layer.out["counts_req"], 0.05, b)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(b.cpu().numpy(), O.bias_update(before, counts, 0.05))
+    assert last < 0.6 * first, (first, last)

@@ -26,8 +26,8 @@ def _route(moe, cfg, inp):
     ws = moe.alloc_workspace(cfg)
     idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
     w = torch.empty((T, K), dtype=torch.float32, device="cuda")
-    moe.moe_route(cfg, inp["x"], inp["W_router"], inp["router_bias"], inp["shared_gate_w"], idx, w,
-                  None, None, ws)
+    moe.moe_route(cfg, inp["x"], inp["W_router"], inp["router_bias"], None, inp["shared_gate_w"],
+                  idx, w, None, None, ws)
     return idx, ws
 
 
