@@ -229,6 +229,15 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
                              const moe_outputs* out, void* workspace, size_t workspace_bytes,
                              cudaStream_t stream);
 
+/* moe_layer_forward that also records five caller-created CUDA events on the stream: before
+ * the router, and after the router, the permutation, the routed experts, and the shared
+ * expert + combine (per-stage timing of the exact call a user makes).  events: HOST array
+ * of 5 events. */
+moe_status moe_layer_forward_profiled(const moe_config* cfg, const moe_weights* w, const void* x,
+                                      const moe_outputs* out, void* workspace,
+                                      size_t workspace_bytes, cudaStream_t stream,
+                                      cudaEvent_t* events);
+
 /* Eq. 75: merge n_parts ungated shared experts into one.  Part j has width widths[j] (HOST array);
  * gate_parts[j], up_parts[j] are [widths[j]][d], down_parts[j] is [d][widths[j]] (HOST arrays of
  * DEVICE pointers).  Out: Ws_gate, Ws_up [sum widths][d] (rows concatenated), Ws_down

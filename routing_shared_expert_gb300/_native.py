@@ -74,6 +74,8 @@ def _load():
         "moe_shared_mlp": ([C, P, P, P, P, P, P, c_size_t, P], c_int32),
         "moe_combine": ([C, P, P, P, P, P, P, P], c_int32),
         "moe_layer_forward": ([C, POINTER(moe_weights), P, POINTER(moe_outputs), P, c_size_t, P], c_int32),
+        "moe_layer_forward_profiled": ([C, POINTER(moe_weights), P, POINTER(moe_outputs), P, c_size_t, P,
+                                        POINTER(c_void_p)], c_int32),
         "moe_merge_shared": ([c_int32, c_int32, c_int32, POINTER(c_int32), POINTER(c_void_p),
                               POINTER(c_void_p), POINTER(c_void_p), P, P, P, P], c_int32),
         "moe_read_status": ([P, POINTER(c_int32), P], c_int32),
@@ -258,6 +260,22 @@ def moe_layer_forward(cfg, weights: moe_weights, x, outputs: moe_outputs, worksp
     _check("moe_layer_forward", _lib.moe_layer_forward(
         ctypes.byref(cfg), ctypes.byref(weights), _ptr(x), ctypes.byref(outputs), _ptr(workspace),
         workspace.numel(), _stream(stream)))
+
+
+def moe_layer_forward_profiled(cfg, weights: moe_weights, x, outputs: moe_outputs, workspace, events,
+                               stream=None):
+    """moe_layer_forward recording 5 torch.cuda.Event objects (created with enable_timing):
+    before the router and after the router, the permutation, the routed experts and the
+    shared expert + combine."""
+    handles = []
+    for ev in events:
+        if ev.cuda_event == 0:       # torch creates the event on first record
+            ev.record()
+        handles.append(ev.cuda_event)
+    arr = (c_void_p * 5)(*handles)
+    _check("moe_layer_forward_profiled", _lib.moe_layer_forward_profiled(
+        ctypes.byref(cfg), ctypes.byref(weights), _ptr(x), ctypes.byref(outputs), _ptr(workspace),
+        workspace.numel(), _stream(stream), arr))
 
 
 def moe_merge_shared(d_model, dtype, gate_parts, up_parts, down_parts, Ws_gate, Ws_up, Ws_down,

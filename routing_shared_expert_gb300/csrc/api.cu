@@ -359,9 +359,17 @@ moe_status moe_combine(const moe_config* cfg, const void* f, const int32_t* rout
   return do_combine(*cfg, f, route_pos, topk_w, g, shared_coef, y, nullptr, stream);
 }
 
-moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x,
-                             const moe_outputs* out, void* workspace, size_t workspace_bytes,
-                             cudaStream_t stream) {
+}  // extern "C"
+
+namespace moe {
+namespace {
+
+// The layer forward; when `ev` is non-null, events [0..4] are recorded on the stream before
+// the router and after the router, the permutation, the routed experts, and the shared
+// expert + combine.
+moe_status layer_forward(const moe_config* cfg, const moe_weights* w, const void* x,
+                         const moe_outputs* out, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream, cudaEvent_t* ev) {
   moe_status s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   if (!w || !out || (!out->y && cfg->T > 0)) return MOE_ERR_INVALID_ARG;
@@ -373,32 +381,62 @@ moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const 
     using P = std::remove_pointer_t<decltype(user)>;
     return user ? user : at<P>(ws, off);
   };
+  auto mark = [&](int i) {
+    return (ev && cudaEventRecord(ev[i], stream) != cudaSuccess) ? MOE_ERR_CUDA : MOE_OK;
+  };
   int32_t* idx = pick(out->topk_idx, L.topk_idx);
   float* tw = pick(out->topk_w, L.topk_w);
   float* sc = pick(out->shared_coef, L.shared_coef);
   int32_t* status = at<int32_t>(ws, L.status);
+  if ((s = mark(0)) != MOE_OK) return s;
   if ((s = do_route(c, x, w->W_router, w->router_bias, w->selection_bias, w->shared_gate_w, idx,
                     tw, sc, out->logits, status, stream)) != MOE_OK)
     return s;
+  if ((s = mark(1)) != MOE_OK) return s;
   PermOut po{pick(out->counts_req, L.counts_req), pick(out->counts_keep, L.counts_keep),
              pick(out->offsets, L.offsets),       pick(out->route_pos, L.route_pos),
              pick(out->perm_src, L.perm_src),     pick(out->R_req, L.R_req),
              pick(out->R_keep, L.R_keep),         pick(out->drop_stats, L.drop_stats),
              at<void>(ws, L.x_perm)};
   if ((s = do_permute(c, L, ws, x, idx, po, stream)) != MOE_OK) return s;
+  if ((s = mark(2)) != MOE_OK) return s;
   void* f = at<void>(ws, L.f);
   // Packed rows: one copy pass, then plain tile loads in the GEMM (a gathered A-load
   // through perm_src needs 32 four-row TMA gathers per stage and runs far slower).
   if ((s = do_grouped(c, L, ws, po.x_perm, po.offsets, nullptr, w->W_gate, w->W_up, w->W_down, f,
                       true, stream)) != MOE_OK)
     return s;
+  if ((s = mark(3)) != MOE_OK) return s;
   void* g = nullptr;
   if (c.d_shared > 0) {
     g = at<void>(ws, L.g);
     if ((s = do_shared(c, L, ws, x, w->Ws_gate, w->Ws_up, w->Ws_down, g, stream)) != MOE_OK)
       return s;
   }
-  return do_combine(c, f, po.route_pos, tw, g, g ? sc : nullptr, out->y, status, stream);
+  if ((s = do_combine(c, f, po.route_pos, tw, g, g ? sc : nullptr, out->y, status, stream)) != MOE_OK)
+    return s;
+  return mark(4);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x,
+                             const moe_outputs* out, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+  return layer_forward(cfg, w, x, out, workspace, workspace_bytes, stream, nullptr);
+}
+
+moe_status moe_layer_forward_profiled(const moe_config* cfg, const moe_weights* w, const void* x,
+                                      const moe_outputs* out, void* workspace,
+                                      size_t workspace_bytes, cudaStream_t stream,
+                                      cudaEvent_t* events) {
+  if (!events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  return layer_forward(cfg, w, x, out, workspace, workspace_bytes, stream, events);
 }
 
 moe_status moe_merge_shared(int32_t d_model, int32_t dtype, int32_t n_parts, const int32_t* widths,

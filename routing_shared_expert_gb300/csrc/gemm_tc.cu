@@ -354,13 +354,6 @@ EncodeFn encode_fn() {
   return fn;
 }
 
-int sm_count() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
-}
-
 size_t smem_bytes(int groups) {
   return 1024 + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5) + 16 + 8 * (groups + 1) + 64;
 }
@@ -371,10 +364,10 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
   if (max_tiles <= 0) return cudaSuccess;
   const size_t smem = smem_bytes(args.groups);
   auto kern = tc_grouped_gemm<SWIGLU>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
+  const int sms = device_sm_count();
+  const int grid = static_cast<int>(max_tiles < sms ? max_tiles : sms);
   kern<<<grid, THREADS, smem, s>>>(a, b0, b1, args);
   return cudaGetLastError();
 }
@@ -382,16 +375,89 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
 }  // namespace
 
 // 2-D bf16 tensor [rows][inner] (row-major, dense), box 64 x box_rows, 128-byte swizzle.
+// Encoded maps are cached (keyed by device, address, shape and box) so that repeated
+// layer calls on the same buffers cost no driver work on the host.
 bool make_bf16_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  struct Entry {
+    int dev;
+    const void* base;
+    uint64_t inner, rows;
+    uint32_t box;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int n = 0, next = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+      if (cache[i].dev == dev && cache[i].base == base && cache[i].inner == inner &&
+          cache[i].rows == rows && cache[i].box == box_rows) {
+        *m = cache[i].map;
+        return true;
+      }
+  }
   EncodeFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry& e = cache[next];
+  e.dev = dev;
+  e.base = base;
+  e.inner = inner;
+  e.rows = rows;
+  e.box = box_rows;
+  e.map = *m;
+  next = (next + 1) % 64;
+  if (n < 64) ++n;
+  return true;
+}
+
+cudaError_t set_smem_once(const void* func, size_t bytes) {
+  struct Entry {
+    const void* func;
+    int dev;
+    size_t bytes;
+  };
+  static std::mutex mu;
+  static Entry seen[64];
+  static int n = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (seen[i].func == func && seen[i].dev == dev && seen[i].bytes >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < n; ++i)
+    if (seen[i].func == func && seen[i].dev == dev) {
+      seen[i].bytes = bytes;
+      return cudaSuccess;
+    }
+  if (n < 64) seen[n++] = Entry{func, dev, bytes};
+  return cudaSuccess;
+}
+
+int device_sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 1;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
 }
 
 cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {

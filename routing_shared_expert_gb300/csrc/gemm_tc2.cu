@@ -64,6 +64,10 @@ struct PairArgs {
   int64_t src_rows;          // rows of x
 };
 
+// Epilogue modes of the pair kernel.
+constexpr int kSwiGLU = 0;    // h = SiLU(gate) * up, bf16
+constexpr int kPlain = 1;     // fp32 rows
+
 struct Tile {
   int g, m, n, seg_start, seg_end;
 };
@@ -86,10 +90,11 @@ __device__ __forceinline__ bool pair_tile(const int* s_tp, const int* s_off, int
   return true;
 }
 
-template <bool SWIGLU>
+template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_pair_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                  const __grid_constant__ CUtensorMap tmB1, const PairArgs args) {
+  constexpr bool SWIGLU = MODE == kSwiGLU;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -360,28 +365,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
-int sm_count_pair() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n >= 2 ? n : 2;
-}
-
 size_t pair_smem_bytes(int groups) {
   return 1024 + STAGES * STAGE_BYTES + EPI_BYTES + 8 * (2 * STAGES + 5) + 16 +
          8 * (static_cast<size_t>(groups) + 1) + 64;
 }
 
-template <bool SWIGLU>
+template <int MODE>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                         const PairArgs& args, int64_t max_pair_tiles, cudaStream_t s) {
   if (max_pair_tiles <= 0) return cudaSuccess;
   const size_t smem = pair_smem_bytes(args.offsets ? args.groups : 1);
-  auto kern = tc_pair_gemm<SWIGLU>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  auto kern = tc_pair_gemm<MODE>;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  const int64_t pairs_max = sm_count_pair() / 2;
+  const int64_t pairs_max = device_sm_count() >= 2 ? device_sm_count() / 2 : 1;
   const int64_t pairs = max_pair_tiles < pairs_max ? max_pair_tiles : pairs_max;
   kern<<<static_cast<unsigned>(2 * pairs), THREADS, smem, s>>>(a, b0, b1, args);
   return cudaGetLastError();
@@ -419,7 +416,7 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.b_rows_per_group = p.width;
   a.out = p.h;
   a.ldo = p.width;
-  cudaError_t e = launch_pair<true>(mA, mG, mU, a, mt_ub * ((p.width + 127) / 128), s);
+  cudaError_t e = launch_pair<kSwiGLU>(mA, mG, mU, a, mt_ub * ((p.width + 127) / 128), s);
   if (e != cudaSuccess) return e;
 
   a.k_dim = p.width;
@@ -428,7 +425,7 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.out = p.out;
   a.ldo = p.d;
   a.gather_src = nullptr;    // h is packed
-  return launch_pair<false>(mH, mD, mD, a, mt_ub * ((p.d + 255) / 256), s);
+  return launch_pair<kPlain>(mH, mD, mD, a, mt_ub * ((p.d + 255) / 256), s);
 }
 
 }  // namespace moe

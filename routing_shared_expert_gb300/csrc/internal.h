@@ -57,6 +57,11 @@ cudaError_t launch_route_tc(const RouteParams& p, cudaStream_t s);
 // 128-byte swizzle, zero fill out of bounds.  False if the driver rejects it.
 bool make_bf16_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 
+// Raise a kernel's dynamic shared-memory limit once per device (host-side cache).
+cudaError_t set_smem_once(const void* func, size_t bytes);
+// Multiprocessor count of the current device (cached).
+int device_sm_count();
+
 // ---- counting, capacity, permutation ----------------------------------------
 struct PermuteParams {
   const void* x;
@@ -88,6 +93,21 @@ cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s);
 cudaError_t launch_tile_prefix(const int32_t* offsets, int32_t N, int32_t* tile_prefix,
                                int32_t* status, cudaStream_t s);
 
+// ---- combine -------------------------------------------------------------------
+struct CombineParams {
+  const void* f;
+  const int32_t* route_pos;
+  const float* topk_w;
+  const void* g;
+  const float* shared_coef;
+  float* y;
+  int64_t T;
+  int32_t d, K;
+  int64_t f_rows;             // rows of f (positions must be below)
+  int32_t* status;
+};
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+
 // ---- expert GEMMs -------------------------------------------------------------
 // One grouped SwiGLU MLP over packed segments (groups = N routed experts) or over
 // one dense block of rows (groups = 1, offsets == nullptr, rows = dense_rows).
@@ -118,20 +138,7 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s);   // CTA p
 inline bool use_pair_tiles(int64_t rows, int32_t groups) { return rows >= 384LL * groups; }
 cudaError_t launch_mlp_f32(const MlpParams& p, cudaStream_t s);
 
-// ---- combine -------------------------------------------------------------------
-struct CombineParams {
-  const void* f;
-  const int32_t* route_pos;
-  const float* topk_w;
-  const void* g;
-  const float* shared_coef;
-  float* y;
-  int64_t T;
-  int32_t d, K;
-  int64_t f_rows;             // rows of f (positions must be below)
-  int32_t* status;
-};
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+
 
 // ---- balancing statistics ------------------------------------------------------
 cudaError_t launch_balance_stats(const moe_config& c, const float* logits, float* partial,

@@ -214,8 +214,7 @@ cudaError_t launch_t(const RouteParams& p, cudaStream_t s) {
   const size_t smem =
       sizeof(float) * (kTokens * (kChunk + 1) + ncols * (kChunk + 1) + kTokens * (ncols + 1));
   auto kern = route_kernel<T, MAXC>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (p.T + kTokens - 1) / kTokens;
   kern<<<static_cast<unsigned>(blocks), kThreads, smem, s>>>(p);

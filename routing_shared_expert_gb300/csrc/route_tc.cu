@@ -313,8 +313,7 @@ cudaError_t launch_route_tc(const RouteParams& p, cudaStream_t s) {
   if (a.stages < 2) a.stages = 2;
   const size_t smem = 1024 + static_cast<size_t>(a.stages) * a.stage_bytes + 8 * 20 + 16 +
                       2 * sizeof(float) * kMaxExperts + 64;
-  cudaError_t e = cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(route_tc_kernel), smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>((p.T + BM - 1) / BM);
   route_tc_kernel<<<grid, THREADS, smem, s>>>(mX, mW, mG, a);

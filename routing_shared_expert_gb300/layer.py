@@ -71,6 +71,12 @@ class MoELayer:
         nat.moe_layer_forward(self.cfg, self.w, x, outs, self.ws, stream)
         return self.out["y"]
 
+    def forward_profiled(self, x: torch.Tensor, events, stream=None, logits: bool = False):
+        """forward() with 5 events recorded inside the call (see moe_layer_forward_profiled)."""
+        outs = self.outputs if logits else self._no_logits()
+        nat.moe_layer_forward_profiled(self.cfg, self.w, x, outs, self.ws, events, stream)
+        return self.out["y"]
+
     def _no_logits(self):
         if not hasattr(self, "_outputs_nolog"):
             d = {k: v for k, v in self.out.items() if k != "logits"}

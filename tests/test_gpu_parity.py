@@ -179,6 +179,20 @@ def test_merge_shared_on_device():
     assert rel_err(layer.out["y"].cpu().double().numpy(), y_ref) <= TOL["f32"]
 
 
+@pytest.mark.parametrize("name", ["olmo_s", "mixtral_s"])
+def test_profiled_forward_equals_forward(name):
+    spec, inp = _spec_and_inputs(name)
+    import routing_shared_expert_gb300 as moe
+    layer = moe.MoELayer(moe.config_from_spec(spec), inp, "cuda")
+    y1 = layer.forward(inp["x"]).clone()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    y2 = layer.forward_profiled(inp["x"], ev).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
+    assert all(t >= 0 for t in times) and sum(times) > 0
+
+
 def test_two_calls_reuse_workspace():
     spec, inp = _spec_and_inputs("mixtral_s")
     import routing_shared_expert_gb300 as moe
