@@ -97,7 +97,7 @@ __device__ __forceinline__ bool tile_coords(const TcArgs& a, const int* s_tp, co
   return true;
 }
 
-template <bool SWIGLU>
+template <bool SWIGLU, bool GATHER>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
@@ -154,9 +154,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Lane 0 waits for free stages, arms the barrier and loads B (and A when A is
-    // packed); when A is gathered every lane loads four of the tile's 128 rows.
-    const bool gather = args.gather_src != nullptr;
     int stage = 0;
     uint32_t phase = 0;
     int issued_parity[STAGES];
@@ -164,36 +161,62 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
     bool ok = true;
     Tile tl;
-    for (int64_t t = blockIdx.x; (gather || lane == 0) && ok && tile_coords(args, s_tp, s_off, n_tiles, t, tl);
-         t += gridDim.x) {
-      const int a_row = tl.seg_start + tl.m * BM;
-      const int b_row = tl.g * args.b_rows_per_group + tl.n * BN_OUT;
-      int32_t src[4] = {0, 0, 0, 0};
-      if (gather)
+    if constexpr (!GATHER) {
+      // Lane 0 alone: wait for a free stage, arm its barrier, load A and B.
+      if (lane == 0) {
+        for (int64_t t = blockIdx.x; ok && tile_coords(args, s_tp, s_off, n_tiles, t, tl);
+             t += gridDim.x) {
+          const int a_row = tl.seg_start + tl.m * BM;
+          const int b_row = tl.g * args.b_rows_per_group + tl.n * BN_OUT;
+          for (int kb = 0; kb < k_blocks; ++kb) {
+            if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
+                                   kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = smem_u32(&full[stage]);
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            const uint32_t sA = smem_base + stage * STAGE_BYTES;
+            const uint32_t sB = sA + A_BYTES;
+            tma_load_2d(sA, &tmA, kb * BK, a_row, fb);
+            tma_load_2d(sB, &tmB0, kb * BK, b_row, fb);
+            if (SWIGLU) tma_load_2d(sB + B_BYTES / 2, &tmB1, kb * BK, b_row, fb);
+            issued_parity[stage] = static_cast<int>(phase);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+    } else {
+      // Whole warp: lane 0 waits and loads B; every lane gathers four of the 128 A rows.
+      for (int64_t t = blockIdx.x; ok && tile_coords(args, s_tp, s_off, n_tiles, t, tl);
+           t += gridDim.x) {
+        const int a_row = tl.seg_start + tl.m * BM;
+        const int b_row = tl.g * args.b_rows_per_group + tl.n * BN_OUT;
+        int32_t src[4];
         gather_rows4(args.gather_src, args.gather_cap, a_row + 4 * lane, tl.seg_start, tl.seg_end,
                      args.src_rows, args.status, src);
-      for (int kb = 0; kb < k_blocks; ++kb) {
-        bool go = true;
-        if (lane == 0)
-          go = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
-                                 kWaitLimitNs);
-        if (gather) go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
-        if (!go) {
-          ok = false;
-          break;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          bool go = true;
+          if (lane == 0)
+            go = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
+                                   kWaitLimitNs);
+          go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+          if (!go) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[stage]);
+          const uint32_t sA = smem_base + stage * STAGE_BYTES;
+          const uint32_t sB = sA + A_BYTES;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            tma_load_2d(sB, &tmB0, kb * BK, b_row, fb);
+            if (SWIGLU) tma_load_2d(sB + B_BYTES / 2, &tmB1, kb * BK, b_row, fb);
+            issued_parity[stage] = static_cast<int>(phase);
+          }
+          tma_gather4(sA + lane * 512, &tmA, kb * BK, src, fb);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        const uint32_t fb = smem_u32(&full[stage]);
-        const uint32_t sA = smem_base + stage * STAGE_BYTES;
-        const uint32_t sB = sA + A_BYTES;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          if (!gather) tma_load_2d(sA, &tmA, kb * BK, a_row, fb);
-          tma_load_2d(sB, &tmB0, kb * BK, b_row, fb);
-          if (SWIGLU) tma_load_2d(sB + B_BYTES / 2, &tmB1, kb * BK, b_row, fb);
-          issued_parity[stage] = static_cast<int>(phase);
-        }
-        if (gather) tma_gather4(sA + lane * 512, &tmA, kb * BK, src, fb);
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
     if (!ok && lane == 0) {
@@ -358,12 +381,12 @@ size_t smem_bytes(int groups) {
   return 1024 + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5) + 16 + 8 * (groups + 1) + 64;
 }
 
-template <bool SWIGLU>
+template <bool SWIGLU, bool GATHER>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                        const TcArgs& args, int64_t max_tiles, cudaStream_t s) {
   if (max_tiles <= 0) return cudaSuccess;
   const size_t smem = smem_bytes(args.groups);
-  auto kern = tc_grouped_gemm<SWIGLU>;
+  auto kern = tc_grouped_gemm<SWIGLU, GATHER>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int sms = device_sm_count();
@@ -493,7 +516,9 @@ cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {
   a.b_rows_per_group = p.width;
   a.out = p.h;
   a.ldo = p.width;
-  cudaError_t e = launch_one<true>(mA, mG, mU, a, mt_ub * ((p.width + 127) / 128), s);
+  const int64_t gu_tiles = mt_ub * ((p.width + 127) / 128);
+  cudaError_t e = gather ? launch_one<true, true>(mA, mG, mU, a, gu_tiles, s)
+                         : launch_one<true, false>(mA, mG, mU, a, gu_tiles, s);
   if (e != cudaSuccess) return e;
 
   // down -> out (h is packed)
@@ -503,7 +528,7 @@ cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {
   a.b_rows_per_group = p.d;
   a.out = p.out;
   a.ldo = p.d;
-  return launch_one<false>(mH, mD, mD, a, mt_ub * ((p.d + 255) / 256), s);
+  return launch_one<false, false>(mH, mD, mD, a, mt_ub * ((p.d + 255) / 256), s);
 }
 
 }  // namespace moe

@@ -90,7 +90,7 @@ __device__ __forceinline__ bool pair_tile(const int* s_tp, const int* s_off, int
   return true;
 }
 
-template <int MODE>
+template <int MODE, bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_pair_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                  const __grid_constant__ CUtensorMap tmB1, const PairArgs args) {
@@ -181,10 +181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
-    // Lane 0 waits for free stages, arms the even CTA's barrier and loads B (and A when
-    // A is packed); when A is gathered every lane loads four of the 128 rows.
     const CUtensorMap* mapB = (SWIGLU && !leader) ? &tmB1 : &tmB0;
-    const bool gather = args.gather_src != nullptr;
     int stage = 0;
     uint32_t phase = 0;
     int issued_parity[STAGES];
@@ -192,36 +189,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
     bool ok = true;
     Tile tl;
-    for (int64_t t = pair_id; (gather || lane == 0) && ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl);
-         t += n_pairs) {
-      const int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * BM;
-      const int b_row = SWIGLU ? tl.g * args.b_rows_per_group + tl.n * 128
-                               : tl.g * args.b_rows_per_group + tl.n * 256 + static_cast<int>(rank) * 128;
-      int32_t src[4] = {0, 0, 0, 0};
-      if (gather)
+    if constexpr (!GATHER) {
+      // Lane 0 alone: wait for a free stage, arm the even CTA's barrier, load A and B.
+      if (lane == 0) {
+        for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl); t += n_pairs) {
+          const int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * BM;
+          const int b_row = SWIGLU ? tl.g * args.b_rows_per_group + tl.n * 128
+                                   : tl.g * args.b_rows_per_group + tl.n * 256 + static_cast<int>(rank) * 128;
+          for (int kb = 0; kb < k_blocks; ++kb) {
+            if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
+                                   kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb_local = smem_u32(&full[stage]);
+            const uint32_t fb_leader = mapa_shared(fb_local, 0);
+            if (leader) mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
+            const uint32_t sA = smem_base + stage * STAGE_BYTES;
+            tma_load_2d_pair(sA, &tmA, kb * BK, a_row, fb_leader);
+            tma_load_2d_pair(sA + A_BYTES, mapB, kb * BK, b_row, fb_leader);
+            issued_parity[stage] = static_cast<int>(phase);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+    } else {
+      // Whole warp: lane 0 waits and loads B; every lane gathers four of the 128 A rows.
+      for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl); t += n_pairs) {
+        const int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * BM;
+        const int b_row = SWIGLU ? tl.g * args.b_rows_per_group + tl.n * 128
+                                 : tl.g * args.b_rows_per_group + tl.n * 256 + static_cast<int>(rank) * 128;
+        int32_t src[4];
         gather_rows4(args.gather_src, args.gather_cap, a_row + 4 * lane, tl.seg_start, tl.seg_end,
                      args.src_rows, args.status, src);
-      for (int kb = 0; kb < k_blocks; ++kb) {
-        bool go = true;
-        if (lane == 0)
-          go = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
-                                 kWaitLimitNs);
-        if (gather) go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
-        if (!go) {
-          ok = false;
-          break;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          bool go = true;
+          if (lane == 0)
+            go = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
+                                   kWaitLimitNs);
+          go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+          if (!go) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb_local = smem_u32(&full[stage]);
+          const uint32_t fb_leader = mapa_shared(fb_local, 0);
+          const uint32_t sA = smem_base + stage * STAGE_BYTES;
+          if (lane == 0) {
+            if (leader) mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
+            tma_load_2d_pair(sA + A_BYTES, mapB, kb * BK, b_row, fb_leader);
+            issued_parity[stage] = static_cast<int>(phase);
+          }
+          tma_gather4_pair(sA + lane * 512, &tmA, kb * BK, src, fb_leader);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        const uint32_t fb_local = smem_u32(&full[stage]);
-        const uint32_t fb_leader = mapa_shared(fb_local, 0);
-        const uint32_t sA = smem_base + stage * STAGE_BYTES;
-        if (lane == 0) {
-          if (leader) mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
-          if (!gather) tma_load_2d_pair(sA, &tmA, kb * BK, a_row, fb_leader);
-          tma_load_2d_pair(sA + A_BYTES, mapB, kb * BK, b_row, fb_leader);
-          issued_parity[stage] = static_cast<int>(phase);
-        }
-        if (gather) tma_gather4_pair(sA + lane * 512, &tmA, kb * BK, src, fb_leader);
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
     if (!ok && leader && lane == 0) {
@@ -370,12 +391,12 @@ size_t pair_smem_bytes(int groups) {
          8 * (static_cast<size_t>(groups) + 1) + 64;
 }
 
-template <int MODE>
+template <int MODE, bool GATHER>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                         const PairArgs& args, int64_t max_pair_tiles, cudaStream_t s) {
   if (max_pair_tiles <= 0) return cudaSuccess;
   const size_t smem = pair_smem_bytes(args.offsets ? args.groups : 1);
-  auto kern = tc_pair_gemm<MODE>;
+  auto kern = tc_pair_gemm<MODE, GATHER>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int64_t pairs_max = device_sm_count() >= 2 ? device_sm_count() / 2 : 1;
@@ -416,7 +437,9 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.b_rows_per_group = p.width;
   a.out = p.h;
   a.ldo = p.width;
-  cudaError_t e = launch_pair<kSwiGLU>(mA, mG, mU, a, mt_ub * ((p.width + 127) / 128), s);
+  const int64_t gu_tiles = mt_ub * ((p.width + 127) / 128);
+  cudaError_t e = gather ? launch_pair<kSwiGLU, true>(mA, mG, mU, a, gu_tiles, s)
+                         : launch_pair<kSwiGLU, false>(mA, mG, mU, a, gu_tiles, s);
   if (e != cudaSuccess) return e;
 
   a.k_dim = p.width;
@@ -425,7 +448,7 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.out = p.out;
   a.ldo = p.d;
   a.gather_src = nullptr;    // h is packed
-  return launch_pair<kPlain>(mH, mD, mD, a, mt_ub * ((p.d + 255) / 256), s);
+  return launch_pair<kPlain, false>(mH, mD, mD, a, mt_ub * ((p.d + 255) / 256), s);
 }
 
 }  // namespace moe
