@@ -27,6 +27,26 @@ METRIC = "MoE-layer fwd tokens/s and TFLOP/s (% of BF16 peak) on 1 GB300"
 NOMINAL_HBM_GBS = 8000.0
 
 
+# DRAM traffic of the dominant stage (the routed gate/up and down launches of one
+# moe_grouped_swiglu call), dram__bytes_read.sum + dram__bytes_write.sum summed over the
+# two launches, from one `ncu --set full` capture per workload (profiles/grouped_gemm_olmo.md).
+# It is reported only while the kernel sources hash to the value they had at capture time.
+STAGE_TRAFFIC = {"olmo": {"sources_sha256": "f0289a26f6fced86", "bytes": 2059274296}}
+TRAFFIC_SOURCES = ("routing_shared_expert_gb300/csrc/gemm_tc2.cu", "routing_shared_expert_gb300/csrc/common.cuh")
+
+
+def stage_traffic(name: str):
+    import hashlib
+    rec = STAGE_TRAFFIC.get(name)
+    if rec is None:
+        return None
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return rec["bytes"] if h.hexdigest()[:16] == rec["sources_sha256"] else None
+
+
 def peaks():
     p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -41,7 +61,7 @@ def peaks():
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -57,12 +77,14 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0: float = None, t1: float = None):
+        """Summarise the samples taken between wall-clock times t0 and t1 (the timed
+        region); if none fell inside it, the samples nearest to it are used instead."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -74,38 +96,133 @@ class ClockSampler:
         rows = []
         with open(self.path) as fh:
             for r in csv.reader(fh):
-                if len(r) >= 9:
+                if len(r) >= 10:
                     rows.append([c.strip() for c in r])
         os.unlink(self.path)
-        if not rows:
+        return summarize_clocks(rows, t0, t1)
+
+
+def _stamp(text: str):
+    import datetime
+    for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+        try:
+            return datetime.datetime.strptime(text, fmt).timestamp()
+        except ValueError:
+            pass
+    return None
+
+
+def summarize_clocks(rows, t0=None, t1=None):
+    """rows: nvidia-smi CSV records (timestamp, index, sm, max sm, power, active, four reasons)."""
+    if not rows:
+        return None
+    stamped = [(_stamp(r[0]), r) for r in rows]
+    inside = [r for t, r in stamped if t is not None and t0 is not None and t0 <= t <= t1]
+    window = "timed region"
+    if not inside and t0 is not None:
+        near = sorted((abs(t - 0.5 * (t0 + t1)), i) for i, (t, _) in enumerate(stamped) if t is not None)
+        inside = [stamped[i][1] for _, i in near[:2]]
+        window = "nearest samples (timed region shorter than the sampling interval)"
+    if not inside:
+        inside, window = rows, "whole run"
+
+    def num(v):
+        try:
+            return float(v)
+        except ValueError:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+    sm = [v for v in (num(r[2]) for r in inside) if v is not None]
+    mx = [v for v in (num(r[3]) for r in inside) if v is not None]
+    pw = [v for v in (num(r[4]) for r in inside) if v is not None]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in inside for i in range(4) if r[6 + i].lower() == "active"})
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(mx) if mx else None,
+            "power_w": statistics.median(pw) if pw else None,
+            "reasons": reasons, "samples": len(inside), "window": window}
+
+
+def max_over_ranks(values, device, world: int):
+    """Each rank's totals -> the element-wise maximum over ranks (the slowest rank sets
+    the job's time)."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: the tokens all ranks processed over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (total_ms / 1e3)
 
 
 # ----------------------------------------------------------------- oracle timing
 
-def time_oracle(spec, inp_host, budget_s: float, min_tokens: int = 64):
-    """Run the oracle on the first S tokens of the workload; S sized for ~budget_s seconds."""
-    import oracle as O
+class ExpertsF64:
+    """Per-expert float64 copies of a [N, ...] weight tensor, converted on first use and
+    kept (up to a host-memory cap): the oracle's inputs held resident in its own number
+    format, as the GPU arm's are held resident in HBM.  The conversion is input
+    preparation, so timed oracle runs are repeated until no conversion happens in them."""
 
-    def run(S):
-        sub = spec.replace(T=S)
-        d = dict(inp_host)
-        d["x"] = inp_host["x"][:S]
+    CAP_BYTES = 24 << 30
+    held = 0            # bytes cached over all instances
+    conversions = 0     # conversions so far (a timed run must add none)
+
+    def __init__(self, t):
+        self.t, self.cache = t, {}
+
+    def __getitem__(self, e):
+        if e in self.cache:
+            return self.cache[e]
+        import oracle as O
+        a = O.f64(self.t[e])
+        ExpertsF64.conversions += 1
+        if ExpertsF64.held + a.nbytes <= ExpertsF64.CAP_BYTES:
+            self.cache[e] = a
+            ExpertsF64.held += a.nbytes
+        return a
+
+
+def oracle_inputs(inp_host: dict) -> dict:
+    import oracle as O
+    out = {}
+    for k, v in inp_host.items():
+        if k in ("W_gate", "W_up", "W_down"):
+            out[k] = ExpertsF64(v)
+        elif hasattr(v, "detach") and v.is_floating_point():
+            out[k] = O.f64(v)
+        else:
+            out[k] = v
+    return out
+
+
+def oracle_seconds(spec, inp_host, S: int) -> float:
+    """Wall time of the oracle's full layer forward on the first S tokens, its weights
+    already converted (the run is repeated, at most twice more, while it converted any)."""
+    sub = spec.replace(T=S)
+    d = dict(inp_host)
+    d["x"] = inp_host["x"][:S]
+    import oracle as O
+    for _ in range(3):
+        c0 = ExpertsF64.conversions
         t0 = time.perf_counter()
         O.moe_forward(sub, d)
-        return time.perf_counter() - t0
+        t = time.perf_counter() - t0
+        if ExpertsF64.conversions == c0:
+            break
+    return t
 
+
+def time_oracle(spec, inp_host, budget_s: float, min_tokens: int = 64):
+    """Run the oracle on the first S tokens of the workload; S sized for ~budget_s seconds."""
     S = min(min_tokens, spec.T)
-    t = run(S)
+    t = oracle_seconds(spec, inp_host, S)
     while t < budget_s / 4 and S < spec.T:
         S = min(spec.T, max(S * 2, int(S * budget_s / max(t, 1e-3) / 2)))
-        t = run(S)
+        t = oracle_seconds(spec, inp_host, S)
     return S, t
 
 
@@ -186,6 +303,14 @@ def sweep_entropy(args, spec):
     return 0
 
 
+def stage_algorithmic_bytes(spec, kept: int) -> int:
+    """Bytes the grouped stage must move at least once: packed rows x_perm and the routed
+    weights (gate, up, down) read, h written and read, fp32 f written."""
+    b = spec.elem_bytes
+    d, dr, N = spec.d_model, spec.d_expert, spec.N
+    return int(kept * d * b + 3 * N * d * dr * b + 2 * kept * dr * b + kept * d * 4)
+
+
 def launches_per_step(spec) -> int:
     """Kernels moe_layer_forward launches for a layer (counted from the library's launch
     sequence): router 1; permutation 4 (count, scan, place, row copy); routed experts 2;
@@ -198,7 +323,7 @@ def launches_per_step(spec) -> int:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="olmo")
@@ -206,6 +331,10 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--sweep", choices=["entropy"], default=None,
                     help="instead of the benchmark line: grouped-GEMM throughput vs entropy deficit")
+    ap.add_argument("--forward-only", type=int, default=0, metavar="R",
+                    help="run R untimed layer forwards and exit (a short, fixed launch sequence "
+                         "for ncu captures: each forward launches the routed gate/up and down "
+                         "GEMMs, then the shared ones)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -226,10 +355,13 @@ def main():
         if rank != 0:
             return 0
         import torch
-        inp = make_inputs(spec, "cpu")
+        inp = oracle_inputs(make_inputs(spec, "cpu"))
+        # one bounded sample size S for every step, sized so the whole run takes a few minutes
+        per_step = min(args.cpu_budget, max(0.05, 150.0 / (args.warmup + args.steps)))
+        S, _ = time_oracle(spec, inp, budget_s=per_step, min_tokens=16)
         times, toks = [], 0
         for i in range(args.warmup + args.steps):
-            S, t = time_oracle(spec, inp, budget_s=min(args.cpu_budget, 6.0), min_tokens=64)
+            t = oracle_seconds(spec, inp, S)
             if i >= args.warmup:
                 times.append(t)
                 toks += S
@@ -260,6 +392,15 @@ def main():
         inp["x"] = make_inputs(spec.replace(N=1, d_expert=64, d_shared=0), dev, seed=rank)["x"]
     layer = moe.MoELayer(moe.config_from_spec(spec), inp, dev)
     x = inp["x"]
+    if args.forward_only > 0:
+        for _ in range(args.forward_only):
+            layer.forward(x, logits=False)
+        torch.cuda.synchronize()
+        if layer.status() != 0:
+            raise RuntimeError(f"layer status {layer.status()}")
+        print(json.dumps({"forward_only": args.forward_only, "workload": spec.name,
+                          "kept": int(layer.out["counts_keep"].sum())}), flush=True)
+        return 0
     stream = torch.cuda.current_stream()
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -276,22 +417,27 @@ def main():
     torch.cuda.synchronize()
     # Timed region: the fused layer call a user makes (moe_layer_forward), with four events
     # recorded inside it by the library after router, permutation, routed experts and
-    # shared expert + combine.
+    # shared expert + combine.  The steps are queued back to back (no host sync between
+    # them); the L2 flush sits between a step's last event and the next step's first.
     stage_names = ("route", "permute", "grouped_swiglu", "shared_combine")
     stage_ms = {k: 0.0 for k in stage_names}
-    step_ms = []
+    events = []
+    w0 = time.time()
     for _ in range(args.steps):
         flush.add_(1)                        # write 256 MiB (> L2) between steps
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         layer.forward_profiled(x, ev)
-        torch.cuda.synchronize()
+        events.append(ev)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop(w0, w1)
+    step_ms = []
+    for ev in events:
         step_ms.append(ev[0].elapsed_time(ev[4]))
         for i, k in enumerate(stage_names):
             stage_ms[k] += ev[i].elapsed_time(ev[i + 1])
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
 
     # end to end through the public call: pinned host x -> device, forward, y -> pinned host
     x_host = x.cpu().pin_memory()
@@ -309,16 +455,12 @@ def main():
         torch.cuda.synchronize()
         e2e.append(a.elapsed_time(b))
 
-    total_ms = sum(step_ms)
-    t_tensor = torch.tensor([total_ms, sum(e2e)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_tensor, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = float(t_tensor[0]), float(t_tensor[1])
+    total_ms, e2e_ms = max_over_ranks([sum(step_ms), sum(e2e)], dev, world)
 
     assert layer.status() == 0, "device status word set during the benchmark"
     kept = int(layer.out["counts_keep"].sum())
     ms = total_ms / args.steps
-    tokens_per_s = world * spec.T / (ms / 1e3)
+    tokens_per_s = job_tokens_per_s(world, spec.T, args.steps, total_ms)
     flops = spec.expert_flops(kept)
     tflops = world * flops / (ms / 1e3) / 1e12
     pk = peaks()
@@ -339,8 +481,10 @@ def main():
                      "bound": "tensor", "achieved": g_tf, "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": g_tf / pk["bf16_tflops"],
                      "frac_sustained": g_tf / pk["bf16_tflops_sustained"],
-                     "peak_source": pk["source"], "traffic": None},
-        "e2e": {"value": world * spec.T / (e2e_ms / args.steps / 1e3), "unit": "tokens/s",
+                     "peak_source": pk["source"], "traffic": stage_traffic(spec.name),
+                     "traffic_unit": "bytes per stage (gate/up + down launches)",
+                     "algorithmic_bytes": stage_algorithmic_bytes(spec, kept)},
+        "e2e": {"value": job_tokens_per_s(world, spec.T, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size(),
                 "d2h_bytes_per_step": layer.out["y"].numel() * 4},
         "gpu_launches": launches_per_step(spec) * args.steps,
@@ -349,7 +493,7 @@ def main():
     }
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        hin = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp.items()}
+        hin = oracle_inputs({k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp.items()})
         S, t = time_oracle(spec, hin, budget_s=args.cpu_budget)
         line["cpu_baseline"] = {"value": S / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": f"first {S} of {spec.T} tokens of the {spec.name} layer, "
