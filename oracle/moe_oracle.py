@@ -47,7 +47,7 @@ import numpy as np
 F64 = np.float64
 
 SCORES = ("softmax", "sigmoid")
-NORMS = ("none", "l1", "softmax_selected")
+NORMS = ("none", "l1", "softmax_selected", "lp")
 SHARED_MODES = ("none", "const", "gate")
 CAP_POLICIES = ("none", "per_expert", "rank_wide")
 
@@ -110,7 +110,7 @@ def sigmoid(z) -> np.ndarray:
         return 1.0 / (1.0 + np.exp(-z))
 
 
-def selected_weights(z, idx, score: str, norm: str) -> np.ndarray:
+def selected_weights(z, idx, score: str, norm: str, p: float = 2.0) -> np.ndarray:
     """Per-slot mixture weights w_t,k before the routed scale ("Appendix E", Table 52).
 
     * ``none``: w = q_S, the selected scores as they are (routed mass m_K < 1
@@ -119,6 +119,9 @@ def selected_weights(z, idx, score: str, norm: str) -> np.ndarray:
       after L1 normalisation; "Shared and Fine-Grained Experts": renormalise the k).
     * ``softmax_selected``: w = softmax(z_S), the softmax over the selected
       logits only (Mixtral row of Table 52).  It does not look at ``score``.
+    * ``lp``: w = q_S / ||q_S||_p = q_S / (sum_{j in S} q_j^p)^(1/p), the L_p
+      normalisation of the selected weights the MegaBlocks row of Table 52 offers
+      (the row names no p; it is a parameter, and p = 1 is ``l1``).
     """
     z = f64(z)
     idx = np.asarray(idx)
@@ -133,6 +136,8 @@ def selected_weights(z, idx, score: str, norm: str) -> np.ndarray:
         return qS
     if norm == "l1":
         return qS / qS.sum(axis=1, keepdims=True)
+    if norm == "lp":
+        return qS / np.power(np.power(qS, p).sum(axis=1, keepdims=True), 1.0 / p)
     raise ValueError(norm)
 
 
@@ -356,7 +361,7 @@ def route(logits, cfg, rho=None, selection_bias=None) -> Routing:
     """Steps from the logits to the packed layout, for a whole batch.
 
     ``cfg`` needs N, K, T, score, norm, alpha, cap_policy, capacity_factor,
-    num_ranks.  ``rho`` defaults to i mod num_ranks.  ``selection_bias`` is the
+    num_ranks (and norm_p for the L_p rule).  ``rho`` defaults to i mod num_ranks.  ``selection_bias`` is the
     optional Eq. 35 bias b (selection only).
     """
     z = f64(logits)
@@ -365,7 +370,7 @@ def route(logits, cfg, rho=None, selection_bias=None) -> Routing:
     if rho is None:
         rho = [i % cfg.num_ranks for i in range(N)]
     idx = select_topk(selection_keys(logits, selection_bias), K)
-    r = cfg.alpha * selected_weights(z, idx, cfg.score, cfg.norm)
+    r = cfg.alpha * selected_weights(z, idx, cfg.score, cfg.norm, getattr(cfg, "norm_p", 2.0))
     C_req = requested_counts(idx, N)
     C_keep = kept_counts(C_req, cfg.cap_policy, cfg.capacity_factor, K, T, rho, cfg.num_ranks)
     route_pos, perm_src, offsets = pack_routes(idx, C_keep, N)

@@ -256,6 +256,41 @@ def test_softmax_selected_equals_l1_on_full_softmax_and_sigmoid_sums():
         assert set(rt.topk_idx[t].tolist()) == set(np.argsort(-q[t])[:8].tolist())
 
 
+def test_lp_normalisation_pins():
+    """Table 52, MegaBlocks row: the selected weights may receive an L_p normalisation.
+    A 3-4-5 triangle by hand: softmax over logits (ln 3, ln 4, ln 1) gives q = (3, 4, 1) / 8;
+    the top 2 in slot order are experts 1, 0 and their L2-normalised weights are 4/5, 3/5."""
+    z = np.log(np.array([[3.0, 4.0, 1.0]]))
+    idx = O.select_topk(z, 2)
+    assert idx.tolist() == [[1, 0]]
+    w = O.selected_weights(z, idx, "softmax", "lp", p=2.0)
+    np.testing.assert_allclose(w[0], [0.8, 0.6], rtol=1e-14)
+    # p = 3 on selected sigmoid scores sigma(ln 3) = 3/4 and sigma(ln 1) = 1/2, by hand:
+    # ||(3/4, 1/2)||_3 = (27/64 + 8/64)^(1/3) = (35/64)^(1/3)
+    z = np.log(np.array([[3.0, 1.0]]))
+    w = O.selected_weights(z, np.array([[0, 1]]), "sigmoid", "lp", p=3.0)
+    n = (35.0 / 64.0) ** (1.0 / 3.0)
+    np.testing.assert_allclose(w[0], [0.75 / n, 0.5 / n], rtol=1e-14)
+    rng = np.random.default_rng(11)
+    z = rng.normal(size=(200, 32))
+    idx = O.select_topk(z, 4)
+    q = np.take_along_axis(O.softmax_all(z), idx, axis=1)
+    # p = 1 is the L1 rule
+    np.testing.assert_allclose(O.selected_weights(z, idx, "softmax", "lp", p=1.0),
+                               O.selected_weights(z, idx, "softmax", "l1"), rtol=1e-14)
+    for pp in (1.5, 2.0, 3.0, 8.0):
+        w = O.selected_weights(z, idx, "softmax", "lp", p=pp)
+        # unit L_p norm, and a per-token rescaling of the scores (ratios kept)
+        np.testing.assert_allclose((w ** pp).sum(1), 1.0, rtol=1e-13)
+        np.testing.assert_allclose(w / w[:, :1], q / q[:, :1], rtol=1e-13)
+    # towards L_inf: K^(-1/p) <= max_k w_k <= 1
+    w = O.selected_weights(z, idx, "softmax", "lp", p=200.0)
+    assert np.all(w.max(1) <= 1 + 1e-15) and np.all(w.max(1) >= 4 ** (-1 / 200) - 1e-15)
+    # through route(): r = alpha w with the config's p
+    rt = O.route(z, Cfg(N=32, K=4, T=200, norm="lp", norm_p=2.0, alpha=4.0))
+    np.testing.assert_allclose((rt.topk_w ** 2).sum(1), 16.0, rtol=1e-13)
+
+
 def test_sigmoid_and_softmax_closed_forms():
     assert O.sigmoid(np.array([[0.0]]))[0, 0] == 0.5
     assert abs(O.sigmoid(np.array([[math.log(3.0)]]))[0, 0] - 0.75) < 1e-15

@@ -42,7 +42,7 @@ class MoEConfig:
     d_shared: int          # shared intermediate width d_s (0 = no shared expert)
     dtype: str             # "f32" or "bf16"
     score: str             # "softmax" | "sigmoid"
-    norm: str              # "none" | "l1" | "softmax_selected"
+    norm: str              # "none" | "l1" | "softmax_selected" | "lp"
     alpha: float           # routed scale
     shared_mode: str       # "none" | "const" | "gate"
     shared_gain: float     # s when shared_mode == "const"
@@ -53,6 +53,7 @@ class MoEConfig:
     init: str              # "fan_in" (std 1/sqrt(fan_in)) or "0.02" (std 0.02)
     logit_bias: str        # "none" | "normal" (N(0,1) per expert) | "zipf1.2"
     shared_split: tuple = ()   # widths of ungated shared experts that merge into d_shared
+    norm_p: float = 2.0        # p of the "lp" rule
 
     @property
     def torch_dtype(self):
