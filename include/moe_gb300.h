@@ -69,8 +69,16 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score;
  *   NONE              w = q_S (routed mass m_K < 1 for a softmax over N > K)
  *   L1_SELECTED       w = q_S / sum_S q (Section 21.1; the Olmo and DeepSeek-V3 rows)
  *   SOFTMAX_SELECTED  w = softmax(z_S), the softmax over the selected logits (Mixtral row)
- * The routed coefficients are r = alpha * w. */
-typedef enum { MOE_NORM_NONE = 0, MOE_NORM_L1_SELECTED = 1, MOE_NORM_SOFTMAX_SELECTED = 2 } moe_norm;
+ *   LP_SELECTED       w = q_S / (sum_S q^p)^(1/p), the L_p normalisation the MegaBlocks row
+ *                     offers; p = moe_config.norm_p in [1, 64] (p = 1 is L1_SELECTED)
+ * The routed coefficients are r = alpha * w.  The same row's option of routed coefficient
+ * K/(K+1) and shared coefficient 1/(K+1) is alpha = K/(K+1) with MOE_SHARED_CONST gain 1/(K+1). */
+typedef enum {
+  MOE_NORM_NONE = 0,
+  MOE_NORM_L1_SELECTED = 1,
+  MOE_NORM_SOFTMAX_SELECTED = 2,
+  MOE_NORM_LP_SELECTED = 3
+} moe_norm;
 
 /* Shared coefficient s(x) of Eq. 80: none (0), a constant gain, or sigmoid(w_s . x) (Eq. 77). */
 typedef enum { MOE_SHARED_NONE = 0, MOE_SHARED_CONST = 1, MOE_SHARED_SIGMOID_GATE = 2 } moe_shared_mode;
@@ -98,6 +106,7 @@ typedef struct moe_config {
   double capacity_factor; /* c > 0 when a capacity policy is set */
   int32_t num_ranks;      /* M_E >= 1: destination ranks of rho (Eq. 20) */
   const int32_t* rho;     /* HOST [N], values in [0, num_ranks); NULL means rho(i) = i mod num_ranks */
+  float norm_p;           /* p of MOE_NORM_LP_SELECTED, finite, 1 <= p <= 64; ignored otherwise */
 } moe_config;
 
 /* Weights of one layer (device pointers, layouts above).  router_bias, selection_bias and

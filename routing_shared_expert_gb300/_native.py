@@ -21,7 +21,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
           -7: "MOE_ERR_MISALIGNED"}
 DTYPES = {"f32": 0, "bf16": 1}
 SCORES = {"softmax": 0, "sigmoid": 1}
-NORMS = {"none": 0, "l1": 1, "softmax_selected": 2}
+NORMS = {"none": 0, "l1": 1, "softmax_selected": 2, "lp": 3}
 SHARED_MODES = {"none": 0, "const": 1, "gate": 2}
 CAP_POLICIES = {"none": 0, "per_expert": 1, "rank_wide": 2}
 
@@ -37,7 +37,8 @@ class moe_config(ctypes.Structure):
                 ("d_expert", c_int32), ("d_shared", c_int32), ("dtype", c_int32),
                 ("score", c_int32), ("norm", c_int32), ("alpha", c_float),
                 ("shared_mode", c_int32), ("shared_gain", c_float), ("cap_policy", c_int32),
-                ("capacity_factor", c_double), ("num_ranks", c_int32), ("rho", POINTER(c_int32))]
+                ("capacity_factor", c_double), ("num_ranks", c_int32), ("rho", POINTER(c_int32)),
+                ("norm_p", c_float)]
 
 
 class moe_weights(ctypes.Structure):
@@ -105,7 +106,7 @@ def _enum(table, v):
 
 def make_config(T, d_model, N, K, d_expert, d_shared, dtype="bf16", score="softmax", norm="l1",
                 alpha=1.0, shared_mode="const", shared_gain=1.0, cap_policy="none",
-                capacity_factor=1.0, num_ranks=1, rho=None) -> moe_config:
+                capacity_factor=1.0, num_ranks=1, rho=None, norm_p=2.0) -> moe_config:
     """Build a ``moe_config``; ``rho`` (host list) is kept alive on the returned object."""
     c = moe_config()
     c.T, c.d_model, c.N, c.K = int(T), int(d_model), int(N), int(K)
@@ -119,6 +120,7 @@ def make_config(T, d_model, N, K, d_expert, d_shared, dtype="bf16", score="softm
     c.cap_policy = _enum(CAP_POLICIES, cap_policy)
     c.capacity_factor = float(capacity_factor)
     c.num_ranks = int(num_ranks)
+    c.norm_p = float(norm_p)
     if rho is not None:
         arr = (c_int32 * len(rho))(*[int(v) for v in rho])
         c._rho_keepalive = arr

@@ -24,7 +24,10 @@ moe_status check_cfg(const moe_config* c) {
   if (c->N > kMaxExperts || c->K > kMaxTopK || c->K > c->N) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
-  if (c->norm < MOE_NORM_NONE || c->norm > MOE_NORM_SOFTMAX_SELECTED) return MOE_ERR_INVALID_ARG;
+  if (c->norm < MOE_NORM_NONE || c->norm > MOE_NORM_LP_SELECTED) return MOE_ERR_INVALID_ARG;
+  if (c->norm == MOE_NORM_LP_SELECTED &&
+      !(std::isfinite(c->norm_p) && c->norm_p >= 1.f && c->norm_p <= 64.f))
+    return MOE_ERR_INVALID_ARG;
   if (c->shared_mode < MOE_SHARED_NONE || c->shared_mode > MOE_SHARED_SIGMOID_GATE)
     return MOE_ERR_INVALID_ARG;
   if ((c->d_shared > 0) != (c->shared_mode != MOE_SHARED_NONE)) return MOE_ERR_INVALID_ARG;
@@ -84,6 +87,7 @@ RouteParams route_params(const moe_config& c, const void* x, const void* W_route
   p.shared_mode = c.shared_mode;
   p.alpha = c.alpha;
   p.shared_gain = c.shared_gain;
+  p.norm_p = c.norm_p;
   p.topk_idx = idx;
   p.topk_w = w;
   p.shared_coef = s;

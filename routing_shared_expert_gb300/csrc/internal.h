@@ -43,6 +43,7 @@ struct RouteParams {
   int64_t T;
   int32_t d, N, K, score, norm, shared_mode;
   float alpha, shared_gain;
+  float norm_p;                  // p of the L_p rule
   int32_t* topk_idx;
   float* topk_w;
   float* shared_coef;

@@ -16,6 +16,7 @@
 // scores and coefficients of the selected experts in registers.
 #include "common.cuh"
 #include "internal.h"
+#include "route_norm.cuh"
 
 namespace moe {
 namespace {
@@ -188,6 +189,8 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
 #pragma unroll
         for (int k = 0; k < kMaxTopK; ++k)
           if (k < p.K) w[k] /= s;
+      } else if (p.norm == MOE_NORM_LP_SELECTED) {
+        lp_normalise(w, p.K, p.norm_p);
       }
     }
     if (lane < p.K) {

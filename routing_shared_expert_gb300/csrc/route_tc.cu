@@ -17,6 +17,7 @@
 // Every wait is bounded; a wait that runs out records MOE_ERR_TIMEOUT.
 #include "common.cuh"
 #include "internal.h"
+#include "route_norm.cuh"
 
 namespace moe {
 namespace {
@@ -259,6 +260,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int j = 0; j < kMaxTopK; ++j)
             if (j < p.K) w[j] /= s;
+        } else if (p.norm == MOE_NORM_LP_SELECTED) {
+          lp_normalise(w, p.K, p.norm_p);
         }
       }
       float shared = 0.f;

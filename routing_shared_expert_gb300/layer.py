@@ -21,7 +21,7 @@ def config_from_spec(spec, T: Optional[int] = None) -> nat.moe_config:
         norm=spec.norm, alpha=spec.alpha, shared_mode=spec.shared_mode,
         shared_gain=spec.shared_gain, cap_policy=spec.cap_policy,
         capacity_factor=spec.capacity_factor, num_ranks=spec.num_ranks,
-        rho=[i % spec.num_ranks for i in range(spec.N)])
+        rho=[i % spec.num_ranks for i in range(spec.N)], norm_p=getattr(spec, "norm_p", 2.0))
 
 
 STAGES = ("route", "permute", "grouped_swiglu", "shared_mlp", "combine")

@@ -59,7 +59,7 @@ def test_workspace_size_valid_and_monotone(nat):
 
 @pytest.mark.parametrize("field,value,status", [
     ("K", 0, -1), ("K", 33, -1), ("N", 0, -1), ("N", 300, -1), ("T", -1, -1),
-    ("dtype", 7, -1), ("score", 3, -1), ("norm", 9, -1), ("shared_mode", 0, -1),
+    ("dtype", 7, -1), ("score", 3, -1), ("norm", 9, -1), ("norm", 4, -1), ("shared_mode", 0, -1),
     ("cap_policy", 5, -1), ("num_ranks", 0, -1), ("alpha", float("nan"), -1),
     ("d_model", 100, -2), ("d_expert", 36, -2),
 ])
@@ -76,6 +76,16 @@ def test_capacity_factor_checked_only_with_a_policy(nat):
     c = _olmo(capacity_factor=-1.0, cap_policy=1)
     with pytest.raises(nat.MoEError):
         nat.moe_workspace_size(c)
+
+
+def test_lp_exponent_checked_only_with_the_lp_rule(nat):
+    for p in (1.0, 2.0, 64.0):
+        assert nat.moe_workspace_size(_olmo(norm=3, norm_p=p)) > 0
+    for p in (0.5, 0.0, -2.0, 65.0, float("nan"), float("inf")):
+        with pytest.raises(nat.MoEError):
+            nat.moe_workspace_size(_olmo(norm=3, norm_p=p))
+    # other rules ignore the field
+    assert nat.moe_workspace_size(_olmo(norm=1, norm_p=float("nan"))) > 0
 
 
 def test_rho_out_of_range_rejected(nat):

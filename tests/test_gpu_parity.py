@@ -44,6 +44,13 @@ SMALL = {
     "pair_s": C["olmo"].replace(T=1100, d_model=448, N=4, K=2, alpha=2.0, d_expert=320,
                                 d_shared=192),
     "pair_cap_s": C["mixtral"].replace(T=1600, d_model=4096, d_expert=448, capacity_factor=1.0),
+    # L_p normalisation of the selected weights (Table 52, MegaBlocks row) on both routers:
+    # the tensor-core bf16 router (softmax, p = 2; sigmoid, p = 8) and the fp32 one (p = 3)
+    "olmo_lp2": C["olmo"].replace(T=500, d_model=256, d_expert=128, d_shared=128, norm="lp",
+                                  norm_p=2.0, alpha=2.0),
+    "dsv3_lp8": C["dsv3"].replace(T=400, d_model=448, d_expert=128, d_shared=128, norm="lp",
+                                  norm_p=8.0),
+    "tiny_lp3": C["tiny"].replace(norm="lp", norm_p=3.0),
 }
 
 
