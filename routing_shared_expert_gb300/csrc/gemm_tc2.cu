@@ -12,10 +12,19 @@
 // of a one-SM 128 x 256 tile), which lets six stages sit in shared memory and
 // keeps the tensor pipe fed from L2.  Each CTA's TMEM holds the fp32
 // accumulator rows of its own 128 rows for all 256 columns.
-//   SwiGLU mode: the even CTA loads the gate weight rows, the odd CTA the up
-//                rows of the same 128 h columns, so TMEM columns [0,128) hold
-//                x W_g and [128,256) hold x W_u for the CTA's rows.
+//   SwiGLU mode: a tile covers 128 h columns.  In a full tile the even CTA loads
+//                their 128 gate weight rows and the odd CTA their 128 up rows,
+//                so TMEM columns [0,128) hold x W_g and [128,256) x W_u.  In a
+//                half tile each CTA loads the gate and the up rows of 64 of the
+//                h columns (two 64-row boxes), so that gate and up of one h
+//                column land in the same TMEM lane, 64 columns apart.
 //   Plain mode:  each CTA loads 128 of the 256 output columns' weight rows.
+// The last tile of a segment is a half tile (M = 128: 64 A rows per CTA) when at
+// most 128 of its rows are real.  A cta_group::2 MMA with M = 128 issues at twice
+// the rate of one with M = 256 (each SM computes 64 rows), so a short tail costs
+// half a tile instead of a whole one.  Its accumulator lands in TMEM lanes 0-63 for
+// B columns [0,128) and lanes 64-127 for columns [128,256), TMEM columns 0-127,
+// rows 64 r + (lane mod 64) in CTA r.
 // The gate/up A rows are either read from a packed buffer (one TMA tile load) or
 // gathered straight from x through the packed-row source table: each lane of the
 // producer warp issues one tile::gather4 of four rows, so the row permutation of
@@ -35,6 +44,7 @@ namespace {
 
 constexpr int BM = 128;                    // rows per CTA
 constexpr int PM = 256;                    // rows per pair tile
+constexpr int HM = 64;                     // rows per CTA of a half tile (M = 128)
 constexpr int BK = 64;
 constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;       // 16 KB
@@ -70,6 +80,7 @@ constexpr int kPlain = 1;     // fp32 rows
 
 struct Tile {
   int g, m, n, seg_start, seg_end;
+  bool half;   // at most BM real rows: an M = 128 tile
 };
 
 __device__ __forceinline__ bool pair_tile(const int* s_tp, const int* s_off, int G, int n_tiles,
@@ -87,13 +98,41 @@ __device__ __forceinline__ bool pair_tile(const int* s_tp, const int* s_off, int
   o.m = static_cast<int>(local % mt);
   o.seg_start = s_off[lo];
   o.seg_end = s_off[lo + 1];
+  o.half = o.seg_end - (o.seg_start + o.m * PM) <= BM;
   return true;
+}
+
+// First weight row of this CTA's B half for a tile (rows of the 2-D [groups * rows][k] view).
+template <bool SWIGLU>
+__device__ __forceinline__ int b_first_row(const PairArgs& args, const Tile& tl, uint32_t rank) {
+  const int base = tl.g * args.b_rows_per_group;
+  if (!SWIGLU) return base + tl.n * 256 + static_cast<int>(rank) * 128;
+  return base + tl.n * 128 + (tl.half ? static_cast<int>(rank) * 64 : 0);
+}
+
+// Loads this CTA's 16 KB B half of one K block.  Plain: 128 weight rows.  SwiGLU full
+// tile: the even CTA's gate rows, the odd CTA's up rows (128 each).  SwiGLU half tile:
+// 64 gate rows then the same 64 up rows.
+template <bool SWIGLU>
+__device__ __forceinline__ void load_b(uint32_t sB, bool half, bool leader, const CUtensorMap* b0,
+                                       const CUtensorMap* b1, const CUtensorMap* b0h,
+                                       const CUtensorMap* b1h, int k, int row, uint32_t bar) {
+  if (!SWIGLU) {
+    tma_load_2d_pair(sB, b0, k, row, bar);
+  } else if (!half) {
+    tma_load_2d_pair(sB, leader ? b0 : b1, k, row, bar);
+  } else {
+    tma_load_2d_pair(sB, b0h, k, row, bar);
+    tma_load_2d_pair(sB + B_BYTES / 2, b1h, k, row, bar);
+  }
 }
 
 template <int MODE, bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-    tc_pair_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                 const __grid_constant__ CUtensorMap tmB1, const PairArgs args) {
+    tc_pair_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA64,
+                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                 const __grid_constant__ CUtensorMap tmB0h, const __grid_constant__ CUtensorMap tmB1h,
+                 const PairArgs args) {
   constexpr bool SWIGLU = MODE == kSwiGLU;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -169,8 +208,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&tmA);
+    if (!GATHER) tma_prefetch_map(&tmA64);
     tma_prefetch_map(&tmB0);
-    if (SWIGLU) tma_prefetch_map(&tmB1);
+    if (SWIGLU) {
+      tma_prefetch_map(&tmB1);
+      tma_prefetch_map(&tmB0h);
+      tma_prefetch_map(&tmB1h);
+    }
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_holder), TMEM_COLS);
   __syncwarp();
@@ -181,7 +225,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
-    const CUtensorMap* mapB = (SWIGLU && !leader) ? &tmB1 : &tmB0;
     int stage = 0;
     uint32_t phase = 0;
     int issued_parity[STAGES];
@@ -193,9 +236,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // Lane 0 alone: wait for a free stage, arm the even CTA's barrier, load A and B.
       if (lane == 0) {
         for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl); t += n_pairs) {
-          const int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * BM;
-          const int b_row = SWIGLU ? tl.g * args.b_rows_per_group + tl.n * 128
-                                   : tl.g * args.b_rows_per_group + tl.n * 256 + static_cast<int>(rank) * 128;
+          const int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * (tl.half ? HM : BM);
+          const CUtensorMap* mapA = tl.half ? &tmA64 : &tmA;
+          const uint32_t tx = 2u * ((tl.half ? A_BYTES / 2 : A_BYTES) + B_BYTES);
+          const int b_row = b_first_row<SWIGLU>(args, tl, rank);
           for (int kb = 0; kb < k_blocks; ++kb) {
             if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
                                    kWaitLimitNs)) {
@@ -204,21 +248,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             }
             const uint32_t fb_local = smem_u32(&full[stage]);
             const uint32_t fb_leader = mapa_shared(fb_local, 0);
-            if (leader) mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
+            if (leader) mbar_arrive_expect_tx(fb_local, tx);
             const uint32_t sA = smem_base + stage * STAGE_BYTES;
-            tma_load_2d_pair(sA, &tmA, kb * BK, a_row, fb_leader);
-            tma_load_2d_pair(sA + A_BYTES, mapB, kb * BK, b_row, fb_leader);
+            tma_load_2d_pair(sA, mapA, kb * BK, a_row, fb_leader);
+            load_b<SWIGLU>(sA + A_BYTES, tl.half, leader, &tmB0, &tmB1, &tmB0h, &tmB1h, kb * BK, b_row,
+                           fb_leader);
             issued_parity[stage] = static_cast<int>(phase);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
         }
       }
     } else {
-      // Whole warp: lane 0 waits and loads B; every lane gathers four of the 128 A rows.
+      // Whole warp: lane 0 waits and loads B; each lane gathers four of the CTA's 128 A
+      // rows (lanes 0-15 the 64 rows of a half tile).
       for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl); t += n_pairs) {
-        const int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * BM;
-        const int b_row = SWIGLU ? tl.g * args.b_rows_per_group + tl.n * 128
-                                 : tl.g * args.b_rows_per_group + tl.n * 256 + static_cast<int>(rank) * 128;
+        const int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * (tl.half ? HM : BM);
+        const uint32_t tx = 2u * ((tl.half ? A_BYTES / 2 : A_BYTES) + B_BYTES);
+        const bool gathers = !tl.half || lane < HM / 4;
+        const int b_row = b_first_row<SWIGLU>(args, tl, rank);
         int32_t src[4];
         gather_rows4(args.gather_src, args.gather_cap, a_row + 4 * lane, tl.seg_start, tl.seg_end,
                      args.src_rows, args.status, src);
@@ -236,11 +283,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t fb_leader = mapa_shared(fb_local, 0);
           const uint32_t sA = smem_base + stage * STAGE_BYTES;
           if (lane == 0) {
-            if (leader) mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
-            tma_load_2d_pair(sA + A_BYTES, mapB, kb * BK, b_row, fb_leader);
+            if (leader) mbar_arrive_expect_tx(fb_local, tx);
+            load_b<SWIGLU>(sA + A_BYTES, tl.half, leader, &tmB0, &tmB1, &tmB0h, &tmB1h, kb * BK, b_row,
+                           fb_leader);
             issued_parity[stage] = static_cast<int>(phase);
           }
-          tma_gather4_pair(sA + lane * 512, &tmA, kb * BK, src, fb_leader);
+          if (gathers) tma_gather4_pair(sA + lane * 512, &tmA, kb * BK, src, fb_leader);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -255,7 +303,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (leader && lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(PM, 256);
+      constexpr uint32_t idesc_full = idesc_bf16_f32(PM, 256);
+      constexpr uint32_t idesc_half = idesc_bf16_f32(2 * HM, 256);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -272,6 +321,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_acc = tmem_base + static_cast<uint32_t>(buf * 256);
+        const uint32_t idesc = tl.half ? idesc_half : idesc_full;
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, args.status,
                                  kWaitLimitNs)) {
@@ -313,16 +363,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
       if (!ready) break;
       tc_fence_after();
-      const int64_t row0 = static_cast<int64_t>(tl.seg_start) + tl.m * PM + rank * BM + q * 32;
+      // Full tile: warp q holds rows 128 r + 32 q .. of all 256 accumulator columns.
+      // Half tile: warp q holds rows 64 r + 32 (q mod 2) .. of accumulator columns
+      // [128 (q / 2), 128 (q / 2) + 128), found in TMEM columns 0-127.
+      const int hq = q >> 1;
+      const int64_t row0 = static_cast<int64_t>(tl.seg_start) + tl.m * PM +
+                           (tl.half ? rank * HM + (q & 1) * 32 : rank * BM + q * 32);
       const int64_t row_end = tl.seg_end < args.out_rows ? tl.seg_end : args.out_rows;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(buf * 256);
       if (SWIGLU) {
+        // full tile: gate of h column j in TMEM column j, up in 128 + j; half tile: the
+        // warp's 64 h columns with gate in TMEM columns [0,64) and up in [64,128)
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+        const int chunks = tl.half ? 2 : 4;
+        const int up_off = tl.half ? 64 : 128;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < chunks; ++c) {
+          const int hcol = tl.n * 128 + (tl.half ? hq * 64 : 0) + 32 * c;
           uint32_t gr[32], ur[32];
-          tmem_ld32x2(taddr + c * 32, taddr + 128 + c * 32, gr, ur);
+          tmem_ld32x2(taddr + 32 * c, taddr + 32 * c + up_off, gr, ur);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint32_t w4[4];
@@ -340,7 +400,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           for (int pass = 0; pass < 4; ++pass) {
             const int r = pass * 8 + lane / 4;
             const int64_t row = row0 + r;
-            const int col = tl.n * 128 + c * 32 + (lane % 4) * 8;
+            const int col = hcol + (lane % 4) * 8;
             const uint4 val = *reinterpret_cast<const uint4*>(stg + r * EPI_LD + (lane % 4) * 4);
             if (row < row_end && col + 8 <= args.n_out)
               *reinterpret_cast<uint4*>(out + row * args.ldo + col) = val;
@@ -349,8 +409,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
       } else {
         float* out = static_cast<float*>(args.out);
+        const int chunks = tl.half ? 4 : 8;
+        const int col_base = tl.n * 256 + (tl.half ? hq * 128 : 0);
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < chunks; ++c) {
           uint32_t ar[32];
           tmem_ld32(taddr + c * 32, ar);
 #pragma unroll
@@ -363,7 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           for (int pass = 0; pass < 8; ++pass) {
             const int r = pass * 4 + lane / 8;
             const int64_t row = row0 + r;
-            const int col = tl.n * 256 + c * 32 + (lane % 8) * 4;
+            const int col = col_base + c * 32 + (lane % 8) * 4;
             const uint4 val = *reinterpret_cast<const uint4*>(stg + r * EPI_LD + (lane % 8) * 4);
             if (row < row_end && col + 4 <= args.n_out)
               *reinterpret_cast<uint4*>(out + row * args.ldo + col) = val;
@@ -392,7 +454,8 @@ size_t pair_smem_bytes(int groups) {
 }
 
 template <int MODE, bool GATHER>
-cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a64, const CUtensorMap& b0,
+                        const CUtensorMap& b1, const CUtensorMap& b0h, const CUtensorMap& b1h,
                         const PairArgs& args, int64_t max_pair_tiles, cudaStream_t s) {
   if (max_pair_tiles <= 0) return cudaSuccess;
   const size_t smem = pair_smem_bytes(args.offsets ? args.groups : 1);
@@ -401,7 +464,7 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUten
   if (e != cudaSuccess) return e;
   const int64_t pairs_max = device_sm_count() >= 2 ? device_sm_count() / 2 : 1;
   const int64_t pairs = max_pair_tiles < pairs_max ? max_pair_tiles : pairs_max;
-  kern<<<static_cast<unsigned>(2 * pairs), THREADS, smem, s>>>(a, b0, b1, args);
+  kern<<<static_cast<unsigned>(2 * pairs), THREADS, smem, s>>>(a, a64, b0, b1, b0h, b1h, args);
   return cudaGetLastError();
 }
 
@@ -413,14 +476,22 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   if (rows_cap == 0 || (dense && p.dense_rows == 0)) return cudaSuccess;
   const int64_t mt_ub = dense ? (p.dense_rows + PM - 1) / PM : (rows_cap + PM - 1) / PM + p.groups;
 
-  CUtensorMap mA, mG, mU, mH, mD;
+  // Full-tile boxes of 128 rows and half-tile boxes of 64 (a gathered A is loaded four
+  // rows at a time through its one-row map).
+  CUtensorMap mA, mA64, mG, mU, mG64, mU64, mH, mH64, mD;
   const bool gather = p.gather_src != nullptr;
+  const uint64_t w_rows = static_cast<uint64_t>(p.groups) * p.width;
   if (!make_bf16_map(&mA, p.A, p.d, gather ? p.src_rows : rows_cap, gather ? 1 : BM) ||
-      !make_bf16_map(&mG, p.W_gate, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
-      !make_bf16_map(&mU, p.W_up, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
+      (!gather && !make_bf16_map(&mA64, p.A, p.d, rows_cap, HM)) ||
+      !make_bf16_map(&mG, p.W_gate, p.d, w_rows, 128) ||
+      !make_bf16_map(&mU, p.W_up, p.d, w_rows, 128) ||
+      !make_bf16_map(&mG64, p.W_gate, p.d, w_rows, HM) ||
+      !make_bf16_map(&mU64, p.W_up, p.d, w_rows, HM) ||
       !make_bf16_map(&mH, p.h, p.width, rows_cap, BM) ||
+      !make_bf16_map(&mH64, p.h, p.width, rows_cap, HM) ||
       !make_bf16_map(&mD, p.W_down, p.width, static_cast<uint64_t>(p.groups) * p.d, 128))
     return cudaErrorInvalidValue;
+  if (gather) mA64 = mA;
 
   PairArgs a{};
   a.offsets = p.offsets;
@@ -438,8 +509,8 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.out = p.h;
   a.ldo = p.width;
   const int64_t gu_tiles = mt_ub * ((p.width + 127) / 128);
-  cudaError_t e = gather ? launch_pair<kSwiGLU, true>(mA, mG, mU, a, gu_tiles, s)
-                         : launch_pair<kSwiGLU, false>(mA, mG, mU, a, gu_tiles, s);
+  cudaError_t e = gather ? launch_pair<kSwiGLU, true>(mA, mA64, mG, mU, mG64, mU64, a, gu_tiles, s)
+                         : launch_pair<kSwiGLU, false>(mA, mA64, mG, mU, mG64, mU64, a, gu_tiles, s);
   if (e != cudaSuccess) return e;
 
   a.k_dim = p.width;
@@ -448,7 +519,7 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.out = p.out;
   a.ldo = p.d;
   a.gather_src = nullptr;    // h is packed
-  return launch_pair<kPlain, false>(mH, mD, mD, a, mt_ub * ((p.d + 255) / 256), s);
+  return launch_pair<kPlain, false>(mH, mH64, mD, mD, mD, mD, a, mt_ub * ((p.d + 255) / 256), s);
 }
 
 }  // namespace moe
