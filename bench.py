@@ -331,6 +331,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--sweep", choices=["entropy"], default=None,
                     help="instead of the benchmark line: grouped-GEMM throughput vs entropy deficit")
+    ap.add_argument("--override", default="", metavar="K=V,...",
+                    help="change integer fields of the workload (e.g. N=32,T=1024: a smaller layer "
+                         "of the same shape per expert, for profiler captures)")
     ap.add_argument("--forward-only", type=int, default=0, metavar="R",
                     help="run R untimed layer forwards and exit (a short, fixed launch sequence "
                          "for ncu captures: each forward launches the routed gate/up and down "
@@ -343,6 +346,8 @@ def main():
 
     from workloads import CONFIGS, make_inputs
     spec = CONFIGS[args.config]
+    if args.override:
+        spec = spec.replace(**{k: int(v) for k, v in (kv.split("=") for kv in args.override.split(","))})
     if args.sweep == "entropy":
         return sweep_entropy(args, spec)
     cores = len(os.sched_getaffinity(0))
@@ -417,9 +422,10 @@ def main():
     torch.cuda.synchronize()
     # Timed region: the fused layer call a user makes (moe_layer_forward), with four events
     # recorded inside it by the library after router, permutation, routed experts and
-    # shared expert + combine.  The steps are queued back to back (no host sync between
+    # combine (the shared expert runs on the library's second stream beside the first
+    # three; the last interval holds the wait for it and the combine).  The steps are queued back to back (no host sync between
     # them); the L2 flush sits between a step's last event and the next step's first.
-    stage_names = ("route", "permute", "grouped_swiglu", "shared_combine")
+    stage_names = ("route", "permute", "grouped_swiglu", "join_combine")
     stage_ms = {k: 0.0 for k in stage_names}
     events = []
     w0 = time.time()

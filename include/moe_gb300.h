@@ -232,16 +232,24 @@ moe_status moe_combine(const moe_config* cfg, const void* f, const int32_t* rout
                        const float* topk_w, const void* g, const float* shared_coef, float* y,
                        cudaStream_t stream);
 
-/* The whole layer: moe_route, moe_permute, moe_grouped_swiglu, moe_shared_mlp, moe_combine in
- * that order on one stream, with intermediates in the workspace.  No host synchronisation. */
+/* The whole layer: moe_route, moe_permute, moe_grouped_swiglu, moe_shared_mlp, moe_combine,
+ * with intermediates in the workspace.  No host synchronisation.  The shared expert, which
+ * needs only x, runs on a second stream beside the router, the permutation and the routed
+ * experts: the call records an event on `stream`, makes the second stream wait for it,
+ * enqueues the shared expert there and makes `stream` wait for it before the combine, so to
+ * the caller the call is ordered on `stream` as if it ran there alone (graph capture of
+ * `stream` takes in both).  The second stream and its two events belong to the calling host
+ * thread and the current device; they are created on the first call and kept for the
+ * thread's lifetime.  Failure to create them returns MOE_ERR_CUDA. */
 moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x,
                              const moe_outputs* out, void* workspace, size_t workspace_bytes,
                              cudaStream_t stream);
 
 /* moe_layer_forward that also records five caller-created CUDA events on the stream: before
- * the router, and after the router, the permutation, the routed experts, and the shared
- * expert + combine (per-stage timing of the exact call a user makes).  events: HOST array
- * of 5 events. */
+ * the router, and after the router, the permutation, the routed experts, and the combine
+ * (per-stage timing of the exact call a user makes; the shared expert runs concurrently
+ * with the first three stages, and the last interval holds any wait for it).  events:
+ * HOST array of 5 events. */
 moe_status moe_layer_forward_profiled(const moe_config* cfg, const moe_weights* w, const void* x,
                                       const moe_outputs* out, void* workspace,
                                       size_t workspace_bytes, cudaStream_t stream,

@@ -5,6 +5,8 @@
 #include <cmath>
 #include <cstring>
 #include <type_traits>
+#include <utility>
+#include <vector>
 
 #include "internal.h"
 
@@ -371,6 +373,48 @@ namespace {
 // The layer forward; when `ev` is non-null, events [0..4] are recorded on the stream before
 // the router and after the router, the permutation, the routed experts, and the shared
 // expert + combine.
+// A second stream of the calling host thread on the current device, with a fork and a
+// join event, created on first use and kept for the thread's lifetime.  The shared
+// expert runs on it, concurrently with the router, the permutation and the routed
+// experts; it needs none of their results.
+struct AuxStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+struct AuxStreams {
+  std::vector<std::pair<int, AuxStream>> per_device;
+  ~AuxStreams() {
+    for (auto& e : per_device) {   // errors at process teardown are of no consequence
+      cudaEventDestroy(e.second.fork);
+      cudaEventDestroy(e.second.join);
+      cudaStreamDestroy(e.second.stream);
+    }
+  }
+};
+
+bool aux_stream(AuxStream* out) {
+  thread_local AuxStreams cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  for (auto& e : cache.per_device)
+    if (e.first == dev) {
+      *out = e.second;
+      return true;
+    }
+  AuxStream a;
+  if (cudaStreamCreateWithFlags(&a.stream, cudaStreamNonBlocking) != cudaSuccess) return false;
+  if (cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) {
+    if (a.fork) cudaEventDestroy(a.fork);
+    cudaStreamDestroy(a.stream);
+    return false;
+  }
+  cache.per_device.emplace_back(dev, a);
+  *out = a;
+  return true;
+}
+
 moe_status layer_forward(const moe_config* cfg, const moe_weights* w, const void* x,
                          const moe_outputs* out, void* workspace, size_t workspace_bytes,
                          cudaStream_t stream, cudaEvent_t* ev) {
@@ -393,9 +437,27 @@ moe_status layer_forward(const moe_config* cfg, const moe_weights* w, const void
   float* sc = pick(out->shared_coef, L.shared_coef);
   int32_t* status = at<int32_t>(ws, L.status);
   if ((s = mark(0)) != MOE_OK) return s;
+  // Fork: the shared expert (Eq. 74-76 on x) is enqueued on the auxiliary stream right
+  // after the router, so the GPU runs it beside the router, the permutation and the
+  // routed experts; the combine waits for it.
+  AuxStream aux;
+  const bool shared = c.d_shared > 0;
+  if (shared) {
+    if (!aux_stream(&aux)) return MOE_ERR_CUDA;
+    if (cudaEventRecord(aux.fork, stream) != cudaSuccess ||
+        cudaStreamWaitEvent(aux.stream, aux.fork, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   if ((s = do_route(c, x, w->W_router, w->router_bias, w->selection_bias, w->shared_gate_w, idx,
                     tw, sc, out->logits, status, stream)) != MOE_OK)
     return s;
+  void* g = nullptr;
+  if (shared) {
+    g = at<void>(ws, L.g);
+    if ((s = do_shared(c, L, ws, x, w->Ws_gate, w->Ws_up, w->Ws_down, g, aux.stream)) != MOE_OK)
+      return s;
+    if (cudaEventRecord(aux.join, aux.stream) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   if ((s = mark(1)) != MOE_OK) return s;
   PermOut po{pick(out->counts_req, L.counts_req), pick(out->counts_keep, L.counts_keep),
              pick(out->offsets, L.offsets),       pick(out->route_pos, L.route_pos),
@@ -411,12 +473,7 @@ moe_status layer_forward(const moe_config* cfg, const moe_weights* w, const void
                       true, stream)) != MOE_OK)
     return s;
   if ((s = mark(3)) != MOE_OK) return s;
-  void* g = nullptr;
-  if (c.d_shared > 0) {
-    g = at<void>(ws, L.g);
-    if ((s = do_shared(c, L, ws, x, w->Ws_gate, w->Ws_up, w->Ws_down, g, stream)) != MOE_OK)
-      return s;
-  }
+  if (shared && cudaStreamWaitEvent(stream, aux.join, 0) != cudaSuccess) return MOE_ERR_CUDA;
   if ((s = do_combine(c, f, po.route_pos, tw, g, g ? sc : nullptr, out->y, status, stream)) != MOE_OK)
     return s;
   return mark(4);
