@@ -1,4 +1,4 @@
-"""Oracle of the routed + shared-expert MoE layer forward (test infrastructure).
+"""Oracle of the routed + shared-expert MoE layer, forward and backward (test infrastructure).
 
 A plain, slow, float64 CPU statement of the layer, written from the pages that
 define the method.  Only the test suite, ``__graft_entry__.smoke()`` and the
@@ -7,3 +7,5 @@ CUDA library, and the library never calls it.
 """
 from .moe_oracle import *  # noqa: F401,F403
 from . import moe_oracle  # noqa: F401
+from . import moe_backward_oracle  # noqa: F401
+from .moe_backward_oracle import dsilu, moe_backward, selected_weights_backward, swiglu_backward  # noqa: F401

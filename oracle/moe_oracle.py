@@ -414,13 +414,14 @@ def moe_forward(cfg, inputs: dict, logits=None):
     """The full layer forward for a whole batch: returns (y [T, d], Routing, s [T]).
 
     ``inputs`` holds the tensors of the workload layout (x, W_router,
-    router_bias, shared_gate_w, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down).
+    router_bias, shared_gate_w, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
+    and optionally the Eq. 35 selection_bias).
     ``logits``, when given, replaces the router projection (used to run the
     selection on exactly the keys another implementation computed).
     """
     x = inputs["x"]
     z = router_logits(x, inputs["W_router"], inputs.get("router_bias")) if logits is None else logits
-    routing = route(z, cfg)
+    routing = route(z, cfg, selection_bias=inputs.get("selection_bias"))
     s = shared_coefficient(x, cfg.shared_mode, cfg.shared_gain, inputs.get("shared_gate_w"))
     Wg, Wu, Wd = inputs["W_gate"], inputs["W_up"], inputs["W_down"]
     shared = None
