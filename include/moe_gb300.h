@@ -296,6 +296,39 @@ moe_status moe_balance_stats(const moe_config* cfg, const float* logits, const i
 moe_status moe_bias_update(int32_t N, const int32_t* counts, float gamma, float* bias,
                            cudaStream_t stream);
 
+/* ---- Backward pass (router coefficients held fixed) ------------------------------------
+ * The expert-path backward of Eq. 74 / Eq. 80 (Section 21, the backward study of Figure
+ * 70: input gradient with the router coefficients fixed, routed and shared weight
+ * gradients).  Per kept route (t, k) of expert e, gf = topk_w[t][k] dy_t and
+ *   dx_t += (W_g^e)^T da + (W_u^e)^T db,  dW_d^e += gf h^T,  dW_g^e += da x_t^T,  dW_u^e += db x_t^T
+ * with a = W_g^e x_t, b = W_u^e x_t (recomputed), h = SiLU(a) b, dh = (W_d^e)^T gf,
+ * da = dh b SiLU'(a), db = dh SiLU(a); the shared expert likewise with gf = s_t dy_t.
+ * Dropped routes carry no gradient.  bf16 layers only, with d_model, d_expert and
+ * d_shared multiples of 128 (others: MOE_ERR_UNSUPPORTED); operands are bf16 (gf, da, db
+ * and h rounded once), accumulation fp32. */
+typedef struct moe_grads {
+  float* dx;        /* [T][d] fp32 */
+  float* dW_gate;   /* [N][d_r][d] fp32 (overwritten) */
+  float* dW_up;     /* [N][d_r][d] fp32 */
+  float* dW_down;   /* [N][d][d_r] fp32 */
+  float* dWs_gate;  /* [d_s][d] fp32; required when d_shared > 0 */
+  float* dWs_up;    /* [d_s][d] fp32 */
+  float* dWs_down;  /* [d][d_s] fp32 */
+} moe_grads;
+
+/* Bytes of scratch moe_layer_backward needs (256-byte aligned; prepare it with
+ * moe_workspace_init before its first use). */
+moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* The backward pass for upstream gradient dy [T][d] fp32 (device).  x and the weights are
+ * those of the forward call; fwd holds that call's routing results (device): topk_idx,
+ * topk_w, counts_keep, offsets, route_pos, perm_src, and shared_coef when d_shared > 0.
+ * Writes every array of grads (device, caller-owned).  Asynchronous on the stream; no
+ * host synchronisation. */
+moe_status moe_layer_backward(const moe_config* cfg, const moe_weights* w, const void* x,
+                              const moe_outputs* fwd, const float* dy, const moe_grads* grads,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Prepare a fresh workspace: zero its device status word (the first 256 bytes).  Call once
  * after allocating a workspace, before its first use.  Asynchronous on the stream. */
 moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream);

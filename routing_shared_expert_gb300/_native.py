@@ -46,6 +46,13 @@ class moe_weights(ctypes.Structure):
                                         "W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down")]
 
 
+GRAD_FIELDS = ("dx", "dW_gate", "dW_up", "dW_down", "dWs_gate", "dWs_up", "dWs_down")
+
+
+class moe_grads(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in GRAD_FIELDS]
+
+
 OUTPUT_FIELDS = ("y", "topk_idx", "topk_w", "shared_coef", "logits", "counts_req", "counts_keep",
                  "offsets", "route_pos", "perm_src", "R_req", "R_keep", "drop_stats")
 
@@ -80,6 +87,9 @@ def _load():
         "moe_merge_shared": ([c_int32, c_int32, c_int32, POINTER(c_int32), POINTER(c_void_p),
                               POINTER(c_void_p), POINTER(c_void_p), P, P, P, P], c_int32),
         "moe_read_status": ([P, POINTER(c_int32), P], c_int32),
+        "moe_backward_workspace_size": ([C, POINTER(c_size_t)], c_int32),
+        "moe_layer_backward": ([C, POINTER(moe_weights), P, POINTER(moe_outputs), P, POINTER(moe_grads),
+                                P, c_size_t, P], c_int32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -296,3 +306,26 @@ def moe_read_status(workspace, stream=None) -> int:
     code = c_int32(0)
     _check("moe_read_status", _lib.moe_read_status(_ptr(workspace), ctypes.byref(code), _stream(stream)))
     return int(code.value)
+
+
+def moe_backward_workspace_size(cfg: moe_config) -> int:
+    n = c_size_t(0)
+    _check("moe_backward_workspace_size", _lib.moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return int(n.value)
+
+
+def make_grads(**tensors) -> moe_grads:
+    g = moe_grads()
+    for name in GRAD_FIELDS:
+        p = _ptr(tensors.get(name))
+        setattr(g, name, p.value if p is not None else None)
+    g._keepalive = list(tensors.values())
+    return g
+
+
+def moe_layer_backward(cfg, weights: moe_weights, x, fwd_outputs: moe_outputs, dy, grads: moe_grads,
+                       workspace, stream=None):
+    _check("moe_layer_backward", _lib.moe_layer_backward(
+        ctypes.byref(cfg), ctypes.byref(weights), _ptr(x), ctypes.byref(fwd_outputs), _ptr(dy),
+        ctypes.byref(grads), _ptr(workspace), workspace.numel(), _stream(stream)))
+

@@ -479,6 +479,214 @@ moe_status layer_forward(const moe_config* cfg, const moe_weights* w, const void
   return mark(4);
 }
 
+
+// ---- backward -------------------------------------------------------------------
+struct BwdLayout {
+  size_t status, seg_pad, x_pad, gf, ab, dab, h, dxr, gs, ab_s, dab_s, h_s, dx_s;
+  size_t total;
+  int64_t rows_cap;   // padded routed rows
+  int64_t t_pad;      // T rounded up to 64
+};
+
+BwdLayout make_bwd_layout(const moe_config& c) {
+  BwdLayout L{};
+  const size_t T = static_cast<size_t>(c.T), N = c.N, K = c.K, d = c.d_model, dr = c.d_expert,
+               ds = c.d_shared;
+  L.rows_cap = static_cast<int64_t>(K * T + 64 * N);
+  L.t_pad = (c.T + 63) / 64 * 64;
+  const size_t R = static_cast<size_t>(L.rows_cap), Tp = static_cast<size_t>(L.t_pad);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L.status = take(256);
+  L.seg_pad = take((N + 1) * 4);
+  L.x_pad = take(R * d * 2);
+  L.gf = take(R * d * 2);
+  L.ab = take(R * 2 * dr * 4);
+  L.dab = take(R * 2 * dr * 2);
+  L.h = take(R * dr * 2);
+  L.dxr = take(R * d * 4);
+  L.gs = take(T * d * 2);
+  L.ab_s = take(Tp * 2 * ds * 4);
+  L.dab_s = take(Tp * 2 * ds * 2);
+  L.h_s = take(Tp * ds * 2);
+  L.dx_s = take(Tp * d * 4);
+  L.total = o;
+  return L;
+}
+
+moe_status check_bwd_cfg(const moe_config* c) {
+  moe_status s = check_cfg(c);
+  if (s != MOE_OK) return s;
+  if (c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c->d_model % 128 != 0 || c->d_expert % 128 != 0 || c->d_shared % 128 != 0)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// The five GEMMs of one expert family (routed: groups of padded segments; shared: one
+// dense group of T rows), then nothing else: the caller combines dx.
+moe_status bwd_family(const moe_config& c, bool routed, const int32_t* seg_pad, int64_t rows,
+                      const void* x_rows, const __nv_bfloat16* gf, float* ab, __nv_bfloat16* dab,
+                      __nv_bfloat16* h, float* dxr, const void* Wg, const void* Wu, const void* Wd,
+                      float* dWg, float* dWu, float* dWd, int32_t* status, cudaStream_t st) {
+  const int G = routed ? c.N : 1;
+  const int64_t d = c.d_model, w = routed ? c.d_expert : c.d_shared;
+  // rows of the row-major activation maps: routed rows_cap; shared: x and gf have T rows
+  // (TMA fills the rows up to T rounded to 64 with zeros), the others t_pad
+  const uint64_t in_rows = routed ? static_cast<uint64_t>(rows) : static_cast<uint64_t>(c.T);
+  CUtensorMap mX, mGf, mDab, mWg, mWu, mWd, mWgMn, mWuMn, mGfMn, mHMn, mDabMn, mXMn;
+  if (!make_bf16_map(&mX, x_rows, d, in_rows, 128) || !make_bf16_map(&mGf, gf, d, in_rows, 128) ||
+      !make_bf16_map(&mDab, dab, 2 * w, rows, 128) ||
+      !make_bf16_map(&mWg, Wg, d, static_cast<uint64_t>(G) * w, 128) ||
+      !make_bf16_map(&mWu, Wu, d, static_cast<uint64_t>(G) * w, 128) ||
+      !make_bf16_map(&mWd, Wd, w, static_cast<uint64_t>(G) * d, 64) ||
+      !make_bf16_map(&mWgMn, Wg, d, static_cast<uint64_t>(G) * w, 64) ||
+      !make_bf16_map(&mWuMn, Wu, d, static_cast<uint64_t>(G) * w, 64) ||
+      !make_bf16_map(&mGfMn, gf, d, in_rows, 64) || !make_bf16_map(&mHMn, h, w, rows, 64) ||
+      !make_bf16_map(&mDabMn, dab, 2 * w, rows, 64) || !make_bf16_map(&mXMn, x_rows, d, in_rows, 64))
+    return MOE_ERR_CUDA;
+  BwdGemmArgs a{};
+  a.seg_off = routed ? seg_pad : nullptr;
+  a.dense_rows = static_cast<int32_t>(rows);
+  a.groups = G;
+  a.status = status;
+  const int64_t sms = device_sm_count();
+  const int64_t row_tiles = rows / 128 + G;   // upper bound of 128-row tiles over all segments
+  auto st_ok = [](cudaError_t e) { return e == cudaSuccess; };
+
+  // recompute [a | b] = x [W_g | W_u]^T  (fp32)
+  a.k_dim = static_cast<int32_t>(d);
+  a.n_dim = static_cast<int32_t>(2 * w);
+  a.b_group_rows = static_cast<int32_t>(w);
+  a.b_split_n = static_cast<int32_t>(w);
+  a.out = ab;
+  a.ldo = 2 * w;
+  if (!st_ok(launch_bwd_gemm(kBwdRowsKMajorB, mX, mWg, mWu, a, row_tiles * (2 * w / 128), st)))
+    return MOE_ERR_CUDA;
+  // dh = gf W_d, then da | db and h
+  a.k_dim = static_cast<int32_t>(d);
+  a.n_dim = static_cast<int32_t>(w);
+  a.b_group_rows = static_cast<int32_t>(d);
+  a.b_split_n = 0;
+  a.b_split_k = 0;
+  a.ab = ab;
+  a.dab = dab;
+  a.hout = h;
+  a.width = static_cast<int32_t>(w);
+  if (!st_ok(launch_bwd_gemm(kBwdRowsMnBSwiglu, mGf, mWd, mWd, a, row_tiles * (w / 128), st)))
+    return MOE_ERR_CUDA;
+  // dx rows = da W_g + db W_u
+  a.k_dim = static_cast<int32_t>(2 * w);
+  a.n_dim = static_cast<int32_t>(d);
+  a.b_group_rows = static_cast<int32_t>(w);
+  a.b_split_k = static_cast<int32_t>(w);
+  a.out = dxr;
+  a.ldo = d;
+  if (!st_ok(launch_bwd_gemm(kBwdRowsMnB, mDab, mWgMn, mWuMn, a, row_tiles * (d / 128), st)))
+    return MOE_ERR_CUDA;
+  // dW_d = gf^T h
+  a.b_split_k = 0;
+  a.b_group_rows = -1;
+  a.m_dim = static_cast<int32_t>(d);
+  a.n_dim = static_cast<int32_t>(w);
+  a.out = dWd;
+  a.out2 = nullptr;
+  a.out_split_m = 0;
+  a.group_stride = d * w;
+  a.ldo = w;
+  if (!st_ok(launch_bwd_gemm(kBwdWeightGrad, mGfMn, mHMn, mHMn, a, G * (d / 128) * (w / 128), st)))
+    return MOE_ERR_CUDA;
+  // dW_g | dW_u = (da | db)^T x
+  a.m_dim = static_cast<int32_t>(2 * w);
+  a.n_dim = static_cast<int32_t>(d);
+  a.out = dWg;
+  a.out2 = dWu;
+  a.out_split_m = static_cast<int32_t>(w);
+  a.group_stride = w * d;
+  a.ldo = d;
+  if (!st_ok(launch_bwd_gemm(kBwdWeightGrad, mDabMn, mXMn, mXMn, a, G * (2 * w / 128) * (d / 128), st)))
+    return MOE_ERR_CUDA;
+  (void)sms;
+  return MOE_OK;
+}
+
+moe_status layer_backward(const moe_config* cfg, const moe_weights* w, const void* x,
+                          const moe_outputs* fwd, const float* dy, const moe_grads* g,
+                          void* ws, size_t ws_bytes, cudaStream_t st) {
+  moe_status s = check_bwd_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (!w || !fwd || !g || !ws) return MOE_ERR_INVALID_ARG;
+  const bool shared = c.d_shared > 0;
+  if (!g->dx || !g->dW_gate || !g->dW_up || !g->dW_down) return MOE_ERR_INVALID_ARG;
+  if (shared && (!g->dWs_gate || !g->dWs_up || !g->dWs_down || !fwd->shared_coef))
+    return MOE_ERR_INVALID_ARG;
+  if (!fwd->topk_idx || !fwd->topk_w || !fwd->counts_keep || !fwd->offsets || !fwd->route_pos ||
+      !fwd->perm_src)
+    return MOE_ERR_INVALID_ARG;
+  if (!w->W_gate || !w->W_up || !w->W_down || (shared && (!w->Ws_gate || !w->Ws_up || !w->Ws_down)))
+    return MOE_ERR_INVALID_ARG;
+  if (c.T > 0 && (!x || !dy)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_MISALIGNED;
+  const BwdLayout L = make_bwd_layout(c);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(g->dx)) return MOE_ERR_MISALIGNED;
+  int32_t* status = at<int32_t>(ws, L.status);
+  int32_t* seg_pad = at<int32_t>(ws, L.seg_pad);
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (!ok(launch_pad_offsets(fwd->counts_keep, c.N, seg_pad, st))) return MOE_ERR_CUDA;
+  if (c.T == 0) return MOE_OK;
+  BwdRowsParams rp{};
+  rp.x = x;
+  rp.dy = dy;
+  rp.counts_keep = fwd->counts_keep;
+  rp.offsets = fwd->offsets;
+  rp.perm_src = fwd->perm_src;
+  rp.route_pos = fwd->route_pos;
+  rp.topk_w = fwd->topk_w;
+  rp.seg_pad = seg_pad;
+  rp.x_pad = at<__nv_bfloat16>(ws, L.x_pad);
+  rp.gf = at<__nv_bfloat16>(ws, L.gf);
+  rp.T = c.T;
+  rp.d = c.d_model;
+  rp.N = c.N;
+  rp.K = c.K;
+  rp.status = status;
+  if (!ok(launch_bwd_rows(rp, L.rows_cap, st))) return MOE_ERR_CUDA;
+  s = bwd_family(c, true, seg_pad, L.rows_cap, rp.x_pad, rp.gf, at<float>(ws, L.ab),
+                 at<__nv_bfloat16>(ws, L.dab), at<__nv_bfloat16>(ws, L.h), at<float>(ws, L.dxr),
+                 w->W_gate, w->W_up, w->W_down, g->dW_gate, g->dW_up, g->dW_down, status, st);
+  if (s != MOE_OK) return s;
+  float* dxs = nullptr;
+  if (shared) {
+    __nv_bfloat16* gs = at<__nv_bfloat16>(ws, L.gs);
+    if (!ok(launch_shared_scale(dy, fwd->shared_coef, c.T, c.d_model, gs, st))) return MOE_ERR_CUDA;
+    dxs = at<float>(ws, L.dx_s);
+    s = bwd_family(c, false, nullptr, L.t_pad, x, gs, at<float>(ws, L.ab_s),
+                   at<__nv_bfloat16>(ws, L.dab_s), at<__nv_bfloat16>(ws, L.h_s), dxs, w->Ws_gate,
+                   w->Ws_up, w->Ws_down, g->dWs_gate, g->dWs_up, g->dWs_down, status, st);
+    if (s != MOE_OK) return s;
+  }
+  BwdCombineParams cp{};
+  cp.dxr = at<float>(ws, L.dxr);
+  cp.dxs = dxs;
+  cp.route_pos = fwd->route_pos;
+  cp.topk_idx = fwd->topk_idx;
+  cp.offsets = fwd->offsets;
+  cp.seg_pad = seg_pad;
+  cp.dx = g->dx;
+  cp.T = c.T;
+  cp.d = c.d_model;
+  cp.N = c.N;
+  cp.K = c.K;
+  cp.status = status;
+  return ok(launch_dx_combine(cp, st)) ? MOE_OK : MOE_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -553,6 +761,20 @@ moe_status moe_bias_update(int32_t N, const int32_t* counts, float gamma, float*
   if (N < 1 || N > kMaxExperts || !counts || !bias || !std::isfinite(gamma))
     return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_bias_update(N, counts, gamma, bias, stream));
+}
+
+moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  moe_status s = check_bwd_cfg(cfg);
+  if (s != MOE_OK) return s;
+  *bytes = make_bwd_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status moe_layer_backward(const moe_config* cfg, const moe_weights* w, const void* x,
+                              const moe_outputs* fwd, const float* dy, const moe_grads* grads,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return layer_backward(cfg, w, x, fwd, dy, grads, workspace, workspace_bytes, stream);
 }
 
 moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream) {

@@ -1,0 +1,435 @@
+// Grouped GEMMs of the layer's backward pass on the tensor cores (tcgen05 + TMEM, fed by TMA).
+//
+// The backward pass of Eq. 74 / Eq. 80 ("Section 21: Merging Routed and Shared Expert
+// Activations", the backward study of Figure 70; "Section 20: One Shared Expert Is All
+// You Need", Eq. 74) needs, per expert segment of packed rows, products whose operands
+// sit in row-major buffers in either orientation:
+//   recompute   [a | b] = x W_g^T | x W_u^T          A = rows (K-major), B = weights (K-major)
+//   dgrad down  dh      = gf W_d                      A = rows (K-major), B = W_d (MN-major)
+//   dgrad g/u   dx      = da W_g + db W_u             A = rows (K-major), B = W_g ; W_u (MN-major)
+//   wgrad down  dW_d    = gf^T h                      A, B = rows read across (MN-major), K = segment
+//   wgrad g/u   dW_g|u  = (da|db)^T x                 A, B = rows read across (MN-major), K = segment
+// One kernel template covers them: C = A B^T with A and B each K-major (K contiguous) or
+// MN-major (M or N contiguous), both loaded by TMA with 128-byte swizzle.  An MN-major
+// operand tile is two 64-column boxes of 64 K-rows (8 KB apart: the descriptor's leading
+// byte offset), K-rows 1024 bytes per 8 (its stride byte offset), and a K step of 16
+// advances the start address by 2048 bytes; the instruction descriptor's bits 15 / 16 mark
+// A / B as MN-major.
+//
+// Segments are padded to multiples of 64 rows with zero rows (the caller's layout), so a
+// GEMM whose K runs over a segment's rows needs no masking.  Two epilogues: fp32 rows
+// (dx, dW), and the SwiGLU backward for the down dgrad, which reads the recomputed a, b
+// and writes da, db (bf16, the next GEMMs' operands) and h = SiLU(a) b (bf16):
+//   da = dh * b * SiLU'(a),  db = dh * SiLU(a),  SiLU'(a) = sigma(a) (1 + a (1 - sigma(a))).
+//
+// Kernel design (one CTA per SM, persistent, 192 threads): warp 0 TMA producer, warp 1
+// TMEM allocation and MMA issue (M = 128, N = 128, K = 16 per instruction), warps 2-5
+// epilogue; 128 x 128 tiles, 6-stage ring of 32 KB, accumulators double buffered in TMEM.
+// Every wait is bounded; a wait that runs out records MOE_ERR_TIMEOUT and the CTA drains
+// what it issued before freeing its TMEM.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 64;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+constexpr uint32_t kMnLbo = 8192;   // bytes between the two 64-wide MN halves of a tile
+constexpr uint32_t kMnSbo = 1024;   // bytes between groups of 8 K-rows
+
+// SMEM descriptor of an MN-major, 128-byte-swizzled operand tile.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((kMnLbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((kMnSbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
+struct BwdTile {
+  int g, m, n;
+  int seg_start, seg_end;   // padded segment rows of group g
+};
+
+__device__ __forceinline__ bool bwd_tile(const BwdGemmArgs& a, bool k_seg, const int* s_off,
+                                         const int* s_tp, int n_tiles, int64_t t, BwdTile& o) {
+  const int G = a.seg_off ? a.groups : 1;
+  if (k_seg) {
+    // fixed tiles per group: m_dim / BM x n_tiles
+    const int mt = a.m_dim / BM;
+    const int64_t per = static_cast<int64_t>(mt) * n_tiles;
+    if (t >= per * G) return false;
+    o.g = static_cast<int>(t / per);
+    const int64_t local = t - static_cast<int64_t>(o.g) * per;
+    o.n = static_cast<int>(local / mt);
+    o.m = static_cast<int>(local % mt);
+  } else {
+    if (t >= static_cast<int64_t>(s_tp[G]) * n_tiles) return false;
+    int lo = 0, hi = G;   // s_tp[lo] * n_tiles <= t < s_tp[hi] * n_tiles
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (static_cast<int64_t>(s_tp[mid]) * n_tiles <= t) lo = mid; else hi = mid;
+    }
+    const int mt = s_tp[lo + 1] - s_tp[lo];
+    const int64_t local = t - static_cast<int64_t>(s_tp[lo]) * n_tiles;
+    o.g = lo;
+    o.n = static_cast<int>(local / mt);
+    o.m = static_cast<int>(local % mt);
+  }
+  o.seg_start = s_off[o.g];
+  o.seg_end = s_off[o.g + 1];
+  return true;
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_bwd_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                const __grid_constant__ CUtensorMap tmB1, const BwdGemmArgs args) {
+  // A_MN: K runs over the segment rows (weight gradients); otherwise the rows are M.
+  constexpr bool K_SEG = A_MN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* never = const_cast<int*>(abort_flag) + 1;
+  const int G = args.seg_off ? args.groups : 1;
+  int* s_off = never + 1;       // [G+1]
+  int* s_tp = s_off + (G + 1);  // [G+1] m-tile prefix (row-segment mode)
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n_tiles = args.n_dim / BN;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 4);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    *never = 0;
+    mbar_fence_init();
+  }
+  if (warp == 3) {
+    if (args.seg_off == nullptr) {
+      if (lane == 0) {
+        s_off[0] = 0;
+        s_off[1] = args.dense_rows;
+        s_tp[0] = 0;
+        s_tp[1] = (args.dense_rows + BM - 1) / BM;
+      }
+    } else {
+      for (int i = lane; i <= G; i += 32) s_off[i] = args.seg_off[i];
+      __syncwarp();
+      int running = 0;
+      for (int base = 0; base < G; base += 32) {
+        const int g = base + lane;
+        int v = 0;
+        if (g < G) {
+          const int len = s_off[g + 1] - s_off[g];
+          if (len < 0 || (len & (BK - 1)) != 0) set_status(args.status, MOE_ERR_DEVICE_BOUNDS);
+          v = len > 0 ? (len + BM - 1) / BM : 0;
+        }
+        int incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        if (g < G) s_tp[g + 1] = running + incl;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) s_tp[0] = 0;
+    }
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB0);
+    tma_prefetch_map(&tmB1);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  auto k_blocks_of = [&](const BwdTile& tl) {
+    return K_SEG ? (tl.seg_end - tl.seg_start) / BK : args.k_dim / BK;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued_parity[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+      bool ok = true;
+      BwdTile tl;
+      for (int64_t t = blockIdx.x; ok && bwd_tile(args, K_SEG, s_off, s_tp, n_tiles, t, tl);
+           t += gridDim.x) {
+        const int kbs = k_blocks_of(tl);
+        const int m0 = tl.m * BM, n0 = tl.n * BN;
+        for (int kb = 0; kb < kbs; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
+                                 kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t sA = smem_base + stage * STAGE_BYTES;
+          const uint32_t sB = sA + A_BYTES;
+          const int k0 = kb * BK;
+          if (A_MN) {
+            const int row = tl.seg_start + k0;
+            tma_load_2d(sA, &tmA, m0, row, fb);
+            tma_load_2d(sA + kMnLbo, &tmA, m0 + 64, row, fb);
+          } else {
+            tma_load_2d(sA, &tmA, k0, tl.seg_start + m0, fb);
+          }
+          if (B_MN) {
+            // B[n][k] = view[row(k)][n]: weights (group rows) or segment rows
+            const CUtensorMap* mb = &tmB0;
+            int row;
+            if (args.b_group_rows < 0) {
+              row = tl.seg_start + k0;
+            } else if (args.b_split_k > 0 && k0 >= args.b_split_k) {
+              mb = &tmB1;
+              row = tl.g * args.b_group_rows + (k0 - args.b_split_k);
+            } else {
+              row = tl.g * args.b_group_rows + k0;
+            }
+            tma_load_2d(sB, mb, n0, row, fb);
+            tma_load_2d(sB + kMnLbo, mb, n0 + 64, row, fb);
+          } else {
+            // B[n][k] = view[g * b_group_rows + n][k], the second map past b_split_n
+            const CUtensorMap* mb = &tmB0;
+            int nn = n0;
+            if (args.b_split_n > 0 && n0 >= args.b_split_n) {
+              mb = &tmB1;
+              nn = n0 - args.b_split_n;
+            }
+            tma_load_2d(sB, mb, k0, tl.g * args.b_group_rows + nn, fb);
+          }
+          issued_parity[stage] = static_cast<int>(phase);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok)
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_parity[s] >= 0)
+            mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>(issued_parity[s]), never,
+                              nullptr, kDrainLimitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN) | (A_MN ? (1u << 15) : 0u) |
+                                 (B_MN ? (1u << 16) : 0u);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      BwdTile tl;
+      int64_t local = 0;
+      for (int64_t t = blockIdx.x; ok && bwd_tile(args, K_SEG, s_off, s_tp, n_tiles, t, tl);
+           t += gridDim.x, ++local) {
+        const int buf = static_cast<int>(local & 1);
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        if (!mbar_wait_bounded(smem_u32(&tempty[buf]), (use & 1u) ^ 1u, abort_flag, args.status,
+                               kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_acc = tmem_base + static_cast<uint32_t>(buf * BN);
+        const int kbs = k_blocks_of(tl);
+        for (int kb = 0; kb < kbs; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, args.status,
+                                 kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_base + stage * STAGE_BYTES;
+          const uint32_t sB = sA + A_BYTES;
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j) {
+            const uint64_t ad = A_MN ? sw128_mnmajor_desc(sA + j * 2048) : sw128_kmajor_desc(sA) + 2 * j;
+            const uint64_t bd = B_MN ? sw128_mnmajor_desc(sB + j * 2048) : sw128_kmajor_desc(sB) + 2 * j;
+            tc_mma_bf16(d_acc, ad, bd, idesc, (kb > 0 || j > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&empty[stage]));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&tfull[buf]));   // with no K blocks this arrives at once
+      }
+      if (!ok) {
+        tc_commit(smem_u32(drain));
+        mbar_wait_bounded(smem_u32(drain), 0, never, nullptr, kDrainLimitNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    BwdTile tl;
+    int64_t local = 0;
+    for (int64_t t = blockIdx.x; bwd_tile(args, K_SEG, s_off, s_tp, n_tiles, t, tl);
+         t += gridDim.x, ++local) {
+      const int buf = static_cast<int>(local & 1);
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      bool ready = true;
+      if (lane == 0)
+        ready = mbar_wait_bounded(smem_u32(&tfull[buf]), use & 1u, abort_flag, args.status,
+                                  kWaitLimitNs);
+      ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+      if (!ready) break;
+      tc_fence_after();
+      const bool empty_k = k_blocks_of(tl) == 0;   // no rows: the product is zero
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(buf * BN);
+      const int r = tl.m * BM + q * 32 + lane;     // tile row of this thread
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        if (empty_k) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        } else {
+          tmem_ld32(taddr + c * 32, v);
+        }
+        const int col = tl.n * BN + c * 32;
+        if (EPI == kBwdEpiF32) {
+          float* base;
+          int64_t row;
+          if (K_SEG) {
+            // C block of group g: rows m (split into out / out2 at out_split_m)
+            row = r;
+            base = args.out + static_cast<int64_t>(tl.g) * args.group_stride;
+            if (args.out_split_m > 0 && r >= args.out_split_m) {
+              base = args.out2 + static_cast<int64_t>(tl.g) * args.group_stride;
+              row = r - args.out_split_m;
+            }
+          } else {
+            row = tl.seg_start + r;
+            base = args.out;
+            if (row >= tl.seg_end) continue;
+          }
+          float* dst = base + row * args.ldo + col;
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            *reinterpret_cast<float4*>(dst + 4 * v4) =
+                make_float4(__uint_as_float(v[4 * v4]), __uint_as_float(v[4 * v4 + 1]),
+                            __uint_as_float(v[4 * v4 + 2]), __uint_as_float(v[4 * v4 + 3]));
+        } else {
+          // SwiGLU backward: dh in v; a, b from ab; da | db and h out (bf16)
+          const int64_t row = tl.seg_start + r;
+          if (row >= tl.seg_end) continue;
+          const float* arow = args.ab + row * (2 * static_cast<int64_t>(args.width));
+          __nv_bfloat16* drow = args.dab + row * (2 * static_cast<int64_t>(args.width));
+          __nv_bfloat16* hrow = args.hout + row * static_cast<int64_t>(args.width);
+#pragma unroll
+          for (int v8 = 0; v8 < 4; ++v8) {
+            uint32_t da2[4], db2[4], h2[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float dav[2], dbv[2], hv[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int j = col + 8 * v8 + 2 * i + e;
+                const float a = arow[j];
+                const float b = arow[args.width + j];
+                const float dh = __uint_as_float(v[8 * v8 + 2 * i + e]);
+                const float sg = 1.0f / (1.0f + __expf(-a));
+                const float sl = a * sg;
+                dav[e] = dh * b * (sg * (1.0f + a * (1.0f - sg)));
+                dbv[e] = dh * sl;
+                hv[e] = sl * b;
+              }
+              da2[i] = pack_bf16x2(dav[0], dav[1]);
+              db2[i] = pack_bf16x2(dbv[0], dbv[1]);
+              h2[i] = pack_bf16x2(hv[0], hv[1]);
+            }
+            const int j0 = col + 8 * v8;
+            *reinterpret_cast<uint4*>(drow + j0) = make_uint4(da2[0], da2[1], da2[2], da2[3]);
+            *reinterpret_cast<uint4*>(drow + args.width + j0) = make_uint4(db2[0], db2[1], db2[2], db2[3]);
+            *reinterpret_cast<uint4*>(hrow + j0) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+size_t bwd_smem_bytes(int groups) {
+  return 1024 + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5) + 16 + 8 * (static_cast<size_t>(groups) + 1) +
+         64;
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_one_bwd(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                           const BwdGemmArgs& args, int64_t max_tiles, cudaStream_t s) {
+  if (max_tiles <= 0) return cudaSuccess;
+  const size_t smem = bwd_smem_bytes(args.seg_off ? args.groups : 1);
+  auto kern = tc_bwd_gemm<A_MN, B_MN, EPI>;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  const int sms = device_sm_count();
+  const int64_t grid = max_tiles < sms ? max_tiles : sms;
+  kern<<<static_cast<unsigned>(grid), THREADS, smem, s>>>(a, b0, b1, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_gemm(int kind, const CUtensorMap& a, const CUtensorMap& b0,
+                            const CUtensorMap& b1, const BwdGemmArgs& args, int64_t max_tiles,
+                            cudaStream_t s) {
+  switch (kind) {
+    case kBwdRowsKMajorB:   // recompute: A rows, B weights K-major, fp32 out
+      return launch_one_bwd<false, false, kBwdEpiF32>(a, b0, b1, args, max_tiles, s);
+    case kBwdRowsMnB:       // dgrad gate/up: A rows, B weights MN-major, fp32 out
+      return launch_one_bwd<false, true, kBwdEpiF32>(a, b0, b1, args, max_tiles, s);
+    case kBwdRowsMnBSwiglu: // dgrad down + SwiGLU backward
+      return launch_one_bwd<false, true, kBwdEpiSwiglu>(a, b0, b1, args, max_tiles, s);
+    case kBwdWeightGrad:    // wgrad: A, B MN-major over segment rows, fp32 blocks
+      return launch_one_bwd<true, true, kBwdEpiF32>(a, b0, b1, args, max_tiles, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -132,6 +133,82 @@ struct MlpParams {
 };
 cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s);        // 1-SM, 128-row tiles
 cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s);   // CTA pairs, 256-row tiles
+
+// ---- backward pass ------------------------------------------------------------
+// Epilogues and kinds of the backward GEMM kernel (gemm_bwd.cu).
+constexpr int kBwdEpiF32 = 0;      // fp32 C rows / blocks
+constexpr int kBwdEpiSwiglu = 1;   // SwiGLU backward of dh: da | db and h (bf16)
+constexpr int kBwdRowsKMajorB = 0;
+constexpr int kBwdRowsMnB = 1;
+constexpr int kBwdRowsMnBSwiglu = 2;
+constexpr int kBwdWeightGrad = 3;
+
+struct BwdGemmArgs {
+  // C_g = A_g B_g^T per group g of segment rows [seg_off[g], seg_off[g+1]) (multiples of
+  // 64; nullptr = one group of dense_rows).  Row mode (A K-major): M = the segment rows,
+  // K = k_dim.  Weight-gradient mode (A MN-major): K = the segment rows, M = m_dim.
+  const int32_t* seg_off;
+  int32_t dense_rows;
+  int32_t groups;
+  int32_t m_dim;
+  int32_t n_dim;
+  int32_t k_dim;
+  // B: K-major rows g * b_group_rows + n (second map past b_split_n), or MN-major rows
+  // g * b_group_rows + k (second map past b_split_k); b_group_rows < 0: MN-major rows are
+  // the segment rows.
+  int32_t b_group_rows;
+  int32_t b_split_k;
+  int32_t b_split_n;
+  // fp32 epilogue: rows of C at out (row mode: segment rows; weight mode: group block
+  // g at out + g * group_stride, rows >= out_split_m at out2)
+  float* out;
+  float* out2;
+  int32_t out_split_m;
+  int64_t group_stride;
+  int64_t ldo;
+  // SwiGLU-backward epilogue
+  const float* ab;            // [rows][2 * width] fp32: a | b
+  __nv_bfloat16* dab;         // [rows][2 * width] bf16: da | db
+  __nv_bfloat16* hout;        // [rows][width] bf16: SiLU(a) * b
+  int32_t width;
+  int32_t* status;
+};
+cudaError_t launch_bwd_gemm(int kind, const CUtensorMap& a, const CUtensorMap& b0,
+                            const CUtensorMap& b1, const BwdGemmArgs& args, int64_t max_tiles,
+                            cudaStream_t s);
+
+struct BwdRowsParams {
+  const void* x;              // [T][d] bf16
+  const float* dy;            // [T][d]
+  const int32_t* counts_keep; // [N]
+  const int32_t* offsets;     // [N+1] packed offsets of the forward
+  const int32_t* perm_src;    // [K*T]
+  const int32_t* route_pos;   // [T][K]
+  const float* topk_w;        // [T][K]
+  const int32_t* seg_pad;     // [N+1] padded offsets
+  __nv_bfloat16* x_pad;       // [rows][d]
+  __nv_bfloat16* gf;          // [rows][d]
+  int64_t T;
+  int32_t d, N, K;
+  int32_t* status;
+};
+struct BwdCombineParams {
+  const float* dxr;           // [rows][d] route rows (padded layout)
+  const float* dxs;           // [T][d] shared rows, or nullptr
+  const int32_t* route_pos;   // [T][K]
+  const int32_t* topk_idx;    // [T][K]
+  const int32_t* offsets;     // [N+1]
+  const int32_t* seg_pad;     // [N+1]
+  float* dx;                  // [T][d]
+  int64_t T;
+  int32_t d, N, K;
+  int32_t* status;
+};
+cudaError_t launch_pad_offsets(const int32_t* counts_keep, int N, int32_t* seg_pad, cudaStream_t s);
+cudaError_t launch_bwd_rows(const BwdRowsParams& p, int64_t rows_cap, cudaStream_t s);
+cudaError_t launch_shared_scale(const float* dy, const float* sc, int64_t T, int d, __nv_bfloat16* gs,
+                                cudaStream_t s);
+cudaError_t launch_dx_combine(const BwdCombineParams& p, cudaStream_t s);
 
 // Tile shape choice for the bf16 expert GEMMs: 256-row pair tiles load half the
 // bytes per multiply-add of 128-row single-SM tiles and win once segments average

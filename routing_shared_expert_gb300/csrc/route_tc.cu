@@ -3,11 +3,15 @@
 // Same step as route.cu (Section 10 "Routing, Capacity, and Load Balancing",
 // Table 16 and Eq. 35; Appendix E "Expert-Merge Normalization in Public MoE
 // Models", Table 52; Section 21, Eq. 80 coefficients), organised for sm_103a:
-//   - one CTA per 128 tokens; warp 0 streams x and W_router K-blocks with TMA
-//     (128-byte swizzle) through a shared-memory ring, warp 1 issues
-//     tcgen05.mma (M = 128 tokens, N = N rounded up to 16, fp32 accumulators in
-//     TMEM), plus an N = 16 MMA against the shared-gate vector w_s when the layer
-//     has a learned shared gate (its logit lands in TMEM column N_pad);
+//   - one CTA per R tokens (R = 32, 64 or 128, so that the grid covers the SMs: the
+//     step streams x once and is bound by HBM, not by the tensor cores); warp 0
+//     streams x and W_router K-blocks with TMA (128-byte swizzle) through a
+//     shared-memory ring, warp 1 issues tcgen05.mma (M = 128 rows, of which the
+//     first R are this CTA's tokens and the rest are ignored; N = N rounded up to
+//     16; fp32 accumulators in TMEM), plus an N = 16 MMA against the shared-gate
+//     vector w_s when the layer has a learned shared gate (its logit lands in TMEM
+//     column N_pad).  With few experts a CTA takes a quarter of the SM's shared
+//     memory and TMEM, so several run per SM;
 //   - warps 2-5 read the accumulators with tcgen05.ld, one token row per
 //     thread, so the selection runs in registers: a sorted top-8 list with
 //     strict comparisons (an equal later expert never displaces an earlier one,
@@ -22,13 +26,11 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;
+constexpr int BM = 128;                    // MMA rows (and A slot rows)
 constexpr int BK = 64;
 constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 512;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int G_BYTES = 16 * BK * 2;
-constexpr int SMEM_RING = 200 * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 100000000ull;
 
@@ -38,6 +40,8 @@ struct RouteTcArgs {
   int32_t gated;       // 1 when the shared gate column is computed
   int32_t stages;
   int32_t stage_bytes;
+  int32_t rows;        // tokens per CTA (R)
+  uint32_t tmem_cols;  // power of two >= n_pad (+16 when gated)
 };
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -61,7 +65,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int k_blocks = (p.d + BK - 1) / BK;
   const uint32_t smem_base = smem_u32(smem);
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * BM;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * a.rows;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -83,12 +87,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_map(&tmW);
     if (a.gated) tma_prefetch_map(&tmG);
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), a.tmem_cols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const uint32_t tx_bytes = static_cast<uint32_t>(A_BYTES + a.n_pad * BK * 2 + (a.gated ? G_BYTES : 0));
+  const uint32_t tx_bytes =
+      static_cast<uint32_t>(a.rows * BK * 2 + a.n_pad * BK * 2 + (a.gated ? G_BYTES : 0));
 
   if (warp == 0) {
     if (lane == 0) {
@@ -157,6 +162,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ---------------- epilogue: one token row per thread ----------------
     const int q = warp & 3;
+    if (q * 32 >= a.rows) goto done;   // TMEM lanes of rows this CTA does not own
+    {
     bool ready = true;
     if (lane == 0)
       ready = mbar_wait_bounded(smem_u32(acc_full), 0, abort_flag, p.status, kWaitLimitNs);
@@ -282,13 +289,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (p.shared_coef) p.shared_coef[t] = shared;
       }
     }
+    }
   }
 
+done:
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc(tmem_base, a.tmem_cols);
   }
 }
 
@@ -298,8 +307,16 @@ cudaError_t launch_route_tc(const RouteParams& p, cudaStream_t s) {
   if (p.T == 0) return cudaSuccess;
   const bool gated = p.shared_mode == MOE_SHARED_SIGMOID_GATE;
   const int n_pad = (p.N + 15) / 16 * 16;
+  // Tokens per CTA: the smallest of 32, 64, 128 whose grid fits the SMs at once (two
+  // CTAs per SM with few experts; one with many, where each CTA's MMAs over all N
+  // columns and its reads of W_router cost the same for any R, so R stays >= 64).
+  const int64_t sms = device_sm_count() > 0 ? device_sm_count() : 1;
+  const bool wide = n_pad > 128;
+  int rows = wide ? 64 : 32;
+  while (rows < BM && (p.T + rows - 1) / rows > (wide ? 1 : 2) * sms) rows *= 2;
   CUtensorMap mX, mW, mG;
-  if (!make_bf16_map(&mX, p.x, p.d, p.T, BM) || !make_bf16_map(&mW, p.W_router, p.d, p.N, n_pad))
+  if (!make_bf16_map(&mX, p.x, p.d, p.T, static_cast<uint32_t>(rows)) ||
+      !make_bf16_map(&mW, p.W_router, p.d, p.N, n_pad))
     return cudaErrorInvalidValue;
   if (gated) {
     if (!make_bf16_map(&mG, p.shared_gate_w, p.d, 1, 16)) return cudaErrorInvalidValue;
@@ -310,15 +327,22 @@ cudaError_t launch_route_tc(const RouteParams& p, cudaStream_t s) {
   a.p = p;
   a.n_pad = n_pad;
   a.gated = gated ? 1 : 0;
+  a.rows = rows;
+  uint32_t cols = 32;
+  while (cols < static_cast<uint32_t>(n_pad + (gated ? 16 : 0))) cols *= 2;
+  a.tmem_cols = cols;
   a.stage_bytes = A_BYTES + n_pad * BK * 2 + (gated ? G_BYTES : 0);
-  a.stages = SMEM_RING / a.stage_bytes;
+  // With at most 128 TMEM columns a CTA leaves room for others on its SM: a ring of
+  // about 100 KB lets two run per SM; otherwise the ring takes most of the 227 KB.
+  const int ring = cols <= 128 ? 100 * 1024 : 200 * 1024;
+  a.stages = ring / a.stage_bytes;
   if (a.stages > 8) a.stages = 8;
   if (a.stages < 2) a.stages = 2;
   const size_t smem = 1024 + static_cast<size_t>(a.stages) * a.stage_bytes + 8 * 20 + 16 +
                       2 * sizeof(float) * kMaxExperts + 64;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(route_tc_kernel), smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>((p.T + BM - 1) / BM);
+  const unsigned grid = static_cast<unsigned>((p.T + rows - 1) / rows);
   route_tc_kernel<<<grid, THREADS, smem, s>>>(mX, mW, mG, a);
   return cudaGetLastError();
 }

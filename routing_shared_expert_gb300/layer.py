@@ -112,5 +112,29 @@ class MoELayer:
         rec(5)
         return o["y"]
 
+    def backward(self, x: torch.Tensor, dy: torch.Tensor, stream=None) -> Dict[str, torch.Tensor]:
+        """Gradients (router coefficients fixed) for upstream gradient dy [T][d] fp32, using
+        the routing of the last forward call; returns dx and the weight gradients (fp32)."""
+        c = self.cfg
+        if getattr(self, "bwd_ws", None) is None:
+            n = nat.moe_backward_workspace_size(c)
+            self.bwd_ws = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+            nat.moe_workspace_init(self.bwd_ws, stream)
+            f32 = dict(dtype=torch.float32, device=self.device)
+            T, d, N, dr, ds = c.T, c.d_model, c.N, c.d_expert, c.d_shared
+            self.grads = {"dx": torch.empty((T, d), **f32),
+                          "dW_gate": torch.empty((N, dr, d), **f32),
+                          "dW_up": torch.empty((N, dr, d), **f32),
+                          "dW_down": torch.empty((N, d, dr), **f32)}
+            if ds > 0:
+                self.grads.update(dWs_gate=torch.empty((ds, d), **f32), dWs_up=torch.empty((ds, d), **f32),
+                                  dWs_down=torch.empty((d, ds), **f32))
+            self.grads_c = nat.make_grads(**self.grads)
+        nat.moe_layer_backward(c, self.w, x, self.outputs, dy, self.grads_c, self.bwd_ws, stream)
+        return self.grads
+
+    def backward_status(self) -> int:
+        return nat.moe_read_status(self.bwd_ws)
+
     def status(self) -> int:
         return nat.moe_read_status(self.ws)

@@ -88,6 +88,34 @@ def test_lp_exponent_checked_only_with_the_lp_rule(nat):
     assert nat.moe_workspace_size(_olmo(norm=1, norm_p=float("nan"))) > 0
 
 
+def test_backward_rejects_unsupported_layers(nat):
+    # fp32 layers, and widths that are not multiples of 128
+    with pytest.raises(nat.MoEError):
+        nat.moe_backward_workspace_size(nat.make_config(T=16, d_model=64, N=8, K=2, d_expert=128,
+                                                        d_shared=64, dtype="f32"))
+    for kw in (dict(d_model=192), dict(d_expert=320), dict(d_shared=64)):
+        c = _olmo(**kw)
+        with pytest.raises(nat.MoEError) as e:
+            nat.moe_backward_workspace_size(c)
+        assert e.value.status == -2
+    assert nat.moe_backward_workspace_size(_olmo()) > nat.moe_workspace_size(_olmo())
+
+
+def test_backward_rejects_null_arguments_before_cuda(nat):
+    import ctypes
+    lib = nat.library()
+    c = _olmo(T=64)
+    n = nat.moe_backward_workspace_size(c)
+    assert n > 0
+    w = nat.moe_weights()
+    o = nat.moe_outputs()
+    g = nat.moe_grads()
+    # null weights / outputs / grads: invalid argument, nothing enqueued
+    st = lib.moe_layer_backward(ctypes.byref(c), ctypes.byref(w), None, ctypes.byref(o), None,
+                                ctypes.byref(g), None, 0, None)
+    assert st == -1
+
+
 def test_rho_out_of_range_rejected(nat):
     c = nat.make_config(T=16, d_model=64, N=4, K=1, d_expert=64, d_shared=0, shared_mode="none",
                         cap_policy="rank_wide", num_ranks=2, rho=[0, 1, 2, 0])
