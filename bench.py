@@ -318,6 +318,55 @@ def launches_per_step(spec) -> int:
     return 1 + 4 + 2 + (2 if spec.d_shared > 0 else 0) + 1
 
 
+# ----------------------------------------------------------------- backward
+
+def bench_backward(args, spec, layer, x, config, dev):
+    """Time moe_layer_backward (router coefficients fixed) on the routing of one forward
+    call: CUDA events around each call, a 256 MiB buffer written between calls."""
+    import torch
+    layer.forward(x, logits=False)
+    g = torch.Generator(device="cpu").manual_seed(7)
+    dy = torch.randn((spec.T, spec.d_model), generator=g).to(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        layer.backward(x, dy)
+        flush.add_(1)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    evs = []
+    w0 = time.time()
+    for _ in range(args.steps):
+        flush.add_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        layer.backward(x, dy)
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    w1 = time.time()
+    clk = clocks.stop(w0, w1)
+    assert layer.backward_status() == 0, "device status word set during the backward benchmark"
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    kept = int(layer.out["counts_keep"].sum())
+    d, dr, ds = spec.d_model, spec.d_expert, spec.d_shared
+    # per routed row: dgrad 6 d d_r, weight gradients 6 d d_r, recompute of a | b 4 d d_r
+    std_flops = 12.0 * d * (dr * kept + ds * spec.T)
+    exe_flops = 16.0 * d * (dr * kept + ds * spec.T)
+    pk = peaks()
+    line = {"metric": "MoE-layer backward (router coefficients fixed) tokens/s on 1 GB300",
+            "value": spec.T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": spec.dtype,
+            "data": "synthetic", "config": dict(config, l2="256 MiB buffer written between calls"),
+            "tflops_executed": exe_flops / (ms / 1e3) / 1e12,
+            "tflops_standard": std_flops / (ms / 1e3) / 1e12,
+            "pct_bf16_peak_executed": 100.0 * exe_flops / (ms / 1e3) / 1e12 / pk["bf16_tflops"],
+            "clocks": clk, "kept_routes": kept}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------- main
 
 def main():
@@ -334,6 +383,9 @@ def main():
     ap.add_argument("--override", default="", metavar="K=V,...",
                     help="change integer fields of the workload (e.g. N=32,T=1024: a smaller layer "
                          "of the same shape per expert, for profiler captures)")
+    ap.add_argument("--mode", choices=["forward", "backward"], default="forward",
+                    help="backward: time moe_layer_backward (router coefficients fixed) on the "
+                         "routing of one forward call, instead of the forward benchmark line")
     ap.add_argument("--forward-only", type=int, default=0, metavar="R",
                     help="run R untimed layer forwards and exit (a short, fixed launch sequence "
                          "for ncu captures: each forward launches the routed gate/up and down "
@@ -407,6 +459,8 @@ def main():
                           "kept": int(layer.out["counts_keep"].sum())}), flush=True)
         return 0
     stream = torch.cuda.current_stream()
+    if args.mode == "backward":
+        return bench_backward(args, spec, layer, x, config, dev)
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(max(args.warmup, 3)):
