@@ -22,9 +22,13 @@
 // and writes da, db (bf16, the next GEMMs' operands) and h = SiLU(a) b (bf16):
 //   da = dh * b * SiLU'(a),  db = dh * SiLU(a),  SiLU'(a) = sigma(a) (1 + a (1 - sigma(a))).
 //
-// Kernel design (one CTA per SM, persistent, 192 threads): warp 0 TMA producer, warp 1
-// TMEM allocation and MMA issue (M = 128, N = 128, K = 16 per instruction), warps 2-5
-// epilogue; 128 x 128 tiles, 6-stage ring of 32 KB, accumulators double buffered in TMEM.
+// Kernel design (persistent CTA pairs, cluster of 2, 192 threads each): a 256 x 256 tile
+// per pair, the even CTA issuing tcgen05.mma cta_group::2 (M = 256, N = 256, K = 16); each
+// CTA loads its 128 rows (or columns) of A and its 128 columns of B per 64-wide K block
+// (32 KB, 6-stage ring), completing on the even CTA's barrier; each CTA's TMEM holds the
+// fp32 accumulators of its 128 rows, double buffered; warp 0 TMA producer, warp 1 TMEM
+// allocation (and MMA issue in the even CTA), warps 2-5 epilogue (fp32 rows staged
+// through shared memory for row-contiguous stores).
 // Every wait is bounded; a wait that runs out records MOE_ERR_TIMEOUT and the CTA drains
 // what it issued before freeing its TMEM.
 #include "common.cuh"
@@ -33,18 +37,23 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 128;
+constexpr int BMC = 128;                  // M rows (or columns) per CTA
+constexpr int BM = 256;                   // M per pair tile
+constexpr int BNC = 128;                  // N columns per CTA
+constexpr int BN = 256;                   // N per pair tile
 constexpr int BK = 64;
 constexpr int STAGES = 6;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
+constexpr int A_BYTES = BMC * BK * 2;
+constexpr int B_BYTES = BNC * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_LD = 36;                // 32-bit words per staged row (16-byte aligned)
+constexpr int EPI_WARP_WORDS = 32 * EPI_LD;
+constexpr int EPI_BYTES = 4 * EPI_WARP_WORDS * 4;
 constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 100000000ull;
-constexpr uint32_t kMnLbo = 8192;   // bytes between the two 64-wide MN halves of a tile
+constexpr uint32_t kMnLbo = 8192;   // bytes between the two 64-wide MN halves of a CTA's tile
 constexpr uint32_t kMnSbo = 1024;   // bytes between groups of 8 K-rows
 
 // SMEM descriptor of an MN-major, 128-byte-swizzled operand tile.
@@ -67,8 +76,7 @@ __device__ __forceinline__ bool bwd_tile(const BwdGemmArgs& a, bool k_seg, const
                                          const int* s_tp, int n_tiles, int64_t t, BwdTile& o) {
   const int G = a.seg_off ? a.groups : 1;
   if (k_seg) {
-    // fixed tiles per group: m_dim / BM x n_tiles
-    const int mt = a.m_dim / BM;
+    const int mt = (a.m_dim + BM - 1) / BM;
     const int64_t per = static_cast<int64_t>(mt) * n_tiles;
     if (t >= per * G) return false;
     o.g = static_cast<int>(t / per);
@@ -94,7 +102,7 @@ __device__ __forceinline__ bool bwd_tile(const BwdGemmArgs& a, bool k_seg, const
 }
 
 template <bool A_MN, bool B_MN, int EPI>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_bwd_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                 const __grid_constant__ CUtensorMap tmB1, const BwdGemmArgs args) {
   // A_MN: K runs over the segment rows (weight gradients); otherwise the rows are M.
@@ -102,7 +110,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* epi = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -112,11 +121,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   int* never = const_cast<int*>(abort_flag) + 1;
   const int G = args.seg_off ? args.groups : 1;
   int* s_off = never + 1;       // [G+1]
-  int* s_tp = s_off + (G + 1);  // [G+1] m-tile prefix (row-segment mode)
+  int* s_tp = s_off + (G + 1);  // [G+1] pair m-tile prefix (row mode)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n_tiles = args.n_dim / BN;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int n_tiles = (args.n_dim + BN - 1) / BN;
   const uint32_t smem_base = smem_u32(smem);
+  const int64_t pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -125,7 +137,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
-      mbar_init(smem_u32(&tempty[b]), 4);
+      mbar_init(smem_u32(&tempty[b]), 8);   // 4 epilogue warps in each CTA of the pair
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -169,9 +181,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_map(&tmB0);
     tma_prefetch_map(&tmB1);
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_holder), TMEM_COLS);
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();   // barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   auto k_blocks_of = [&](const BwdTile& tl) {
@@ -179,7 +192,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -188,27 +201,30 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
       bool ok = true;
       BwdTile tl;
-      for (int64_t t = blockIdx.x; ok && bwd_tile(args, K_SEG, s_off, s_tp, n_tiles, t, tl);
-           t += gridDim.x) {
+      for (int64_t t = pair_id; ok && bwd_tile(args, K_SEG, s_off, s_tp, n_tiles, t, tl);
+           t += n_pairs) {
         const int kbs = k_blocks_of(tl);
-        const int m0 = tl.m * BM, n0 = tl.n * BN;
+        // this CTA's halves: M (rows or columns) m0.., N columns n0..
+        const int m0 = tl.m * BM + static_cast<int>(rank) * BMC;
+        const int n0 = tl.n * BN + static_cast<int>(rank) * BNC;
         for (int kb = 0; kb < kbs; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
                                  kWaitLimitNs)) {
             ok = false;
             break;
           }
-          const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t fb_local = smem_u32(&full[stage]);
+          const uint32_t fb = mapa_shared(fb_local, 0);
+          if (leader) mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
           const uint32_t sA = smem_base + stage * STAGE_BYTES;
           const uint32_t sB = sA + A_BYTES;
           const int k0 = kb * BK;
           if (A_MN) {
             const int row = tl.seg_start + k0;
-            tma_load_2d(sA, &tmA, m0, row, fb);
-            tma_load_2d(sA + kMnLbo, &tmA, m0 + 64, row, fb);
+            tma_load_2d_pair(sA, &tmA, m0, row, fb);
+            tma_load_2d_pair(sA + kMnLbo, &tmA, m0 + 64, row, fb);
           } else {
-            tma_load_2d(sA, &tmA, k0, tl.seg_start + m0, fb);
+            tma_load_2d_pair(sA, &tmA, k0, tl.seg_start + m0, fb);
           }
           if (B_MN) {
             // B[n][k] = view[row(k)][n]: weights (group rows) or segment rows
@@ -222,8 +238,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else {
               row = tl.g * args.b_group_rows + k0;
             }
-            tma_load_2d(sB, mb, n0, row, fb);
-            tma_load_2d(sB + kMnLbo, mb, n0 + 64, row, fb);
+            tma_load_2d_pair(sB, mb, n0, row, fb);
+            tma_load_2d_pair(sB + kMnLbo, mb, n0 + 64, row, fb);
           } else {
             // B[n][k] = view[g * b_group_rows + n][k], the second map past b_split_n
             const CUtensorMap* mb = &tmB0;
@@ -232,21 +248,21 @@ __global__ void __launch_bounds__(THREADS, 1)
               mb = &tmB1;
               nn = n0 - args.b_split_n;
             }
-            tma_load_2d(sB, mb, k0, tl.g * args.b_group_rows + nn, fb);
+            tma_load_2d_pair(sB, mb, k0, tl.g * args.b_group_rows + nn, fb);
           }
           issued_parity[stage] = static_cast<int>(phase);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok)
+      if (!ok && leader)
         for (int s = 0; s < STAGES; ++s)
           if (issued_parity[s] >= 0)
             mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>(issued_parity[s]), never,
                               nullptr, kDrainLimitNs);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (leader && lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN) | (A_MN ? (1u << 15) : 0u) |
                                  (B_MN ? (1u << 16) : 0u);
       int stage = 0;
@@ -254,8 +270,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       BwdTile tl;
       int64_t local = 0;
-      for (int64_t t = blockIdx.x; ok && bwd_tile(args, K_SEG, s_off, s_tp, n_tiles, t, tl);
-           t += gridDim.x, ++local) {
+      for (int64_t t = pair_id; ok && bwd_tile(args, K_SEG, s_off, s_tp, n_tiles, t, tl);
+           t += n_pairs, ++local) {
         const int buf = static_cast<int>(local & 1);
         const uint32_t use = static_cast<uint32_t>(local >> 1);
         if (!mbar_wait_bounded(smem_u32(&tempty[buf]), (use & 1u) ^ 1u, abort_flag, args.status,
@@ -279,26 +295,27 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int j = 0; j < BK / 16; ++j) {
             const uint64_t ad = A_MN ? sw128_mnmajor_desc(sA + j * 2048) : sw128_kmajor_desc(sA) + 2 * j;
             const uint64_t bd = B_MN ? sw128_mnmajor_desc(sB + j * 2048) : sw128_kmajor_desc(sB) + 2 * j;
-            tc_mma_bf16(d_acc, ad, bd, idesc, (kb > 0 || j > 0) ? 1u : 0u);
+            tc_mma_bf16_pair(d_acc, ad, bd, idesc, (kb > 0 || j > 0) ? 1u : 0u);
           }
-          tc_commit(smem_u32(&empty[stage]));
+          tc_commit_pair(smem_u32(&empty[stage]), 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(smem_u32(&tfull[buf]));   // with no K blocks this arrives at once
+        tc_commit_pair(smem_u32(&tfull[buf]), 0x3);   // with no K blocks this arrives at once
       }
       if (!ok) {
-        tc_commit(smem_u32(drain));
+        tc_commit_pair(smem_u32(drain), 0x1);
         mbar_wait_bounded(smem_u32(drain), 0, never, nullptr, kDrainLimitNs);
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
+    uint32_t* stg = epi + (warp - 2) * EPI_WARP_WORDS;
     BwdTile tl;
     int64_t local = 0;
-    for (int64_t t = blockIdx.x; bwd_tile(args, K_SEG, s_off, s_tp, n_tiles, t, tl);
-         t += gridDim.x, ++local) {
+    for (int64_t t = pair_id; bwd_tile(args, K_SEG, s_off, s_tp, n_tiles, t, tl);
+         t += n_pairs, ++local) {
       const int buf = static_cast<int>(local & 1);
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       bool ready = true;
@@ -311,9 +328,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool empty_k = k_blocks_of(tl) == 0;   // no rows: the product is zero
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
-      const int r = tl.m * BM + q * 32 + lane;     // tile row of this thread
+      const int r0 = tl.m * BM + static_cast<int>(rank) * BMC + q * 32;   // first tile row of the warp
+      // destination of the warp's 32 rows (fp32 epilogue); rows past the end are dropped
+      float* obase = args.out;
+      int64_t orow0 = 0;
+      int64_t rows_left = 0;
+      if (EPI == kBwdEpiF32) {
+        if (K_SEG) {
+          orow0 = r0;
+          obase = args.out + static_cast<int64_t>(tl.g) * args.group_stride;
+          if (args.out_split_m > 0 && r0 >= args.out_split_m) {
+            obase = args.out2 + static_cast<int64_t>(tl.g) * args.group_stride;
+            orow0 = r0 - args.out_split_m;
+          }
+          rows_left = args.m_dim - r0;
+        } else {
+          orow0 = tl.seg_start + r0;
+          rows_left = tl.seg_end - orow0;
+        }
+      }
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
+        const int col = tl.n * BN + c * 32;
+        if (col >= args.n_dim) break;
         uint32_t v[32];
         if (empty_k) {
 #pragma unroll
@@ -321,82 +358,82 @@ __global__ void __launch_bounds__(THREADS, 1)
         } else {
           tmem_ld32(taddr + c * 32, v);
         }
-        const int col = tl.n * BN + c * 32;
         if (EPI == kBwdEpiF32) {
-          float* base;
-          int64_t row;
-          if (K_SEG) {
-            // C block of group g: rows m (split into out / out2 at out_split_m)
-            row = r;
-            base = args.out + static_cast<int64_t>(tl.g) * args.group_stride;
-            if (args.out_split_m > 0 && r >= args.out_split_m) {
-              base = args.out2 + static_cast<int64_t>(tl.g) * args.group_stride;
-              row = r - args.out_split_m;
-            }
-          } else {
-            row = tl.seg_start + r;
-            base = args.out;
-            if (row >= tl.seg_end) continue;
-          }
-          float* dst = base + row * args.ldo + col;
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4)
-            *reinterpret_cast<float4*>(dst + 4 * v4) =
-                make_float4(__uint_as_float(v[4 * v4]), __uint_as_float(v[4 * v4 + 1]),
-                            __uint_as_float(v[4 * v4 + 2]), __uint_as_float(v[4 * v4 + 3]));
+            *reinterpret_cast<uint4*>(stg + lane * EPI_LD + 4 * v4) =
+                make_uint4(v[4 * v4], v[4 * v4 + 1], v[4 * v4 + 2], v[4 * v4 + 3]);
+          __syncwarp();
+          // eight lanes per row (16 bytes each), four rows per pass
+#pragma unroll
+          for (int pass = 0; pass < 8; ++pass) {
+            const int rr = pass * 4 + lane / 8;
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * EPI_LD + (lane % 8) * 4);
+            if (rr < rows_left)
+              *reinterpret_cast<uint4*>(obase + (orow0 + rr) * args.ldo + col + (lane % 8) * 4) = val;
+          }
+          __syncwarp();
         } else {
           // SwiGLU backward: dh in v; a, b from ab; da | db and h out (bf16)
-          const int64_t row = tl.seg_start + r;
-          if (row >= tl.seg_end) continue;
-          const float* arow = args.ab + row * (2 * static_cast<int64_t>(args.width));
-          __nv_bfloat16* drow = args.dab + row * (2 * static_cast<int64_t>(args.width));
-          __nv_bfloat16* hrow = args.hout + row * static_cast<int64_t>(args.width);
+          const int64_t row = tl.seg_start + r0 + lane;
+          if (row < tl.seg_end) {
+            const float4* arow =
+                reinterpret_cast<const float4*>(args.ab + row * (2 * static_cast<int64_t>(args.width)) + col);
+            const float4* brow = reinterpret_cast<const float4*>(
+                args.ab + row * (2 * static_cast<int64_t>(args.width)) + args.width + col);
+            __nv_bfloat16* drow = args.dab + row * (2 * static_cast<int64_t>(args.width));
+            __nv_bfloat16* hrow = args.hout + row * static_cast<int64_t>(args.width);
 #pragma unroll
-          for (int v8 = 0; v8 < 4; ++v8) {
-            uint32_t da2[4], db2[4], h2[4];
+            for (int v8 = 0; v8 < 4; ++v8) {
+              const float4 a0 = arow[2 * v8], a1 = arow[2 * v8 + 1];
+              const float4 b0 = brow[2 * v8], b1 = brow[2 * v8 + 1];
+              const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+              const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+              uint32_t da2[4], db2[4], h2[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float dav[2], dbv[2], hv[2];
+              for (int i = 0; i < 4; ++i) {
+                float dav[2], dbv[2], hv[2];
 #pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int j = col + 8 * v8 + 2 * i + e;
-                const float a = arow[j];
-                const float b = arow[args.width + j];
-                const float dh = __uint_as_float(v[8 * v8 + 2 * i + e]);
-                const float sg = 1.0f / (1.0f + __expf(-a));
-                const float sl = a * sg;
-                dav[e] = dh * b * (sg * (1.0f + a * (1.0f - sg)));
-                dbv[e] = dh * sl;
-                hv[e] = sl * b;
+                for (int e = 0; e < 2; ++e) {
+                  const float a = av[2 * i + e];
+                  const float b = bv[2 * i + e];
+                  const float dh = __uint_as_float(v[8 * v8 + 2 * i + e]);
+                  const float sg = 1.0f / (1.0f + __expf(-a));
+                  const float sl = a * sg;
+                  dav[e] = dh * b * (sg * (1.0f + a * (1.0f - sg)));
+                  dbv[e] = dh * sl;
+                  hv[e] = sl * b;
+                }
+                da2[i] = pack_bf16x2(dav[0], dav[1]);
+                db2[i] = pack_bf16x2(dbv[0], dbv[1]);
+                h2[i] = pack_bf16x2(hv[0], hv[1]);
               }
-              da2[i] = pack_bf16x2(dav[0], dav[1]);
-              db2[i] = pack_bf16x2(dbv[0], dbv[1]);
-              h2[i] = pack_bf16x2(hv[0], hv[1]);
+              const int j0 = col + 8 * v8;
+              *reinterpret_cast<uint4*>(drow + j0) = make_uint4(da2[0], da2[1], da2[2], da2[3]);
+              *reinterpret_cast<uint4*>(drow + args.width + j0) = make_uint4(db2[0], db2[1], db2[2], db2[3]);
+              *reinterpret_cast<uint4*>(hrow + j0) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
             }
-            const int j0 = col + 8 * v8;
-            *reinterpret_cast<uint4*>(drow + j0) = make_uint4(da2[0], da2[1], da2[2], da2[3]);
-            *reinterpret_cast<uint4*>(drow + args.width + j0) = make_uint4(db2[0], db2[1], db2[2], db2[3]);
-            *reinterpret_cast<uint4*>(hrow + j0) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
     }
   }
 
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();   // no CTA leaves while its partner may still use its memory
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
 size_t bwd_smem_bytes(int groups) {
-  return 1024 + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5) + 16 + 8 * (static_cast<size_t>(groups) + 1) +
-         64;
+  return 1024 + STAGES * STAGE_BYTES + EPI_BYTES + 8 * (2 * STAGES + 5) + 16 +
+         8 * (static_cast<size_t>(groups) + 1) + 64;
 }
 
 template <bool A_MN, bool B_MN, int EPI>
@@ -407,9 +444,9 @@ cudaError_t launch_one_bwd(const CUtensorMap& a, const CUtensorMap& b0, const CU
   auto kern = tc_bwd_gemm<A_MN, B_MN, EPI>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  const int sms = device_sm_count();
-  const int64_t grid = max_tiles < sms ? max_tiles : sms;
-  kern<<<static_cast<unsigned>(grid), THREADS, smem, s>>>(a, b0, b1, args);
+  const int64_t pairs_max = device_sm_count() >= 2 ? device_sm_count() / 2 : 1;
+  const int64_t pairs = max_tiles < pairs_max ? max_tiles : pairs_max;
+  kern<<<static_cast<unsigned>(2 * pairs), THREADS, smem, s>>>(a, b0, b1, args);
   return cudaGetLastError();
 }
 
