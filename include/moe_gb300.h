@@ -303,9 +303,14 @@ moe_status moe_bias_update(int32_t N, const int32_t* counts, float gamma, float*
  *   dx_t += (W_g^e)^T da + (W_u^e)^T db,  dW_d^e += gf h^T,  dW_g^e += da x_t^T,  dW_u^e += db x_t^T
  * with a = W_g^e x_t, b = W_u^e x_t (recomputed), h = SiLU(a) b, dh = (W_d^e)^T gf,
  * da = dh b SiLU'(a), db = dh SiLU(a); the shared expert likewise with gf = s_t dy_t.
- * Dropped routes carry no gradient.  bf16 layers only, with d_model, d_expert and
- * d_shared multiples of 128 (others: MOE_ERR_UNSUPPORTED); operands are bf16 (gf, da, db
- * and h rounded once), accumulation fp32. */
+ * Dropped routes carry no gradient.  With grads->dW_router given, the coefficients carry
+ * gradient too (Figure 70 (b) "including router gradient"): dr_tk = dy_t . f_{e_tk}(x_t),
+ * ds_t = dy_t . g(x_t), differentiated through the selected-weight rule and the scores
+ * (Table 52) back to the logits z (the selection held fixed): dW_r = dz^T x, dx += dz W_r,
+ * and for a learned shared gate dw_s = sum_t ds_t s_t (1 - s_t) x_t, dx += that times w_s.
+ * bf16 layers only, with d_model, d_expert and d_shared multiples of 128 (others:
+ * MOE_ERR_UNSUPPORTED); GEMM operands are bf16 (dy, da, db, r h and dz rounded once),
+ * accumulation fp32. */
 typedef struct moe_grads {
   float* dx;        /* [T][d] fp32 */
   float* dW_gate;   /* [N][d_r][d] fp32 (overwritten) */
@@ -314,6 +319,9 @@ typedef struct moe_grads {
   float* dWs_gate;  /* [d_s][d] fp32; required when d_shared > 0 */
   float* dWs_up;    /* [d_s][d] fp32 */
   float* dWs_down;  /* [d][d_s] fp32 */
+  float* dW_router;        /* [N][d] fp32, or NULL: when given, the gradient through the router
+                            * coefficients is included (dx too); needs fwd->logits */
+  float* dshared_gate_w;   /* [d] fp32: with dW_router and a learned shared gate (Eq. 77) */
 } moe_grads;
 
 /* Bytes of scratch moe_layer_backward needs (256-byte aligned; prepare it with
@@ -322,7 +330,8 @@ moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* The backward pass for upstream gradient dy [T][d] fp32 (device).  x and the weights are
  * those of the forward call; fwd holds that call's routing results (device): topk_idx,
- * topk_w, counts_keep, offsets, route_pos, perm_src, and shared_coef when d_shared > 0.
+ * topk_w, counts_keep, offsets, route_pos, perm_src, shared_coef when d_shared > 0, and
+ * logits when grads->dW_router is given.
  * Writes every array of grads (device, caller-owned).  Asynchronous on the stream; no
  * host synchronisation. */
 moe_status moe_layer_backward(const moe_config* cfg, const moe_weights* w, const void* x,

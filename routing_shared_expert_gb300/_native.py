@@ -46,7 +46,8 @@ class moe_weights(ctypes.Structure):
                                         "W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down")]
 
 
-GRAD_FIELDS = ("dx", "dW_gate", "dW_up", "dW_down", "dWs_gate", "dWs_up", "dWs_down")
+GRAD_FIELDS = ("dx", "dW_gate", "dW_up", "dW_down", "dWs_gate", "dWs_up", "dWs_down", "dW_router",
+               "dshared_gate_w")
 
 
 class moe_grads(ctypes.Structure):

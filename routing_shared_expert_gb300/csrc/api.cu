@@ -482,10 +482,13 @@ moe_status layer_forward(const moe_config* cfg, const moe_weights* w, const void
 
 // ---- backward -------------------------------------------------------------------
 struct BwdLayout {
-  size_t status, seg_pad, x_pad, gf, ab, dab, h, dxr, gs, ab_s, dab_s, h_s, dx_s;
+  size_t status, seg_pad, x_pad, gf, r_pad, ab, dab, h, dxr, dot, gs, s_pad, ab_s, dab_s, h_s, dx_s,
+      dot_s, dz, dxz, du, dws_part;
   size_t total;
   int64_t rows_cap;   // padded routed rows
   int64_t t_pad;      // T rounded up to 64
+  int32_t nt, nt_s;   // 256-column tiles of d_r and d_s (partial dot products per row)
+  int32_t n128;       // N rounded up to 128 (columns of dz)
 };
 
 BwdLayout make_bwd_layout(const moe_config& c) {
@@ -501,19 +504,30 @@ BwdLayout make_bwd_layout(const moe_config& c) {
     o = align256(o + bytes);
     return at;
   };
+  L.nt = static_cast<int32_t>((dr + 255) / 256);
+  L.nt_s = static_cast<int32_t>((ds + 255) / 256);
+  L.n128 = static_cast<int32_t>((N + 127) / 128 * 128);
   L.status = take(256);
   L.seg_pad = take((N + 1) * 4);
   L.x_pad = take(R * d * 2);
   L.gf = take(R * d * 2);
+  L.r_pad = take(R * 4);
   L.ab = take(R * 2 * dr * 4);
   L.dab = take(R * 2 * dr * 2);
   L.h = take(R * dr * 2);
   L.dxr = take(R * d * 4);
+  L.dot = take(R * L.nt * 4);
   L.gs = take(T * d * 2);
+  L.s_pad = take(Tp * 4);
   L.ab_s = take(Tp * 2 * ds * 4);
   L.dab_s = take(Tp * 2 * ds * 2);
   L.h_s = take(Tp * ds * 2);
   L.dx_s = take(Tp * d * 4);
+  L.dot_s = take(Tp * static_cast<size_t>(L.nt_s) * 4);
+  L.dz = take(T * static_cast<size_t>(L.n128) * 2);
+  L.dxz = take(Tp * d * 4);
+  L.du = take(T * 4);
+  L.dws_part = take(static_cast<size_t>(kDwsChunks) * d * 4);
   L.total = o;
   return L;
 }
@@ -530,9 +544,10 @@ moe_status check_bwd_cfg(const moe_config* c) {
 // The five GEMMs of one expert family (routed: groups of padded segments; shared: one
 // dense group of T rows), then nothing else: the caller combines dx.
 moe_status bwd_family(const moe_config& c, bool routed, const int32_t* seg_pad, int64_t rows,
-                      const void* x_rows, const __nv_bfloat16* gf, float* ab, __nv_bfloat16* dab,
-                      __nv_bfloat16* h, float* dxr, const void* Wg, const void* Wu, const void* Wd,
-                      float* dWg, float* dWu, float* dWd, int32_t* status, cudaStream_t st) {
+                      const void* x_rows, const __nv_bfloat16* gf, const float* row_scale,
+                      float* dot_part, float* ab, __nv_bfloat16* dab, __nv_bfloat16* h, float* dxr,
+                      const void* Wg, const void* Wu, const void* Wd, float* dWg, float* dWu,
+                      float* dWd, int32_t* status, cudaStream_t st) {
   const int G = routed ? c.N : 1;
   const int64_t d = c.d_model, w = routed ? c.d_expert : c.d_shared;
   // rows of the row-major activation maps: routed rows_cap; shared: x and gf have T rows
@@ -576,6 +591,8 @@ moe_status bwd_family(const moe_config& c, bool routed, const int32_t* seg_pad, 
   a.ab = ab;
   a.dab = dab;
   a.hout = h;
+  a.row_scale = row_scale;
+  a.dot_part = dot_part;
   a.width = static_cast<int32_t>(w);
   if (!st_ok(launch_bwd_gemm(kBwdRowsMnBSwiglu, mGf, mWd, mWd, a, row_tiles * (w / 128), st)))
     return MOE_ERR_CUDA;
@@ -630,6 +647,11 @@ moe_status layer_backward(const moe_config* cfg, const moe_weights* w, const voi
     return MOE_ERR_INVALID_ARG;
   if (!w->W_gate || !w->W_up || !w->W_down || (shared && (!w->Ws_gate || !w->Ws_up || !w->Ws_down)))
     return MOE_ERR_INVALID_ARG;
+  // the gradient through the router coefficients, when dW_router is given
+  const bool router = g->dW_router != nullptr;
+  const bool gate = router && shared && c.shared_mode == MOE_SHARED_SIGMOID_GATE;
+  if (router && (!fwd->logits || !w->W_router)) return MOE_ERR_INVALID_ARG;
+  if (gate && (!g->dshared_gate_w || !w->shared_gate_w)) return MOE_ERR_INVALID_ARG;
   if (c.T > 0 && (!x || !dy)) return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_MISALIGNED;
   const BwdLayout L = make_bwd_layout(c);
@@ -651,29 +673,99 @@ moe_status layer_backward(const moe_config* cfg, const moe_weights* w, const voi
   rp.seg_pad = seg_pad;
   rp.x_pad = at<__nv_bfloat16>(ws, L.x_pad);
   rp.gf = at<__nv_bfloat16>(ws, L.gf);
+  rp.r_pad = at<float>(ws, L.r_pad);
   rp.T = c.T;
   rp.d = c.d_model;
   rp.N = c.N;
   rp.K = c.K;
   rp.status = status;
   if (!ok(launch_bwd_rows(rp, L.rows_cap, st))) return MOE_ERR_CUDA;
-  s = bwd_family(c, true, seg_pad, L.rows_cap, rp.x_pad, rp.gf, at<float>(ws, L.ab),
+  s = bwd_family(c, true, seg_pad, L.rows_cap, rp.x_pad, rp.gf, rp.r_pad,
+                 router ? at<float>(ws, L.dot) : nullptr, at<float>(ws, L.ab),
                  at<__nv_bfloat16>(ws, L.dab), at<__nv_bfloat16>(ws, L.h), at<float>(ws, L.dxr),
                  w->W_gate, w->W_up, w->W_down, g->dW_gate, g->dW_up, g->dW_down, status, st);
   if (s != MOE_OK) return s;
   float* dxs = nullptr;
   if (shared) {
     __nv_bfloat16* gs = at<__nv_bfloat16>(ws, L.gs);
-    if (!ok(launch_shared_scale(dy, fwd->shared_coef, c.T, c.d_model, gs, st))) return MOE_ERR_CUDA;
+    float* s_pad = at<float>(ws, L.s_pad);
+    if (!ok(launch_shared_scale(dy, fwd->shared_coef, c.T, L.t_pad, c.d_model, gs, s_pad, st)))
+      return MOE_ERR_CUDA;
     dxs = at<float>(ws, L.dx_s);
-    s = bwd_family(c, false, nullptr, L.t_pad, x, gs, at<float>(ws, L.ab_s),
-                   at<__nv_bfloat16>(ws, L.dab_s), at<__nv_bfloat16>(ws, L.h_s), dxs, w->Ws_gate,
-                   w->Ws_up, w->Ws_down, g->dWs_gate, g->dWs_up, g->dWs_down, status, st);
+    s = bwd_family(c, false, nullptr, L.t_pad, x, gs, s_pad, gate ? at<float>(ws, L.dot_s) : nullptr,
+                   at<float>(ws, L.ab_s), at<__nv_bfloat16>(ws, L.dab_s),
+                   at<__nv_bfloat16>(ws, L.h_s), dxs, w->Ws_gate, w->Ws_up, w->Ws_down,
+                   g->dWs_gate, g->dWs_up, g->dWs_down, status, st);
     if (s != MOE_OK) return s;
+  }
+  float* dxz = nullptr;
+  float* du = nullptr;
+  if (router) {
+    // dz per token, then dW_r = dz^T x and dz W_r
+    __nv_bfloat16* dz = at<__nv_bfloat16>(ws, L.dz);
+    RouterBwdParams zp{};
+    zp.logits = fwd->logits;
+    zp.topk_idx = fwd->topk_idx;
+    zp.route_pos = fwd->route_pos;
+    zp.offsets = fwd->offsets;
+    zp.seg_pad = seg_pad;
+    zp.dot_part = at<float>(ws, L.dot);
+    zp.nt = L.nt;
+    zp.dot_part_s = gate ? at<float>(ws, L.dot_s) : nullptr;
+    zp.nt_s = L.nt_s;
+    zp.shared_coef = fwd->shared_coef;
+    zp.T = c.T;
+    zp.N = c.N;
+    zp.K = c.K;
+    zp.score = c.score;
+    zp.norm = c.norm;
+    zp.alpha = c.alpha;
+    zp.norm_p = c.norm_p;
+    zp.dz = dz;
+    zp.n128 = L.n128;
+    du = gate ? at<float>(ws, L.du) : nullptr;
+    zp.du = du;
+    zp.status = status;
+    if (!ok(launch_router_bwd(zp, st))) return MOE_ERR_CUDA;
+    CUtensorMap mZk, mZm, mWr, mX;
+    if (!make_bf16_map(&mZk, dz, L.n128, c.T, 128) || !make_bf16_map(&mZm, dz, L.n128, c.T, 64) ||
+        !make_bf16_map(&mWr, w->W_router, c.d_model, c.N, 64) ||
+        !make_bf16_map(&mX, x, c.d_model, c.T, 64))
+      return MOE_ERR_CUDA;
+    BwdGemmArgs a{};
+    a.seg_off = nullptr;
+    a.dense_rows = static_cast<int32_t>(L.t_pad);
+    a.groups = 1;
+    a.status = status;
+    // dW_r [N][d] = dz^T x (K = tokens)
+    a.m_dim = c.N;
+    a.n_dim = c.d_model;
+    a.b_group_rows = -1;
+    a.out = g->dW_router;
+    a.ldo = c.d_model;
+    if (!ok(launch_bwd_gemm(kBwdWeightGrad, mZm, mX, mX, a,
+                            ((c.N + 255) / 256) * ((c.d_model + 255) / 256), st)))
+      return MOE_ERR_CUDA;
+    // dz W_r [T][d] (K = N rounded up to 128; dz is zero past N and W_r reads zero past N)
+    dxz = at<float>(ws, L.dxz);
+    a.m_dim = 0;
+    a.k_dim = L.n128;
+    a.n_dim = c.d_model;
+    a.b_group_rows = 0;
+    a.out = dxz;
+    a.ldo = c.d_model;
+    if (!ok(launch_bwd_gemm(kBwdRowsMnB, mZk, mWr, mWr, a,
+                            (L.t_pad / 256 + 1) * ((c.d_model + 255) / 256), st)))
+      return MOE_ERR_CUDA;
+    if (gate && !ok(launch_dws(du, x, c.T, c.d_model, at<float>(ws, L.dws_part), g->dshared_gate_w, st)))
+      return MOE_ERR_CUDA;
   }
   BwdCombineParams cp{};
   cp.dxr = at<float>(ws, L.dxr);
   cp.dxs = dxs;
+  cp.dxz = dxz;
+  cp.du = du;
+  cp.gate_w = static_cast<const __nv_bfloat16*>(w->shared_gate_w);
   cp.route_pos = fwd->route_pos;
   cp.topk_idx = fwd->topk_idx;
   cp.offsets = fwd->offsets;

@@ -35,8 +35,9 @@ __global__ void pad_offsets_kernel(const int32_t* counts_keep, int N, int32_t* s
   }
 }
 
-// One warp per padded row: the row of x and the scaled upstream gradient of its route,
-// or zeros for a padding row.
+// One warp per padded row: the row of x, the upstream gradient dy of its token (bf16,
+// unscaled) and the route's coefficient r (applied in the GEMM epilogues), or zeros for a
+// padding row.
 __global__ void __launch_bounds__(256) bwd_rows_kernel(BwdRowsParams p) {
   __shared__ int32_t s_pad[kMaxExperts + 1];
   for (int i = threadIdx.x; i <= p.N; i += blockDim.x) s_pad[i] = p.seg_pad[i];
@@ -59,6 +60,7 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(BwdRowsParams p) {
       xo[v] = make_uint4(0, 0, 0, 0);
       go[v] = make_uint4(0, 0, 0, 0);
     }
+    if (lane == 0) p.r_pad[pp] = 0.f;
     return;
   }
   const int64_t pos = p.offsets[e] + local;
@@ -83,24 +85,31 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(BwdRowsParams p) {
   for (int v = lane; v < vecs; v += 32) {
     xo[v] = xi[v];
     const float4 a = dyi[2 * v], b = dyi[2 * v + 1];
-    go[v] = make_uint4(pack_bf16x2(r * a.x, r * a.y), pack_bf16x2(r * a.z, r * a.w),
-                       pack_bf16x2(r * b.x, r * b.y), pack_bf16x2(r * b.z, r * b.w));
+    go[v] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                       pack_bf16x2(b.z, b.w));
   }
+  if (lane == 0) p.r_pad[pp] = r;
 }
 
-// gs[t] = s_t dy_t (bf16), one warp per token.
+// gs[t] = dy_t (bf16) and s_pad[t] = s_t (0 for the rows up to T rounded to 64), one
+// warp per row.
 __global__ void __launch_bounds__(256) shared_scale_kernel(const float* dy, const float* s, int64_t T,
-                                                           int d, __nv_bfloat16* gs) {
+                                                           int64_t t_pad, int d, __nv_bfloat16* gs,
+                                                           float* s_pad) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + warp;
-  if (t >= T) return;
-  const float c = s[t];
+  if (t >= t_pad) return;
+  if (t >= T) {
+    if (lane == 0) s_pad[t] = 0.f;
+    return;
+  }
+  if (lane == 0) s_pad[t] = s[t];
   const float4* dyi = reinterpret_cast<const float4*>(dy + t * d);
   uint4* o = reinterpret_cast<uint4*>(gs + t * d);
   for (int v = lane; v < d / 8; v += 32) {
     const float4 a = dyi[2 * v], b = dyi[2 * v + 1];
-    o[v] = make_uint4(pack_bf16x2(c * a.x, c * a.y), pack_bf16x2(c * a.z, c * a.w),
-                      pack_bf16x2(c * b.x, c * b.y), pack_bf16x2(c * b.z, c * b.w));
+    o[v] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                      pack_bf16x2(b.z, b.w));
   }
 }
 
@@ -134,11 +143,189 @@ __global__ void __launch_bounds__(256) dx_combine_kernel(BwdCombineParams p) {
       const float4 v = *reinterpret_cast<const float4*>(p.dxs + t * p.d + c);
       acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
+    if (p.dxz) {   // through the router: dz W_r
+      const float4 v = *reinterpret_cast<const float4*>(p.dxz + t * p.d + c);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    if (p.du) {    // through a learned shared gate: du w_s
+      const float u = p.du[t];
+      const float4 w = make_float4(to_f32(p.gate_w[c]), to_f32(p.gate_w[c + 1]),
+                                   to_f32(p.gate_w[c + 2]), to_f32(p.gate_w[c + 3]));
+      acc.x += u * w.x; acc.y += u * w.y; acc.z += u * w.z; acc.w += u * w.w;
+    }
     *reinterpret_cast<float4*>(p.dx + t * p.d + c) = acc;
   }
 }
 
+// Gradient through the router coefficients, one warp per token (Table 52 rules; the
+// selection held fixed): dr_k = dy . f_k = sum over tiles of dh_u . h of the route's row
+// (zero for a dropped route), dw = alpha dr, then
+//   softmax over the selected logits:  dz_S = w (dw - sum_k w_k dw_k)
+//   otherwise dq_S from the rule (none: dw; L1: (dw - sum w dw) / sum q_S;
+//   L_p: dw / n - (sum w dw) w^(p-1) / n) and dz = q (dq - sum_S q dq) for softmax
+//   scores, dz_S = dq_S q_S (1 - q_S) for sigmoid scores.
+// A learned shared gate s = sigma(u) adds du = (dy . g) s (1 - s), dy . g likewise from
+// the shared expert's tiles.
+__global__ void __launch_bounds__(256) router_bwd_kernel(RouterBwdParams p) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (t >= p.T) return;
+  const float* z = p.logits + t * p.N;
+  // coefficient gradients of the K slots
+  float dw[kMaxTopK], zs[kMaxTopK];
+  int si[kMaxTopK];
+#pragma unroll
+  for (int k = 0; k < kMaxTopK; ++k) {
+    dw[k] = 0.f;
+    zs[k] = 0.f;
+    si[k] = -1;
+    if (k < p.K) {
+      const int e = p.topk_idx[t * p.K + k];
+      si[k] = e;
+      zs[k] = (e >= 0 && e < p.N) ? z[e] : 0.f;
+      const int32_t pos = p.route_pos[t * p.K + k];
+      if (pos >= 0 && e >= 0 && e < p.N) {
+        const int64_t row = p.seg_pad[e] + (pos - p.offsets[e]);
+        float acc = 0.f;
+        for (int n = 0; n < p.nt; ++n) acc += p.dot_part[row * p.nt + n];
+        dw[k] = p.alpha * acc;
+      }
+    }
+  }
+  float dzS[kMaxTopK];
+  float c = 0.f;          // softmax scores: sum_S q dq
+  float m = -INFINITY, sum = 0.f;
+  const bool soft = p.score == MOE_SCORE_SOFTMAX;
+  if (p.norm == MOE_NORM_SOFTMAX_SELECTED) {
+    float ms = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k)
+      if (k < p.K) ms = fmaxf(ms, zs[k]);
+    float w[kMaxTopK], tot = 0.f, wdw = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k) {
+      w[k] = k < p.K ? expf(zs[k] - ms) : 0.f;
+      tot += w[k];
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k) {
+      w[k] /= tot;
+      wdw += w[k] * dw[k];
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k) dzS[k] = k < p.K ? w[k] * (dw[k] - wdw) : 0.f;
+  } else {
+    float q[kMaxTopK];
+    if (soft) {
+      for (int j = lane; j < p.N; j += 32) m = fmaxf(m, z[j]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      for (int j = lane; j < p.N; j += 32) sum += expf(z[j] - m);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k)
+      q[k] = k < p.K ? (soft ? expf(zs[k] - m) / sum : 1.f / (1.f + expf(-zs[k]))) : 0.f;
+    float dq[kMaxTopK];
+    if (p.norm == MOE_NORM_NONE) {
+#pragma unroll
+      for (int k = 0; k < kMaxTopK; ++k) dq[k] = dw[k];
+    } else {
+      float S = 0.f;
+      if (p.norm == MOE_NORM_L1_SELECTED) {
+#pragma unroll
+        for (int k = 0; k < kMaxTopK; ++k) S += q[k];
+      } else {   // L_p: n = (sum q^p)^(1/p), scaled by the largest q
+        float mx = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxTopK; ++k) mx = fmaxf(mx, q[k]);
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxTopK; ++k)
+          if (k < p.K) acc += powf(q[k] / mx, p.norm_p);
+        S = mx * powf(acc, 1.f / p.norm_p);
+      }
+      float w[kMaxTopK], wdw = 0.f;
+#pragma unroll
+      for (int k = 0; k < kMaxTopK; ++k) {
+        w[k] = q[k] / S;
+        wdw += w[k] * dw[k];
+      }
+#pragma unroll
+      for (int k = 0; k < kMaxTopK; ++k) {
+        if (p.norm == MOE_NORM_L1_SELECTED)
+          dq[k] = (dw[k] - wdw) / S;
+        else
+          dq[k] = k < p.K ? dw[k] / S - wdw * powf(w[k], p.norm_p - 1.f) / S : 0.f;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k) {
+      if (soft) c += q[k] * dq[k];
+      dzS[k] = k < p.K ? (soft ? q[k] * dq[k] : dq[k] * q[k] * (1.f - q[k])) : 0.f;
+    }
+  }
+  // dz over all columns: selected ones get their slot term; with softmax scores every
+  // column also gets -q_j c
+  __nv_bfloat16* out = p.dz + t * p.n128;
+  for (int j = lane; j < p.n128; j += 32) {
+    float v = 0.f;
+    if (j < p.N) {
+#pragma unroll
+      for (int k = 0; k < kMaxTopK; ++k)
+        if (k < p.K && si[k] == j) v += dzS[k];
+      if (soft && p.norm != MOE_NORM_SOFTMAX_SELECTED) v -= expf(z[j] - m) / sum * c;
+    }
+    out[j] = __float2bfloat16(v);
+  }
+  if (p.du != nullptr && lane == 0) {
+    float ds = 0.f;
+    for (int n = 0; n < p.nt_s; ++n) ds += p.dot_part_s[t * p.nt_s + n];
+    const float s = p.shared_coef[t];
+    p.du[t] = ds * s * (1.f - s);
+  }
+}
+
+// dw_s = sum_t du_t x_t: partial sums over 64 chunks of tokens, then their ordered sum.
+__global__ void __launch_bounds__(256) dws_partial_kernel(const float* du, const __nv_bfloat16* x,
+                                                          int64_t T, int d, float* part) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= d) return;
+  const int64_t per = (T + gridDim.y - 1) / gridDim.y;
+  const int64_t t0 = blockIdx.y * per;
+  const int64_t t1 = t0 + per < T ? t0 + per : T;
+  float acc = 0.f;
+  for (int64_t t = t0; t < t1; ++t) acc += du[t] * __bfloat162float(x[t * d + i]);
+  part[static_cast<int64_t>(blockIdx.y) * d + i] = acc;
+}
+
+__global__ void __launch_bounds__(256) dws_final_kernel(const float* part, int chunks, int d, float* dws) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= d) return;
+  float acc = 0.f;
+  for (int c = 0; c < chunks; ++c) acc += part[static_cast<int64_t>(c) * d + i];
+  dws[i] = acc;
+}
+
 }  // namespace
+
+cudaError_t launch_router_bwd(const RouterBwdParams& p, cudaStream_t s) {
+  if (p.T <= 0) return cudaSuccess;
+  router_bwd_kernel<<<static_cast<unsigned>((p.T + 7) / 8), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dws(const float* du, const void* x, int64_t T, int d, float* part, float* dws,
+                       cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>((d + 255) / 256), kDwsChunks);
+  dws_partial_kernel<<<grid, 256, 0, s>>>(du, static_cast<const __nv_bfloat16*>(x), T, d, part);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dws_final_kernel<<<static_cast<unsigned>((d + 255) / 256), 256, 0, s>>>(part, kDwsChunks, d, dws);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pad_offsets(const int32_t* counts_keep, int N, int32_t* seg_pad, cudaStream_t s) {
   pad_offsets_kernel<<<1, 32, 0, s>>>(counts_keep, N, seg_pad);
@@ -151,10 +338,11 @@ cudaError_t launch_bwd_rows(const BwdRowsParams& p, int64_t rows_cap, cudaStream
   return cudaGetLastError();
 }
 
-cudaError_t launch_shared_scale(const float* dy, const float* sc, int64_t T, int d, __nv_bfloat16* gs,
-                                cudaStream_t s) {
-  if (T <= 0) return cudaSuccess;
-  shared_scale_kernel<<<static_cast<unsigned>((T + 7) / 8), 256, 0, s>>>(dy, sc, T, d, gs);
+cudaError_t launch_shared_scale(const float* dy, const float* sc, int64_t T, int64_t t_pad, int d,
+                                __nv_bfloat16* gs, float* s_pad, cudaStream_t s) {
+  if (t_pad <= 0) return cudaSuccess;
+  shared_scale_kernel<<<static_cast<unsigned>((t_pad + 7) / 8), 256, 0, s>>>(dy, sc, T, t_pad, d, gs,
+                                                                            s_pad);
   return cudaGetLastError();
 }
 

@@ -347,6 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           rows_left = tl.seg_end - orow0;
         }
       }
+      float dot = 0.f;   // SwiGLU epilogue: this row's sum of dh_u * h over the tile's columns
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         const int col = tl.n * BN + c * 32;
@@ -374,9 +375,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           __syncwarp();
         } else {
-          // SwiGLU backward: dh in v; a, b from ab; da | db and h out (bf16)
+          // SwiGLU backward: dh_u in v; a, b from ab; da | db and scale * h out (bf16)
           const int64_t row = tl.seg_start + r0 + lane;
           if (row < tl.seg_end) {
+            const float sc = args.row_scale[row];
             const float4* arow =
                 reinterpret_cast<const float4*>(args.ab + row * (2 * static_cast<int64_t>(args.width)) + col);
             const float4* brow = reinterpret_cast<const float4*>(
@@ -397,12 +399,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 for (int e = 0; e < 2; ++e) {
                   const float a = av[2 * i + e];
                   const float b = bv[2 * i + e];
-                  const float dh = __uint_as_float(v[8 * v8 + 2 * i + e]);
+                  const float dhu = __uint_as_float(v[8 * v8 + 2 * i + e]);
+                  const float dh = sc * dhu;
                   const float sg = 1.0f / (1.0f + __expf(-a));
                   const float sl = a * sg;
                   dav[e] = dh * b * (sg * (1.0f + a * (1.0f - sg)));
                   dbv[e] = dh * sl;
-                  hv[e] = sl * b;
+                  hv[e] = sc * (sl * b);
+                  dot += dhu * (sl * b);
                 }
                 da2[i] = pack_bf16x2(dav[0], dav[1]);
                 db2[i] = pack_bf16x2(dbv[0], dbv[1]);
@@ -415,6 +419,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             }
           }
         }
+      }
+      if (EPI == kBwdEpiSwiglu && args.dot_part != nullptr) {
+        const int64_t row = tl.seg_start + r0 + lane;
+        if (row < tl.seg_end) args.dot_part[row * ((args.width + BN - 1) / BN) + tl.n] = dot;
       }
       tc_fence_before();
       __syncwarp();

@@ -166,10 +166,13 @@ struct BwdGemmArgs {
   int32_t out_split_m;
   int64_t group_stride;
   int64_t ldo;
-  // SwiGLU-backward epilogue
+  // SwiGLU-backward epilogue: the accumulator is dh_u = W_d^T dy of a row whose
+  // coefficient is row_scale[row] (r or s); dh = row_scale * dh_u
   const float* ab;            // [rows][2 * width] fp32: a | b
   __nv_bfloat16* dab;         // [rows][2 * width] bf16: da | db
-  __nv_bfloat16* hout;        // [rows][width] bf16: SiLU(a) * b
+  __nv_bfloat16* hout;        // [rows][width] bf16: row_scale * SiLU(a) * b
+  const float* row_scale;     // [rows]
+  float* dot_part;            // [rows][ceil(width / 256)]: sum over the tile's columns of dh_u * h
   int32_t width;
   int32_t* status;
 };
@@ -187,7 +190,8 @@ struct BwdRowsParams {
   const float* topk_w;        // [T][K]
   const int32_t* seg_pad;     // [N+1] padded offsets
   __nv_bfloat16* x_pad;       // [rows][d]
-  __nv_bfloat16* gf;          // [rows][d]
+  __nv_bfloat16* gf;          // [rows][d] dy of the row's token (bf16)
+  float* r_pad;               // [rows] the row's coefficient r (0 for padding rows)
   int64_t T;
   int32_t d, N, K;
   int32_t* status;
@@ -195,6 +199,9 @@ struct BwdRowsParams {
 struct BwdCombineParams {
   const float* dxr;           // [rows][d] route rows (padded layout)
   const float* dxs;           // [T][d] shared rows, or nullptr
+  const float* dxz;           // [T][d] dz W_r (gradient through the router), or nullptr
+  const float* du;            // [T] gradient of the shared-gate logit, or nullptr
+  const __nv_bfloat16* gate_w;   // [d] w_s when du is given
   const int32_t* route_pos;   // [T][K]
   const int32_t* topk_idx;    // [T][K]
   const int32_t* offsets;     // [N+1]
@@ -204,10 +211,33 @@ struct BwdCombineParams {
   int32_t d, N, K;
   int32_t* status;
 };
+struct RouterBwdParams {
+  const float* logits;        // [T][N] z (+ logit bias) of the forward call
+  const int32_t* topk_idx;    // [T][K]
+  const int32_t* route_pos;   // [T][K]
+  const int32_t* offsets;     // [N+1]
+  const int32_t* seg_pad;     // [N+1]
+  const float* dot_part;      // [rows][nt] routed dh_u . h per tile
+  int32_t nt;
+  const float* dot_part_s;    // [t_pad][nt_s] shared, when du is wanted
+  int32_t nt_s;
+  const float* shared_coef;   // [T]
+  int64_t T;
+  int32_t N, K, score, norm;
+  float alpha, norm_p;
+  __nv_bfloat16* dz;          // [T][n128]
+  int32_t n128;
+  float* du;                  // [T] or nullptr
+  int32_t* status;
+};
+constexpr int kDwsChunks = 64;
+cudaError_t launch_router_bwd(const RouterBwdParams& p, cudaStream_t s);
+cudaError_t launch_dws(const float* du, const void* x, int64_t T, int d, float* part, float* dws,
+                       cudaStream_t s);
 cudaError_t launch_pad_offsets(const int32_t* counts_keep, int N, int32_t* seg_pad, cudaStream_t s);
 cudaError_t launch_bwd_rows(const BwdRowsParams& p, int64_t rows_cap, cudaStream_t s);
-cudaError_t launch_shared_scale(const float* dy, const float* sc, int64_t T, int d, __nv_bfloat16* gs,
-                                cudaStream_t s);
+cudaError_t launch_shared_scale(const float* dy, const float* sc, int64_t T, int64_t t_pad, int d,
+                                __nv_bfloat16* gs, float* s_pad, cudaStream_t s);
 cudaError_t launch_dx_combine(const BwdCombineParams& p, cudaStream_t s);
 
 // Tile shape choice for the bf16 expert GEMMs: 256-row pair tiles load half the

@@ -112,10 +112,16 @@ class MoELayer:
         rec(5)
         return o["y"]
 
-    def backward(self, x: torch.Tensor, dy: torch.Tensor, stream=None) -> Dict[str, torch.Tensor]:
-        """Gradients (router coefficients fixed) for upstream gradient dy [T][d] fp32, using
-        the routing of the last forward call; returns dx and the weight gradients (fp32)."""
+    def backward(self, x: torch.Tensor, dy: torch.Tensor, stream=None,
+                 router_grad: bool = False) -> Dict[str, torch.Tensor]:
+        """Gradients for upstream gradient dy [T][d] fp32, using the routing of the last
+        forward call (which must have written the logits when ``router_grad``); returns dx
+        and the weight gradients (fp32).  ``router_grad`` adds the gradient through the
+        router coefficients (dW_router, and dshared_gate_w for a learned shared gate)."""
         c = self.cfg
+        if getattr(self, "_bwd_router", None) != router_grad:
+            self.bwd_ws = None
+            self._bwd_router = router_grad
         if getattr(self, "bwd_ws", None) is None:
             n = nat.moe_backward_workspace_size(c)
             self.bwd_ws = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
@@ -129,6 +135,10 @@ class MoELayer:
             if ds > 0:
                 self.grads.update(dWs_gate=torch.empty((ds, d), **f32), dWs_up=torch.empty((ds, d), **f32),
                                   dWs_down=torch.empty((d, ds), **f32))
+            if router_grad:
+                self.grads["dW_router"] = torch.empty((N, d), **f32)
+                if c.shared_mode == nat.SHARED_MODES["gate"]:
+                    self.grads["dshared_gate_w"] = torch.empty((d,), **f32)
             self.grads_c = nat.make_grads(**self.grads)
         nat.moe_layer_backward(c, self.w, x, self.outputs, dy, self.grads_c, self.bwd_ws, stream)
         return self.grads

@@ -41,8 +41,8 @@ def _bf16(a):
 
 
 def _emulated(spec, hin, dy, fwd):
-    """The same backward with the kernels' rounding: gf = bf16(r dy), h, da, db rounded to
-    bf16, everything else float64 (a diagnostic reference for the kernel arithmetic)."""
+    """The same backward with the kernels' rounding: dy, r h, da, db rounded to bf16,
+    everything else float64 (a diagnostic reference for the kernel arithmetic)."""
     x = O.f64(hin["x"])
     T, d = x.shape
     idx = fwd["topk_idx"]
@@ -54,28 +54,29 @@ def _emulated(spec, hin, dy, fwd):
     dWu = np.zeros_like(dWg)
     dWd = np.zeros((N,) + tuple(hin["W_down"].shape[1:]))
 
-    def fam(xr, gfr, Wg, Wu, Wd):
+    def fam(xr, dyr, sc, Wg, Wu, Wd):
+        # the kernels: dh = c (dy_bf16 W_d), dW_d = dy_bf16^T bf16(c h)
         a = xr @ Wg.T
         b = xr @ Wu.T
-        h = _bf16(O.silu(a) * b)
-        dh = gfr @ Wd
+        hf = O.silu(a) * b
+        dh = sc[:, None] * (dyr @ Wd)
         da = _bf16(dh * b * O.dsilu(a))
         db = _bf16(dh * O.silu(a))
-        return da @ Wg + db @ Wu, da.T @ xr, db.T @ xr, gfr.T @ h
+        return da @ Wg + db @ Wu, da.T @ xr, db.T @ xr, dyr.T @ _bf16(sc[:, None] * hf)
 
+    dyb = _bf16(dy)
     for e in range(N):
         toks, slots = np.nonzero((idx == e) & (pos >= 0))
         if len(toks) == 0:
             continue
-        gfr = _bf16(w[toks, slots][:, None] * dy[toks])
-        dxe, g1, g2, g3 = fam(x[toks], gfr, O.f64(hin["W_gate"][e]), O.f64(hin["W_up"][e]),
-                             O.f64(hin["W_down"][e]))
+        dxe, g1, g2, g3 = fam(x[toks], dyb[toks], w[toks, slots], O.f64(hin["W_gate"][e]),
+                              O.f64(hin["W_up"][e]), O.f64(hin["W_down"][e]))
         np.add.at(out["dx"], toks, dxe)
         dWg[e], dWu[e], dWd[e] = g1, g2, g3
     out.update(dW_gate=dWg, dW_up=dWu, dW_down=dWd)
     if spec.d_shared:
-        gs = _bf16(fwd["shared_coef"][:, None] * dy)
-        dxs, g1, g2, g3 = fam(x, gs, O.f64(hin["Ws_gate"]), O.f64(hin["Ws_up"]), O.f64(hin["Ws_down"]))
+        dxs, g1, g2, g3 = fam(x, dyb, fwd["shared_coef"], O.f64(hin["Ws_gate"]), O.f64(hin["Ws_up"]),
+                              O.f64(hin["Ws_down"]))
         out["dx"] += dxs
         out.update(dWs_gate=g1, dWs_up=g2, dWs_down=g3)
     return out
@@ -141,3 +142,36 @@ def test_backward_twice_same_result():
     assert layer.backward_status() == 0
     for k in a:
         assert torch.equal(a[k], b[k]), k
+
+
+ROUTER_SHAPES = {
+    # the selected-weight rules of Table 52 and the learned shared gate (Eq. 77)
+    "olmo_l1": SHAPES["olmo_s"],                                                    # softmax, L1, alpha = K
+    "qwen2_none_gate": SHAPES["qwen2_s"],                                           # softmax, none, sigmoid gate
+    "dsv3_sigmoid_l1": SHAPES["dsv3_s"],                                            # sigmoid, L1, alpha = 2.5
+    "mixtral_selected": SHAPES["mixtral_cap"],                                      # softmax over selected, drops
+    "olmo_lp3": SHAPES["olmo_k1"].replace(K=2, norm="lp", norm_p=3.0, alpha=2.0),   # L_p
+}
+
+
+@pytest.mark.parametrize("name", list(ROUTER_SHAPES))
+def test_backward_through_router(name):
+    spec = ROUTER_SHAPES[name]
+    inp = make_inputs(spec, "cuda")
+    layer = run_layer(spec, inp)
+    assert layer.status() == 0
+    check_routing_exact(layer, spec)
+    g = torch.Generator(device="cpu").manual_seed(11)
+    dy = torch.randn((spec.T, spec.d_model), generator=g).to("cuda")
+    grads = layer.backward(inp["x"], dy, router_grad=True)
+    torch.cuda.synchronize()
+    assert layer.backward_status() == 0
+    hin = host(inp)
+    ref = O.moe_backward(spec, hin, dy.cpu().numpy(), router_grad=True,
+                         logits=layer.out["logits"].cpu().numpy())
+    keys = ["dx", "dW_router", "dW_down"] + (["dshared_gate_w"] if spec.shared_mode == "gate" else [])
+    for k in keys:
+        got = grads[k].cpu().numpy()
+        er, em = _rms_rel(got, ref[k]), _rel(got, ref[k])
+        assert er <= BWD_RMS_TOL and em <= BWD_MAX_TOL, f"{name} {k}: rms {er:.3e} max {em:.3e}"
+
