@@ -324,12 +324,13 @@ def bench_backward(args, spec, layer, x, config, dev):
     """Time moe_layer_backward (router coefficients fixed) on the routing of one forward
     call: CUDA events around each call, a 256 MiB buffer written between calls."""
     import torch
-    layer.forward(x, logits=False)
+    layer.forward(x, logits=True)
+    rg = bool(args.router_grad)
     g = torch.Generator(device="cpu").manual_seed(7)
     dy = torch.randn((spec.T, spec.d_model), generator=g).to(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(max(args.warmup, 3)):
-        layer.backward(x, dy)
+        layer.backward(x, dy, router_grad=rg)
         flush.add_(1)
     torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device())
@@ -341,7 +342,7 @@ def bench_backward(args, spec, layer, x, config, dev):
         flush.add_(1)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        layer.backward(x, dy)
+        layer.backward(x, dy, router_grad=rg)
         b.record()
         evs.append((a, b))
     torch.cuda.synchronize()
@@ -355,7 +356,8 @@ def bench_backward(args, spec, layer, x, config, dev):
     std_flops = 12.0 * d * (dr * kept + ds * spec.T)
     exe_flops = 16.0 * d * (dr * kept + ds * spec.T)
     pk = peaks()
-    line = {"metric": "MoE-layer backward (router coefficients fixed) tokens/s on 1 GB300",
+    line = {"metric": "MoE-layer backward (%s) tokens/s on 1 GB300" % (
+                "including the router gradient" if rg else "router coefficients fixed"),
             "value": spec.T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": spec.dtype,
             "data": "synthetic", "config": dict(config, l2="256 MiB buffer written between calls"),
@@ -386,6 +388,8 @@ def main():
     ap.add_argument("--mode", choices=["forward", "backward"], default="forward",
                     help="backward: time moe_layer_backward (router coefficients fixed) on the "
                          "routing of one forward call, instead of the forward benchmark line")
+    ap.add_argument("--router-grad", action="store_true",
+                    help="with --mode backward: include the gradient through the router coefficients")
     ap.add_argument("--forward-only", type=int, default=0, metavar="R",
                     help="run R untimed layer forwards and exit (a short, fixed launch sequence "
                          "for ncu captures: each forward launches the routed gate/up and down "
