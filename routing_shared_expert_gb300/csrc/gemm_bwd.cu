@@ -385,10 +385,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 args.ab + row * (2 * static_cast<int64_t>(args.width)) + args.width + col);
             __nv_bfloat16* drow = args.dab + row * (2 * static_cast<int64_t>(args.width));
             __nv_bfloat16* hrow = args.hout + row * static_cast<int64_t>(args.width);
+            // all 16 loads of the chunk issued before any store (no aliasing assumed)
+            float4 a4[8], b4[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              a4[i] = __ldg(arow + i);
+              b4[i] = __ldg(brow + i);
+            }
 #pragma unroll
             for (int v8 = 0; v8 < 4; ++v8) {
-              const float4 a0 = arow[2 * v8], a1 = arow[2 * v8 + 1];
-              const float4 b0 = brow[2 * v8], b1 = brow[2 * v8 + 1];
+              const float4 a0 = a4[2 * v8], a1 = a4[2 * v8 + 1];
+              const float4 b0 = b4[2 * v8], b1 = b4[2 * v8 + 1];
               const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
               const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
               uint32_t da2[4], db2[4], h2[4];
