@@ -9,7 +9,7 @@
 // its own shared memory and rows 128-255 from its partner's; B columns 0-127
 // from its own and 128-255 from its partner's.  Each CTA therefore loads only
 // 16 KB of A and 16 KB of B per 64-wide K step (half the bytes per multiply-add
-// of a one-SM 128 x 256 tile), which lets six stages sit in shared memory and
+// of a one-SM 128 x 256 tile), which lets six K blocks sit in shared memory and
 // keeps the tensor pipe fed from L2.  Each CTA's TMEM holds the fp32
 // accumulator rows of its own 128 rows for all 256 columns.
 //   SwiGLU mode: a tile covers 128 h columns.  In a full tile the even CTA loads
@@ -22,7 +22,8 @@
 // The last tile of a segment is a half tile (M = 128: 64 A rows per CTA) when at
 // most 128 of its rows are real.  A cta_group::2 MMA with M = 128 issues at twice
 // the rate of one with M = 256 (each SM computes 64 rows), so a short tail costs
-// half a tile instead of a whole one.  Its accumulator lands in TMEM lanes 0-63 for
+// half a tile instead of a whole one, once the issuer's waits are spread over
+// enough MMAs (the ring stage width below).  Its accumulator lands in TMEM lanes 0-63 for
 // B columns [0,128) and lanes 64-127 for columns [128,256), TMEM columns 0-127,
 // rows 64 r + (lane mod 64) in CTA r.
 // The gate/up A rows are either read from a packed buffer (one TMA tile load) or
@@ -46,10 +47,16 @@ constexpr int BM = 128;                    // rows per CTA
 constexpr int PM = 256;                    // rows per pair tile
 constexpr int HM = 64;                     // rows per CTA of a half tile (M = 128)
 constexpr int BK = 64;
-constexpr int STAGES = 6;
+// The ring holds six K blocks of 64 (32 KB each).  A ring stage is one K block, or two
+// (three stages of 64 KB) when the launch asks for it: the MMA issuer then waits once
+// per 8 MMAs instead of once per 4, which matters when an MMA group is short (a half
+// tile's 4 MMAs take 256 cycles, less than one wait-to-issue round trip of the issuer),
+// while the finer ring keeps more bytes in flight for weight-streaming launches.
+constexpr int RING_BLOCKS = 6;
 constexpr int A_BYTES = BM * BK * 2;       // 16 KB
 constexpr int B_BYTES = 128 * BK * 2;      // 16 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SUB_BYTES = A_BYTES + B_BYTES;
+constexpr int RING_BYTES = RING_BLOCKS * SUB_BYTES;
 constexpr int EPI_LD = 36;                 // 32-bit words per staged row (16-byte aligned)
 constexpr int EPI_WARP_WORDS = 32 * EPI_LD;
 constexpr int EPI_BYTES = 4 * EPI_WARP_WORDS * 4;
@@ -127,7 +134,7 @@ __device__ __forceinline__ void load_b(uint32_t sB, bool half, bool leader, cons
   }
 }
 
-template <int MODE, bool GATHER>
+template <int MODE, bool GATHER, int KSUB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_pair_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA64,
                  const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
@@ -137,10 +144,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint32_t* epi = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
+  uint32_t* epi = reinterpret_cast<uint32_t*>(smem + RING_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES + EPI_BYTES);
+  uint64_t* empty = full + RING_BLOCKS;
+  uint64_t* tfull = empty + RING_BLOCKS;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -156,11 +163,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   constexpr int BN_OUT = SWIGLU ? 128 : 256;
   const int n_tiles = (args.n_out + BN_OUT - 1) / BN_OUT;
   const int k_blocks = (args.k_dim + BK - 1) / BK;
+  constexpr int ksub = KSUB;
+  constexpr int stages = RING_BLOCKS / KSUB;
+  constexpr int stage_bytes = KSUB * SUB_BYTES;
   const uint32_t smem_base = smem_u32(smem);
   const int64_t pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < RING_BLOCKS; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
@@ -227,9 +237,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ producer (both CTAs)
     int stage = 0;
     uint32_t phase = 0;
-    int issued_parity[STAGES];
+    int issued_parity[RING_BLOCKS];
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+    for (int s = 0; s < RING_BLOCKS; ++s) issued_parity[s] = -1;
     bool ok = true;
     Tile tl;
     if constexpr (!GATHER) {
@@ -240,7 +250,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const CUtensorMap* mapA = tl.half ? &tmA64 : &tmA;
           const uint32_t tx = 2u * ((tl.half ? A_BYTES / 2 : A_BYTES) + B_BYTES);
           const int b_row = b_first_row<SWIGLU>(args, tl, rank);
-          for (int kb = 0; kb < k_blocks; ++kb) {
+          for (int kb0 = 0; kb0 < k_blocks; kb0 += ksub) {
             if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
                                    kWaitLimitNs)) {
               ok = false;
@@ -248,13 +258,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             }
             const uint32_t fb_local = smem_u32(&full[stage]);
             const uint32_t fb_leader = mapa_shared(fb_local, 0);
-            if (leader) mbar_arrive_expect_tx(fb_local, tx);
-            const uint32_t sA = smem_base + stage * STAGE_BYTES;
-            tma_load_2d_pair(sA, mapA, kb * BK, a_row, fb_leader);
-            load_b<SWIGLU>(sA + A_BYTES, tl.half, leader, &tmB0, &tmB1, &tmB0h, &tmB1h, kb * BK, b_row,
-                           fb_leader);
+            const int nv = ksub == 1 ? 1 : min(ksub, k_blocks - kb0);
+            if (leader) mbar_arrive_expect_tx(fb_local, tx * static_cast<uint32_t>(nv));
+#pragma unroll
+            for (int u = 0; u < nv; ++u) {
+              const int kb = kb0 + u;
+              const uint32_t sA = smem_base + stage * stage_bytes + u * SUB_BYTES;
+              tma_load_2d_pair(sA, mapA, kb * BK, a_row, fb_leader);
+              load_b<SWIGLU>(sA + A_BYTES, tl.half, leader, &tmB0, &tmB1, &tmB0h, &tmB1h, kb * BK,
+                             b_row, fb_leader);
+            }
             issued_parity[stage] = static_cast<int>(phase);
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            if (++stage == stages) { stage = 0; phase ^= 1u; }
           }
         }
       }
@@ -269,7 +284,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         int32_t src[4];
         gather_rows4(args.gather_src, args.gather_cap, a_row + 4 * lane, tl.seg_start, tl.seg_end,
                      args.src_rows, args.status, src);
-        for (int kb = 0; kb < k_blocks; ++kb) {
+        for (int kb0 = 0; kb0 < k_blocks; kb0 += ksub) {
           bool go = true;
           if (lane == 0)
             go = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
@@ -281,21 +296,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           const uint32_t fb_local = smem_u32(&full[stage]);
           const uint32_t fb_leader = mapa_shared(fb_local, 0);
-          const uint32_t sA = smem_base + stage * STAGE_BYTES;
+          const int nv = ksub == 1 ? 1 : min(ksub, k_blocks - kb0);
           if (lane == 0) {
-            if (leader) mbar_arrive_expect_tx(fb_local, tx);
-            load_b<SWIGLU>(sA + A_BYTES, tl.half, leader, &tmB0, &tmB1, &tmB0h, &tmB1h, kb * BK, b_row,
-                           fb_leader);
+            if (leader) mbar_arrive_expect_tx(fb_local, tx * static_cast<uint32_t>(nv));
             issued_parity[stage] = static_cast<int>(phase);
           }
-          if (gathers) tma_gather4_pair(sA + lane * 512, &tmA, kb * BK, src, fb_leader);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+#pragma unroll
+          for (int u = 0; u < nv; ++u) {
+            const int kb = kb0 + u;
+            const uint32_t sA = smem_base + stage * stage_bytes + u * SUB_BYTES;
+            if (lane == 0)
+              load_b<SWIGLU>(sA + A_BYTES, tl.half, leader, &tmB0, &tmB1, &tmB0h, &tmB1h, kb * BK,
+                             b_row, fb_leader);
+            if (gathers) tma_gather4_pair(sA + lane * 512, &tmA, kb * BK, src, fb_leader);
+          }
+          if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
       }
     }
     if (!ok && leader && lane == 0) {
       // The even CTA's full barriers count both CTAs' copies: wait for them to land.
-      for (int s = 0; s < STAGES; ++s)
+      for (int s = 0; s < stages; ++s)
         if (issued_parity[s] >= 0)
           mbar_wait_bounded(smem_u32(&full[s]), static_cast<uint32_t>(issued_parity[s]), never,
                             nullptr, kDrainLimitNs);
@@ -322,22 +343,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d_acc = tmem_base + static_cast<uint32_t>(buf * 256);
         const uint32_t idesc = tl.half ? idesc_half : idesc_full;
-        for (int kb = 0; kb < k_blocks; ++kb) {
+        for (int kb0 = 0; kb0 < k_blocks; kb0 += ksub) {
           if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, args.status,
                                  kWaitLimitNs)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sA = smem_base + stage * STAGE_BYTES;
-          const uint64_t a_desc = sw128_kmajor_desc(sA);
-          const uint64_t b_desc = sw128_kmajor_desc(sA + A_BYTES);
+          const int nv = ksub == 1 ? 1 : min(ksub, k_blocks - kb0);
 #pragma unroll
-          for (int j = 0; j < BK / 16; ++j)
-            tc_mma_bf16_pair(d_acc, a_desc + 2 * j, b_desc + 2 * j, idesc,
-                             (kb > 0 || j > 0) ? 1u : 0u);
+          for (int u = 0; u < nv; ++u) {
+            const uint32_t sA = smem_base + stage * stage_bytes + u * SUB_BYTES;
+            const uint64_t a_desc = sw128_kmajor_desc(sA);
+            const uint64_t b_desc = sw128_kmajor_desc(sA + A_BYTES);
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j)
+              tc_mma_bf16_pair(d_acc, a_desc + 2 * j, b_desc + 2 * j, idesc,
+                               (kb0 + u > 0 || j > 0) ? 1u : 0u);
+          }
           tc_commit_pair(smem_u32(&empty[stage]), 0x3);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         tc_commit_pair(smem_u32(&tfull[buf]), 0x3);
@@ -449,17 +474,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 size_t pair_smem_bytes(int groups) {
-  return 1024 + STAGES * STAGE_BYTES + EPI_BYTES + 8 * (2 * STAGES + 5) + 16 +
+  return 1024 + RING_BYTES + EPI_BYTES + 8 * (2 * RING_BLOCKS + 5) + 16 +
          8 * (static_cast<size_t>(groups) + 1) + 64;
 }
 
-template <int MODE, bool GATHER>
+template <int MODE, bool GATHER, int KSUB>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a64, const CUtensorMap& b0,
                         const CUtensorMap& b1, const CUtensorMap& b0h, const CUtensorMap& b1h,
                         const PairArgs& args, int64_t max_pair_tiles, cudaStream_t s) {
   if (max_pair_tiles <= 0) return cudaSuccess;
   const size_t smem = pair_smem_bytes(args.offsets ? args.groups : 1);
-  auto kern = tc_pair_gemm<MODE, GATHER>;
+  auto kern = tc_pair_gemm<MODE, GATHER, KSUB>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int64_t pairs_max = device_sm_count() >= 2 ? device_sm_count() / 2 : 1;
@@ -502,6 +527,10 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.gather_src = p.gather_src;
   a.gather_cap = rows_cap;
   a.src_rows = p.src_rows;
+  // Two K blocks per ring stage when the average group has at least 512 rows (each
+  // weight byte feeds enough rows for the tensor pipe to bound the launch); one
+  // otherwise, and for gathered A rows.
+  const bool wide = !gather && (dense ? p.dense_rows : rows_cap / (p.groups > 0 ? p.groups : 1)) >= 512;
 
   a.k_dim = p.d;
   a.n_out = p.width;
@@ -509,8 +538,10 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.out = p.h;
   a.ldo = p.width;
   const int64_t gu_tiles = mt_ub * ((p.width + 127) / 128);
-  cudaError_t e = gather ? launch_pair<kSwiGLU, true>(mA, mA64, mG, mU, mG64, mU64, a, gu_tiles, s)
-                         : launch_pair<kSwiGLU, false>(mA, mA64, mG, mU, mG64, mU64, a, gu_tiles, s);
+  cudaError_t e =
+      gather ? launch_pair<kSwiGLU, true, 1>(mA, mA64, mG, mU, mG64, mU64, a, gu_tiles, s)
+      : wide ? launch_pair<kSwiGLU, false, 2>(mA, mA64, mG, mU, mG64, mU64, a, gu_tiles, s)
+             : launch_pair<kSwiGLU, false, 1>(mA, mA64, mG, mU, mG64, mU64, a, gu_tiles, s);
   if (e != cudaSuccess) return e;
 
   a.k_dim = p.width;
@@ -519,7 +550,9 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.out = p.out;
   a.ldo = p.d;
   a.gather_src = nullptr;    // h is packed
-  return launch_pair<kPlain, false>(mH, mH64, mD, mD, mD, mD, a, mt_ub * ((p.d + 255) / 256), s);
+  const int64_t d_tiles = mt_ub * ((p.d + 255) / 256);
+  return wide ? launch_pair<kPlain, false, 2>(mH, mH64, mD, mD, mD, mD, a, d_tiles, s)
+              : launch_pair<kPlain, false, 1>(mH, mH64, mD, mD, mD, mD, a, d_tiles, s);
 }
 
 }  // namespace moe
