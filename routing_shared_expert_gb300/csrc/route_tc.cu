@@ -204,23 +204,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int i = 0; i < 32; ++i) {
           if (c0 + i >= p.N) break;
           zmax = fmaxf(zmax, z[i]);
-          float cv = sel ? z[i] + s_sel[c0 + i] : z[i];
-          float cz = z[i];
-          int ci = c0 + i;
+          const float cv = sel ? z[i] + s_sel[c0 + i] : z[i];
+          const float cz = z[i];
+          const int ci = c0 + i;
           if (bi[kMaxTopK - 1] == EMPTY || cv > bv[kMaxTopK - 1]) {
+            // The kept keys are a descending prefix of the list; the new key goes behind
+            // every kept key it does not exceed (an equal later expert never displaces an
+            // earlier one).  Its place is a count and the shift is per slot, so one
+            // insertion is a few dependent steps rather than a chain along the list.
+            int pos = 0;
 #pragma unroll
-            for (int j = 0; j < kMaxTopK; ++j) {
-              const bool take = bi[j] == EMPTY || cv > bv[j];
-              const float tv = take ? bv[j] : cv;
-              const float tz = take ? bz[j] : cz;
-              const int ti = take ? bi[j] : ci;
-              bv[j] = take ? cv : bv[j];
-              bz[j] = take ? cz : bz[j];
-              bi[j] = take ? ci : bi[j];
-              cv = tv;
-              cz = tz;
-              ci = ti;
+            for (int j = 0; j < kMaxTopK; ++j) pos += (bi[j] != EMPTY && !(cv > bv[j])) ? 1 : 0;
+#pragma unroll
+            for (int j = kMaxTopK - 1; j > 0; --j) {
+              const bool shift = j > pos, here = j == pos;
+              bv[j] = shift ? bv[j - 1] : (here ? cv : bv[j]);
+              bz[j] = shift ? bz[j - 1] : (here ? cz : bz[j]);
+              bi[j] = shift ? bi[j - 1] : (here ? ci : bi[j]);
             }
+            if (pos == 0) { bv[0] = cv; bz[0] = cz; bi[0] = ci; }
           }
         }
       }
