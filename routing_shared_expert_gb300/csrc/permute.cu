@@ -72,29 +72,64 @@ __global__ void __launch_bounds__(1024) scan_kernel(PermuteParams p) {
   }
   __syncthreads();
 
-  // 2. capacity, offsets, destination totals: sequential over experts, in ascending
-  //    expert index (the local-expert-major admission order of the rank-wide rule).
-  if (threadIdx.x == 0) {
-    for (int q = 0; q < p.num_ranks; ++q) { rreq[q] = 0; rkeep[q] = 0; }
-    int total_drop = 0;
-    offs[0] = 0;
-    tprefix[0] = 0;
-    for (int e = 0; e < p.N; ++e) {
-      const int q = p.rho[e];
-      int keep = creq[e];
-      if (p.cap_policy == MOE_CAP_PER_EXPERT) {
-        keep = min(keep, p.cap);
-      } else if (p.cap_policy == MOE_CAP_RANK_WIDE) {
-        keep = min(keep, p.cap - rkeep[q]);
+  // 2. kept counts and destination totals.  The per-expert and unlimited rules decide
+  //    each expert alone.  The rank-wide budget is shared by a rank's experts in
+  //    ascending expert index (the local-expert-major admission order of the rank-wide
+  //    rule): one thread per rank walks its experts in that order.
+  if (p.cap_policy == MOE_CAP_RANK_WIDE) {
+    for (int q = threadIdx.x; q < p.num_ranks; q += blockDim.x) {
+      int used = 0, req = 0;
+      for (int e = 0; e < p.N; ++e) {
+        if (p.rho[e] != q) continue;
+        const int keep = min(creq[e], p.cap - used);
+        ckeep[e] = keep;
+        used += keep;
+        req += creq[e];
       }
-      ckeep[e] = keep;
-      rreq[q] += creq[e];
-      rkeep[q] += keep;
-      total_drop += creq[e] - keep;
-      offs[e + 1] = offs[e] + keep;
-      tprefix[e + 1] = tprefix[e] + (keep + kTcRows - 1) / kTcRows;
+      rreq[q] = req;
+      rkeep[q] = used;
     }
-    dropped = total_drop;
+  } else {
+    for (int q = threadIdx.x; q < p.num_ranks; q += blockDim.x) { rreq[q] = 0; rkeep[q] = 0; }
+    __syncthreads();
+    for (int e = threadIdx.x; e < p.N; e += blockDim.x) {
+      const int keep = p.cap_policy == MOE_CAP_PER_EXPERT ? min(creq[e], p.cap) : creq[e];
+      ckeep[e] = keep;
+      atomicAdd(&rreq[p.rho[e]], creq[e]);
+      atomicAdd(&rkeep[p.rho[e]], keep);
+    }
+  }
+  __syncthreads();
+  // 3. offsets (Eq. 26), the prefix of 128-row tiles, and the dropped-route total: one
+  //    warp scans the experts 32 at a time.
+  if (warp == 0) {
+    int run_o = 0, run_t = 0, drop = 0;
+    for (int base = 0; base < p.N; base += 32) {
+      const int e = base + lane;
+      const int k = e < p.N ? ckeep[e] : 0;
+      const int nt = (k + kTcRows - 1) / kTcRows;
+      if (e < p.N) drop += creq[e] - k;
+      int io = k, it = nt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o1 = __shfl_up_sync(0xffffffffu, io, off);
+        const int o2 = __shfl_up_sync(0xffffffffu, it, off);
+        if (lane >= off) { io += o1; it += o2; }
+      }
+      if (e < p.N) {
+        offs[e + 1] = run_o + io;
+        tprefix[e + 1] = run_t + it;
+      }
+      run_o += __shfl_sync(0xffffffffu, io, 31);
+      run_t += __shfl_sync(0xffffffffu, it, 31);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) drop += __shfl_xor_sync(0xffffffffu, drop, off);
+    if (lane == 0) {
+      offs[0] = 0;
+      tprefix[0] = 0;
+      dropped = drop;
+    }
   }
   __syncthreads();
 
