@@ -31,7 +31,7 @@ NOMINAL_HBM_GBS = 8000.0
 # moe_grouped_swiglu call), dram__bytes_read.sum + dram__bytes_write.sum summed over the
 # two launches, from one `ncu --set full` capture per workload (profiles/grouped_gemm_olmo.md).
 # It is reported only while the kernel sources hash to the value they had at capture time.
-STAGE_TRAFFIC = {"olmo": {"sources_sha256": "69cf054998199f9a", "bytes": 2057626784}}
+STAGE_TRAFFIC = {"olmo": {"sources_sha256": "c49fcc06ab0ca398", "bytes": 2057998712}}
 TRAFFIC_SOURCES = ("routing_shared_expert_gb300/csrc/gemm_tc2.cu", "routing_shared_expert_gb300/csrc/common.cuh")
 
 
