@@ -342,6 +342,15 @@ moe_status moe_layer_backward(const moe_config* cfg, const moe_weights* w, const
  * after allocating a workspace, before its first use.  Asynchronous on the stream. */
 moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Self-check of the device-side wait bound (no counterpart on the pages): one CTA waits on a
+ * barrier that nothing arrives on, bounded by limit_ns (1 ns .. 2 s) of %globaltimer, the same
+ * bounded wait every tensor-core kernel uses.  The wait runs out, MOE_ERR_TIMEOUT lands in the
+ * workspace status word and the CTA exits; the context stays usable.  Asynchronous on the stream;
+ * read the result with moe_read_status().  Errors: MOE_ERR_INVALID_ARG (NULL or < 256-byte
+ * workspace, limit out of range), MOE_ERR_MISALIGNED, MOE_ERR_CUDA (launch failure). */
+moe_status moe_check_wait_bound(void* workspace, size_t workspace_bytes, int64_t limit_ns,
+                                cudaStream_t stream);
+
 /* Read and clear the device status word of a workspace.  Synchronises the stream and copies
  * 4 bytes to the host.  *code (host) receives MOE_OK or the first device-detected error. */
 moe_status moe_read_status(void* workspace, int32_t* code, cudaStream_t stream);

@@ -88,6 +88,7 @@ def _load():
         "moe_merge_shared": ([c_int32, c_int32, c_int32, POINTER(c_int32), POINTER(c_void_p),
                               POINTER(c_void_p), POINTER(c_void_p), P, P, P, P], c_int32),
         "moe_read_status": ([P, POINTER(c_int32), P], c_int32),
+        "moe_check_wait_bound": ([P, c_size_t, c_int64, P], c_int32),
         "moe_backward_workspace_size": ([C, POINTER(c_size_t)], c_int32),
         "moe_layer_backward": ([C, POINTER(moe_weights), P, POINTER(moe_outputs), P, POINTER(moe_grads),
                                 P, c_size_t, P], c_int32),
@@ -307,6 +308,13 @@ def moe_read_status(workspace, stream=None) -> int:
     code = c_int32(0)
     _check("moe_read_status", _lib.moe_read_status(_ptr(workspace), ctypes.byref(code), _stream(stream)))
     return int(code.value)
+
+
+def moe_check_wait_bound(workspace, limit_ns: int, stream=None):
+    """Self-check of the device wait bound (see the C header): leaves MOE_ERR_TIMEOUT in the
+    workspace status word once a barrier wait of limit_ns runs out."""
+    _check("moe_check_wait_bound", _lib.moe_check_wait_bound(_ptr(workspace), workspace.numel(),
+                                                               int(limit_ns), _stream(stream)))
 
 
 def moe_backward_workspace_size(cfg: moe_config) -> int:

@@ -875,6 +875,17 @@ moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, cudaStrea
   return cudaMemsetAsync(workspace, 0, 256, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+moe_status moe_check_wait_bound(void* workspace, size_t workspace_bytes, int64_t limit_ns,
+                                cudaStream_t stream) {
+  if (!workspace || workspace_bytes < 256 || limit_ns <= 0 || limit_ns > 2000000000LL)
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_MISALIGNED;
+  return launch_wait_bound_check(static_cast<int32_t*>(workspace), static_cast<uint64_t>(limit_ns),
+                                 stream) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
 moe_status moe_read_status(void* workspace, int32_t* code, cudaStream_t stream) {
   if (!workspace || !code) return MOE_ERR_INVALID_ARG;
   int32_t host = 0;

@@ -257,4 +257,7 @@ cudaError_t launch_balance_stats(const moe_config& c, const float* logits, float
 cudaError_t launch_bias_update(int32_t N, const int32_t* counts, float gamma, float* bias,
                                cudaStream_t s);
 
+// One CTA waits, bounded by limit_ns, on a barrier nothing arrives on (csrc/selfcheck.cu).
+cudaError_t launch_wait_bound_check(int32_t* status, uint64_t limit_ns, cudaStream_t s);
+
 }  // namespace moe

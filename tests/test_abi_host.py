@@ -162,3 +162,12 @@ def test_status_strings(nat):
     for code in range(-7, 1):
         assert lib.moe_status_string(code)
     assert nat.version().startswith("moe_gb300")
+
+
+def test_wait_bound_check_rejects_before_cuda(nat):
+    lib = nat.library()
+    assert lib.moe_check_wait_bound(None, 1 << 20, 1000000, None) == -1          # no workspace
+    assert lib.moe_check_wait_bound(ctypes.c_void_p(0x100000), 16, 1000000, None) == -1   # too small
+    assert lib.moe_check_wait_bound(ctypes.c_void_p(0x100000), 1 << 20, 0, None) == -1    # no limit
+    assert lib.moe_check_wait_bound(ctypes.c_void_p(0x100000), 1 << 20, 3000000000, None) == -1
+    assert lib.moe_check_wait_bound(ctypes.c_void_p(0x100001), 1 << 20, 1000000, None) == -7  # misaligned
