@@ -44,6 +44,9 @@ SMALL = {
     "pair_s": C["olmo"].replace(T=1100, d_model=448, N=4, K=2, alpha=2.0, d_expert=320,
                                 d_shared=192),
     "pair_cap_s": C["mixtral"].replace(T=1600, d_model=4096, d_expert=448, capacity_factor=1.0),
+    # pair tiles over segments of at most two 256-row tiles (~256 rows per expert): the
+    # expert GEMMs run a segment's second row tile on the same pair right after its first
+    "pair_short_s": C["dsv3"].replace(T=2048, d_model=512, N=64, d_expert=256, d_shared=128),
     # L_p normalisation of the selected weights (Table 52, MegaBlocks row) on both routers:
     # the tensor-core bf16 router (softmax, p = 2; sigmoid, p = 8) and the fp32 one (p = 3)
     "olmo_lp2": C["olmo"].replace(T=500, d_model=256, d_expert=128, d_shared=128, norm="lp",
@@ -89,7 +92,7 @@ def test_staged_entry_points_equal_fused(name):
         assert torch.equal(a.out[k], b.out[k]), k
 
 
-@pytest.mark.parametrize("name", ["olmo_s", "pair_s", "tiny", "mixtral_tightcap"])
+@pytest.mark.parametrize("name", ["olmo_s", "pair_s", "pair_short_s", "tiny", "mixtral_tightcap"])
 def test_gathered_rows_equal_packed_rows(name):
     """The expert GEMM reading rows of x through perm_src gives exactly what it gives on the
     explicitly permuted copy x_perm (both tile shapes, and the fp32 path)."""
