@@ -445,7 +445,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             *reinterpret_cast<uint4*>(stg + lane * EPI_LD + 4 * v) =
                 make_uint4(ar[4 * v], ar[4 * v + 1], ar[4 * v + 2], ar[4 * v + 3]);
           __syncwarp();
-          // eight lanes per row (16 bytes each), four rows per pass
+          // eight lanes per row (16 bytes each), four rows per pass; streaming stores: f is
+          // read once more, by the combine, long after this tile
 #pragma unroll
           for (int pass = 0; pass < 8; ++pass) {
             const int r = pass * 4 + lane / 8;
@@ -453,7 +454,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const int col = col_base + c * 32 + (lane % 8) * 4;
             const uint4 val = *reinterpret_cast<const uint4*>(stg + r * EPI_LD + (lane % 8) * 4);
             if (row < row_end && col + 4 <= args.n_out)
-              *reinterpret_cast<uint4*>(out + row * args.ldo + col) = val;
+              __stcs(reinterpret_cast<uint4*>(out + row * args.ldo + col), val);
           }
           __syncwarp();
         }
