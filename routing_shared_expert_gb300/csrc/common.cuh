@@ -268,6 +268,27 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const CUtens
       : "memory");
 }
 
+// Bulk tensor store of one 2-D box from shared memory (tracked by bulk async-groups of the
+// issuing thread), and the group operations around it.  Writes to the box by other threads
+// are made visible to the store by fence_proxy_async_smem() in each writer first.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t c0, int32_t c1,
+                                             uint32_t smem_src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(smem_src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of every committed store have been read
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// every committed store has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Four-row gather (see tma_gather4) completing on an mbarrier of either CTA of the pair.
 __device__ __forceinline__ void tma_gather4_pair(uint32_t smem_dst, const CUtensorMap* map, int32_t c0,
                                                  const int32_t (&r)[4], uint32_t bar) {

@@ -139,7 +139,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_pair_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA64,
                  const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                  const __grid_constant__ CUtensorMap tmB0h, const __grid_constant__ CUtensorMap tmB1h,
-                 const PairArgs args) {
+                 const __grid_constant__ CUtensorMap tmOut, const PairArgs args) {
   constexpr bool SWIGLU = MODE == kSwiGLU;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -433,36 +433,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           __syncwarp();
         }
       } else {
+        // One 32 x 32 fp32 block per chunk, staged in the 128-byte swizzled layout of the
+        // output map (16-byte piece v of row r at piece v ^ (r mod 8): conflict-free) and
+        // written by one TMA store when it lies inside the segment and the width; blocks
+        // crossing the segment's end (the next rows belong to another segment) or the width
+        // are written by the lanes.
         float* out = static_cast<float*>(args.out);
         const int chunks = tl.half ? 4 : 8;
         const int col_base = tl.n * 256 + (tl.half ? hq * 128 : 0);
+        uint8_t* blk = reinterpret_cast<uint8_t*>(epi) + (warp - 2) * 4096;
+        const bool rows_in = row0 + 32 <= row_end;
 #pragma unroll 1
         for (int c = 0; c < chunks; ++c) {
           uint32_t ar[32];
           tmem_ld32(taddr + c * 32, ar);
+          const int col0 = col_base + c * 32;
+          if (lane == 0) bulk_wait_read_all();   // the previous block has been read out
+          __syncwarp();
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            *reinterpret_cast<uint4*>(stg + lane * EPI_LD + 4 * v) =
+            *reinterpret_cast<uint4*>(blk + lane * 128 + ((v ^ (lane & 7)) * 16)) =
                 make_uint4(ar[4 * v], ar[4 * v + 1], ar[4 * v + 2], ar[4 * v + 3]);
-          __syncwarp();
-          // eight lanes per row (16 bytes each), four rows per pass; streaming stores: f is
-          // read once more, by the combine, long after this tile
+          if (rows_in && col0 + 32 <= args.n_out) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmOut, col0, static_cast<int32_t>(row0), smem_u32(blk));
+              bulk_commit();
+            }
+          } else {
+            __syncwarp();
+            // eight lanes per row (16 bytes each), four rows per pass
 #pragma unroll
-          for (int pass = 0; pass < 8; ++pass) {
-            const int r = pass * 4 + lane / 8;
-            const int64_t row = row0 + r;
-            const int col = col_base + c * 32 + (lane % 8) * 4;
-            const uint4 val = *reinterpret_cast<const uint4*>(stg + r * EPI_LD + (lane % 8) * 4);
-            if (row < row_end && col + 4 <= args.n_out)
-              __stcs(reinterpret_cast<uint4*>(out + row * args.ldo + col), val);
+            for (int pass = 0; pass < 8; ++pass) {
+              const int r = pass * 4 + lane / 8;
+              const int64_t row = row0 + r;
+              const int col = col0 + (lane % 8) * 4;
+              const uint4 val =
+                  *reinterpret_cast<const uint4*>(blk + r * 128 + (((lane % 8) ^ (r & 7)) * 16));
+              if (row < row_end && col + 4 <= args.n_out)
+                __stcs(reinterpret_cast<uint4*>(out + row * args.ldo + col), val);
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
     }
+    if (!SWIGLU && lane == 0) bulk_wait_all();   // the output blocks are written
   }
 
   __syncwarp();
@@ -482,7 +502,8 @@ size_t pair_smem_bytes(int groups) {
 template <int MODE, bool GATHER, int KSUB>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a64, const CUtensorMap& b0,
                         const CUtensorMap& b1, const CUtensorMap& b0h, const CUtensorMap& b1h,
-                        const PairArgs& args, int64_t max_pair_tiles, cudaStream_t s) {
+                        const CUtensorMap& out, const PairArgs& args, int64_t max_pair_tiles,
+                        cudaStream_t s) {
   if (max_pair_tiles <= 0) return cudaSuccess;
   const size_t smem = pair_smem_bytes(args.offsets ? args.groups : 1);
   auto kern = tc_pair_gemm<MODE, GATHER, KSUB>;
@@ -490,7 +511,7 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a64, const CUte
   if (e != cudaSuccess) return e;
   const int64_t pairs_max = device_sm_count() >= 2 ? device_sm_count() / 2 : 1;
   const int64_t pairs = max_pair_tiles < pairs_max ? max_pair_tiles : pairs_max;
-  kern<<<static_cast<unsigned>(2 * pairs), THREADS, smem, s>>>(a, a64, b0, b1, b0h, b1h, args);
+  kern<<<static_cast<unsigned>(2 * pairs), THREADS, smem, s>>>(a, a64, b0, b1, b0h, b1h, out, args);
   return cudaGetLastError();
 }
 
@@ -540,9 +561,9 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.ldo = p.width;
   const int64_t gu_tiles = mt_ub * ((p.width + 127) / 128);
   cudaError_t e =
-      gather ? launch_pair<kSwiGLU, true, 1>(mA, mA64, mG, mU, mG64, mU64, a, gu_tiles, s)
-      : wide ? launch_pair<kSwiGLU, false, 2>(mA, mA64, mG, mU, mG64, mU64, a, gu_tiles, s)
-             : launch_pair<kSwiGLU, false, 1>(mA, mA64, mG, mU, mG64, mU64, a, gu_tiles, s);
+      gather ? launch_pair<kSwiGLU, true, 1>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s)
+      : wide ? launch_pair<kSwiGLU, false, 2>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s)
+             : launch_pair<kSwiGLU, false, 1>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s);
   if (e != cudaSuccess) return e;
 
   a.k_dim = p.width;
@@ -552,8 +573,10 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.ldo = p.d;
   a.gather_src = nullptr;    // h is packed
   const int64_t d_tiles = mt_ub * ((p.d + 255) / 256);
-  return wide ? launch_pair<kPlain, false, 2>(mH, mH64, mD, mD, mD, mD, a, d_tiles, s)
-              : launch_pair<kPlain, false, 1>(mH, mH64, mD, mD, mD, mD, a, d_tiles, s);
+  CUtensorMap mF;
+  if (!make_f32_map(&mF, p.out, p.d, rows_cap)) return cudaErrorInvalidValue;
+  return wide ? launch_pair<kPlain, false, 2>(mH, mH64, mD, mD, mD, mD, mF, a, d_tiles, s)
+              : launch_pair<kPlain, false, 1>(mH, mH64, mD, mD, mD, mD, mF, a, d_tiles, s);
 }
 
 }  // namespace moe
