@@ -46,9 +46,7 @@ constexpr int STAGES = 6;
 constexpr int A_BYTES = BMC * BK * 2;
 constexpr int B_BYTES = BNC * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int EPI_LD = 36;                // 32-bit words per staged row (16-byte aligned)
-constexpr int EPI_WARP_WORDS = 32 * EPI_LD;
-constexpr int EPI_BYTES = 4 * EPI_WARP_WORDS * 4;
+constexpr int EPI_BYTES = 4 * 4096;        // one 32 x 32 fp32 staging block per epilogue warp
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -104,7 +102,8 @@ __device__ __forceinline__ bool bwd_tile(const BwdGemmArgs& a, bool k_seg, const
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_bwd_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                const __grid_constant__ CUtensorMap tmB1, const BwdGemmArgs args) {
+                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO,
+                const __grid_constant__ CUtensorMap tmO2, const BwdGemmArgs args) {
   // A_MN: K runs over the segment rows (weight gradients); otherwise the rows are M.
   constexpr bool K_SEG = A_MN;
   extern __shared__ uint8_t smem_raw[];
@@ -311,7 +310,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
-    uint32_t* stg = epi + (warp - 2) * EPI_WARP_WORDS;
     BwdTile tl;
     int64_t local = 0;
     for (int64_t t = pair_id; bwd_tile(args, K_SEG, s_off, s_tp, n_tiles, t, tl);
@@ -333,20 +331,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       float* obase = args.out;
       int64_t orow0 = 0;
       int64_t rows_left = 0;
+      int64_t map_row = 0;        // first row of the warp's block in the store map
+      bool second = false;        // the block goes to out2
       if (EPI == kBwdEpiF32) {
         if (K_SEG) {
+          // groups of rpg rows, group_stride apart (one group: m_dim rows)
+          const int64_t rpg = args.group_stride > 0 ? args.group_stride / args.ldo : args.m_dim;
           orow0 = r0;
           obase = args.out + static_cast<int64_t>(tl.g) * args.group_stride;
           if (args.out_split_m > 0 && r0 >= args.out_split_m) {
             obase = args.out2 + static_cast<int64_t>(tl.g) * args.group_stride;
             orow0 = r0 - args.out_split_m;
+            second = true;
           }
           rows_left = args.m_dim - r0;
+          map_row = static_cast<int64_t>(tl.g) * rpg + orow0;
         } else {
           orow0 = tl.seg_start + r0;
           rows_left = tl.seg_end - orow0;
+          map_row = orow0;
         }
       }
+      uint8_t* blk = reinterpret_cast<uint8_t*>(epi) + (warp - 2) * 4096;   // fp32 block staging
       float dot = 0.f;   // SwiGLU epilogue: this row's sum of dh_u * h over the tile's columns
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -360,20 +366,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           tmem_ld32(taddr + c * 32, v);
         }
         if (EPI == kBwdEpiF32) {
+          // The 32 x 32 block, staged in the 128-byte swizzled layout of the store maps
+          // (16-byte piece j of row r at piece j ^ (r mod 8)), goes out by one TMA store when
+          // all its rows and columns are inside; else the lanes write the rows that are.
+          if (lane == 0) bulk_wait_read_all();   // the previous block has been read out
+          __syncwarp();
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4)
-            *reinterpret_cast<uint4*>(stg + lane * EPI_LD + 4 * v4) =
+            *reinterpret_cast<uint4*>(blk + lane * 128 + ((v4 ^ (lane & 7)) * 16)) =
                 make_uint4(v[4 * v4], v[4 * v4 + 1], v[4 * v4 + 2], v[4 * v4 + 3]);
-          __syncwarp();
-          // eight lanes per row (16 bytes each), four rows per pass
+          if (rows_left >= 32 && col + 32 <= args.n_dim) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(second ? &tmO2 : &tmO, col, static_cast<int32_t>(map_row), smem_u32(blk));
+              bulk_commit();
+            }
+          } else {
+            __syncwarp();
+            // eight lanes per row (16 bytes each), four rows per pass
 #pragma unroll
-          for (int pass = 0; pass < 8; ++pass) {
-            const int rr = pass * 4 + lane / 8;
-            const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * EPI_LD + (lane % 8) * 4);
-            if (rr < rows_left)
-              *reinterpret_cast<uint4*>(obase + (orow0 + rr) * args.ldo + col + (lane % 8) * 4) = val;
+            for (int pass = 0; pass < 8; ++pass) {
+              const int rr = pass * 4 + lane / 8;
+              const uint4 val =
+                  *reinterpret_cast<const uint4*>(blk + rr * 128 + (((lane % 8) ^ (rr & 7)) * 16));
+              if (rr < rows_left)
+                *reinterpret_cast<uint4*>(obase + (orow0 + rr) * args.ldo + col + (lane % 8) * 4) = val;
+            }
+            __syncwarp();
           }
-          __syncwarp();
         } else {
           // SwiGLU backward: dh_u in v; a, b from ab; da | db and scale * h out (bf16)
           const int64_t row = tl.seg_start + r0 + lane;
@@ -435,6 +456,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
     }
+    if (EPI == kBwdEpiF32 && lane == 0) bulk_wait_all();   // the output blocks are written
   }
 
   __syncwarp();
@@ -456,12 +478,24 @@ cudaError_t launch_one_bwd(const CUtensorMap& a, const CUtensorMap& b0, const CU
                            const BwdGemmArgs& args, int64_t max_tiles, cudaStream_t s) {
   if (max_tiles <= 0) return cudaSuccess;
   const size_t smem = bwd_smem_bytes(args.seg_off ? args.groups : 1);
+  // store maps of the fp32 outputs (out, and out2 of a split output); unused otherwise
+  CUtensorMap mo = a, mo2 = a;
+  if (EPI == kBwdEpiF32) {
+    const int64_t rpg = args.group_stride > 0 ? args.group_stride / args.ldo : args.m_dim;
+    const int64_t rows = A_MN ? static_cast<int64_t>(args.seg_off ? args.groups : 1) * rpg
+                              : static_cast<int64_t>(args.dense_rows);
+    if (!make_f32_map(&mo, args.out, static_cast<uint64_t>(args.ldo), static_cast<uint64_t>(rows)))
+      return cudaErrorInvalidValue;
+    if (args.out2 && !make_f32_map(&mo2, args.out2, static_cast<uint64_t>(args.ldo),
+                                   static_cast<uint64_t>(rows)))
+      return cudaErrorInvalidValue;
+  }
   auto kern = tc_bwd_gemm<A_MN, B_MN, EPI>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int64_t pairs_max = device_sm_count() >= 2 ? device_sm_count() / 2 : 1;
   const int64_t pairs = max_tiles < pairs_max ? max_tiles : pairs_max;
-  kern<<<static_cast<unsigned>(2 * pairs), THREADS, smem, s>>>(a, b0, b1, args);
+  kern<<<static_cast<unsigned>(2 * pairs), THREADS, smem, s>>>(a, b0, b1, mo, mo2, args);
   return cudaGetLastError();
 }
 
