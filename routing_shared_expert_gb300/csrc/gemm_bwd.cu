@@ -46,7 +46,10 @@ constexpr int STAGES = 6;
 constexpr int A_BYTES = BMC * BK * 2;
 constexpr int B_BYTES = BNC * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int EPI_BYTES = 4 * 4096;        // one 32 x 32 fp32 staging block per epilogue warp
+// Output staging per epilogue warp: one 32 x 32 fp32 block, or the da, db and h 32 x 32
+// bf16 blocks of the SwiGLU epilogue (2 KB each).
+constexpr int EPI_WARP_BYTES = 6144;
+constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -352,7 +355,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           map_row = orow0;
         }
       }
-      uint8_t* blk = reinterpret_cast<uint8_t*>(epi) + (warp - 2) * 4096;   // fp32 block staging
+      uint8_t* blk = reinterpret_cast<uint8_t*>(epi) + (warp - 2) * EPI_WARP_BYTES;   // output staging
       float dot = 0.f;   // SwiGLU epilogue: this row's sum of dh_u * h over the tile's columns
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -396,8 +399,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             __syncwarp();
           }
         } else {
-          // SwiGLU backward: dh_u in v; a, b from ab; da | db and scale * h out (bf16)
+          // SwiGLU backward: dh_u in v; a, b from ab; da | db and scale * h out (bf16).  When
+          // all 32 rows of the warp lie in the segment the three 32 x 32 blocks are staged in
+          // the 64-byte swizzled layout of the store maps (16-byte piece j of row r at piece
+          // j ^ ((r / 2) mod 4)) and go out by TMA; else each lane stores its own row.
           const int64_t row = tl.seg_start + r0 + lane;
+          const bool block_in = tl.seg_start + r0 + 32 <= tl.seg_end;
+          if (block_in) {
+            if (lane == 0) bulk_wait_read_all();   // the previous blocks have been read out
+            __syncwarp();
+          }
           if (row < tl.seg_end) {
             const float sc = args.row_scale[row];
             const float4* arow =
@@ -440,10 +451,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 db2[i] = pack_bf16x2(dbv[0], dbv[1]);
                 h2[i] = pack_bf16x2(hv[0], hv[1]);
               }
-              const int j0 = col + 8 * v8;
-              *reinterpret_cast<uint4*>(drow + j0) = make_uint4(da2[0], da2[1], da2[2], da2[3]);
-              *reinterpret_cast<uint4*>(drow + args.width + j0) = make_uint4(db2[0], db2[1], db2[2], db2[3]);
-              *reinterpret_cast<uint4*>(hrow + j0) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+              if (block_in) {
+                const int off = lane * 64 + ((v8 ^ ((lane >> 1) & 3)) * 16);
+                *reinterpret_cast<uint4*>(blk + off) = make_uint4(da2[0], da2[1], da2[2], da2[3]);
+                *reinterpret_cast<uint4*>(blk + 2048 + off) = make_uint4(db2[0], db2[1], db2[2], db2[3]);
+                *reinterpret_cast<uint4*>(blk + 4096 + off) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+              } else {
+                const int j0 = col + 8 * v8;
+                *reinterpret_cast<uint4*>(drow + j0) = make_uint4(da2[0], da2[1], da2[2], da2[3]);
+                *reinterpret_cast<uint4*>(drow + args.width + j0) = make_uint4(db2[0], db2[1], db2[2], db2[3]);
+                *reinterpret_cast<uint4*>(hrow + j0) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+              }
+            }
+          }
+          if (block_in) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int32_t brow = static_cast<int32_t>(tl.seg_start + r0);
+              tma_store_2d(&tmO, col, brow, smem_u32(blk));                     // da
+              tma_store_2d(&tmO, args.width + col, brow, smem_u32(blk + 2048));  // db
+              tma_store_2d(&tmO2, col, brow, smem_u32(blk + 4096));             // scale * h
+              bulk_commit();
             }
           }
         }
@@ -456,7 +485,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
     }
-    if (EPI == kBwdEpiF32 && lane == 0) bulk_wait_all();   // the output blocks are written
+    if (lane == 0) bulk_wait_all();   // the output blocks are written
   }
 
   __syncwarp();
@@ -478,8 +507,15 @@ cudaError_t launch_one_bwd(const CUtensorMap& a, const CUtensorMap& b0, const CU
                            const BwdGemmArgs& args, int64_t max_tiles, cudaStream_t s) {
   if (max_tiles <= 0) return cudaSuccess;
   const size_t smem = bwd_smem_bytes(args.seg_off ? args.groups : 1);
-  // store maps of the fp32 outputs (out, and out2 of a split output); unused otherwise
+  // store maps of the outputs: fp32 out (and out2 of a split output), or the SwiGLU
+  // epilogue's bf16 da | db and h
   CUtensorMap mo = a, mo2 = a;
+  if (EPI == kBwdEpiSwiglu) {
+    const uint64_t rows = static_cast<uint64_t>(args.dense_rows);
+    if (!make_bf16_store_map(&mo, args.dab, 2 * static_cast<uint64_t>(args.width), rows) ||
+        !make_bf16_store_map(&mo2, args.hout, static_cast<uint64_t>(args.width), rows))
+      return cudaErrorInvalidValue;
+  }
   if (EPI == kBwdEpiF32) {
     const int64_t rpg = args.group_stride > 0 ? args.group_stride / args.ldo : args.m_dim;
     const int64_t rows = A_MN ? static_cast<int64_t>(args.seg_off ? args.groups : 1) * rpg

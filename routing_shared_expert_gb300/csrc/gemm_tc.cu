@@ -399,17 +399,20 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
 
 namespace {
 
-// 2-D tensor [rows][inner] (row-major, dense), box box_inner x box_rows, 128-byte swizzle.
-// Encoded maps are cached (keyed by device, element type, address, shape and box) so that
-// repeated layer calls on the same buffers cost no driver work on the host.
+// 2-D tensor [rows][inner] (row-major, dense), box box_inner x box_rows, with the given
+// shared-memory swizzle.  Encoded maps are cached (keyed by device, element type, address,
+// shape, box and swizzle) so that repeated layer calls on the same buffers cost no driver
+// work on the host.
 bool make_map_2d(CUtensorMap* m, CUtensorMapDataType type, uint32_t elem_bytes, const void* base,
-                 uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+                 uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+                 CUtensorMapSwizzle swizzle) {
   struct Entry {
     int dev;
     CUtensorMapDataType type;
     const void* base;
     uint64_t inner, rows;
     uint32_t box_inner, box_rows;
+    CUtensorMapSwizzle swizzle;
     CUtensorMap map;
   };
   static std::mutex mu;
@@ -422,7 +425,7 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType type, uint32_t elem_bytes, 
     for (int i = 0; i < n; ++i)
       if (cache[i].dev == dev && cache[i].type == type && cache[i].base == base &&
           cache[i].inner == inner && cache[i].rows == rows && cache[i].box_inner == box_inner &&
-          cache[i].box_rows == box_rows) {
+          cache[i].box_rows == box_rows && cache[i].swizzle == swizzle) {
         *m = cache[i].map;
         return true;
       }
@@ -434,8 +437,8 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType type, uint32_t elem_bytes, 
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   if (enc(m, type, 2, const_cast<void*>(base), dims, strides, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
   std::lock_guard<std::mutex> lock(mu);
   Entry& e = cache[next];
@@ -446,6 +449,7 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType type, uint32_t elem_bytes, 
   e.rows = rows;
   e.box_inner = box_inner;
   e.box_rows = box_rows;
+  e.swizzle = swizzle;
   e.map = *m;
   next = (next + 1) % 64;
   if (n < 64) ++n;
@@ -456,13 +460,22 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType type, uint32_t elem_bytes, 
 
 // bf16 [rows][inner], box 64 x box_rows (128-byte rows of the box), 128-byte swizzle.
 bool make_bf16_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
-  return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, rows, BK, box_rows);
+  return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, rows, BK, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // fp32 [rows][inner], box 32 x 32 (128-byte rows), 128-byte swizzle: the output blocks the
 // expert GEMM epilogues store with TMA.
 bool make_f32_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows) {
-  return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, inner, rows, 32, 32);
+  return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, inner, rows, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// bf16 [rows][inner], box 32 x 32 (64-byte rows), 64-byte swizzle: the 32-column blocks the
+// backward SwiGLU epilogue stores with TMA.
+bool make_bf16_store_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows) {
+  return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, rows, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 cudaError_t set_smem_once(const void* func, size_t bytes) {

@@ -59,6 +59,7 @@ cudaError_t launch_route_tc(const RouteParams& p, cudaStream_t s);
 // 128-byte swizzle, zero fill out of bounds.  False if the driver rejects it.
 bool make_bf16_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 bool make_f32_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows);
+bool make_bf16_store_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows);
 
 // Raise a kernel's dynamic shared-memory limit once per device (host-side cache).
 cudaError_t set_smem_once(const void* func, size_t bytes);
