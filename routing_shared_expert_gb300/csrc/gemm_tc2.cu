@@ -33,7 +33,8 @@
 // Roles per CTA (192 threads): warp 0 TMA producer (both CTAs; completions are
 // counted on the even CTA's barrier), warp 1 TMEM allocation and, in the even
 // CTA only, the MMA issuer; warps 2-5 epilogue.  The epilogue stages each
-// 32 x 32 block through shared memory so that global stores are row-contiguous.
+// 32 x 32 block through shared memory: h blocks go out as row-contiguous lane stores,
+// fp32 f blocks as TMA bulk tensor stores (lane stores at a segment's end).
 // Every wait is bounded by %globaltimer; a wait that runs out records
 // MOE_ERR_TIMEOUT and the CTA drains what it issued before the final cluster
 // barrier and TMEM release.
