@@ -21,7 +21,7 @@
 // Every wait is bounded; a wait that runs out records MOE_ERR_TIMEOUT.
 #include "common.cuh"
 #include "internal.h"
-#include "route_norm.cuh"
+#include "route_select.cuh"
 
 namespace moe {
 namespace {
@@ -173,123 +173,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t t = t0 + q * 32 + lane;
       const bool valid = t < p.T;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      constexpr int EMPTY = 0x7fffffff;
-      float bv[kMaxTopK], bz[kMaxTopK];   // selection key and unbiased logit of each slot
-      int bi[kMaxTopK];
-#pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) { bv[j] = 0.f; bz[j] = 0.f; bi[j] = EMPTY; }
-      float zmax = -INFINITY;
-      const bool sel = p.selection_bias != nullptr;
-      float* lrow = (p.logits && valid) ? p.logits + t * p.N : nullptr;
-      // pass 1: keys, logits output, top-8 list
-      for (int c0 = 0; c0 < p.N; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(taddr + c0, r);
-        float z[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) z[i] = __uint_as_float(r[i]) + (c0 + i < p.N ? s_bias[c0 + i] : 0.f);
-        if (lrow) {
-          if (c0 + 32 <= p.N && (p.N & 3) == 0 && (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              *reinterpret_cast<float4*>(lrow + c0 + 4 * v) =
-                  make_float4(z[4 * v], z[4 * v + 1], z[4 * v + 2], z[4 * v + 3]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c0 + i < p.N) lrow[c0 + i] = z[i];
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (c0 + i >= p.N) break;
-          zmax = fmaxf(zmax, z[i]);
-          const float cv = sel ? z[i] + s_sel[c0 + i] : z[i];
-          const float cz = z[i];
-          const int ci = c0 + i;
-          if (bi[kMaxTopK - 1] == EMPTY || cv > bv[kMaxTopK - 1]) {
-            // The kept keys are a descending prefix of the list; the new key goes behind
-            // every kept key it does not exceed (an equal later expert never displaces an
-            // earlier one).  Its place is a count and the shift is per slot, so one
-            // insertion is a few dependent steps rather than a chain along the list.
-            int pos = 0;
-#pragma unroll
-            for (int j = 0; j < kMaxTopK; ++j) pos += (bi[j] != EMPTY && !(cv > bv[j])) ? 1 : 0;
-#pragma unroll
-            for (int j = kMaxTopK - 1; j > 0; --j) {
-              const bool shift = j > pos, here = j == pos;
-              bv[j] = shift ? bv[j - 1] : (here ? cv : bv[j]);
-              bz[j] = shift ? bz[j - 1] : (here ? cz : bz[j]);
-              bi[j] = shift ? bi[j - 1] : (here ? ci : bi[j]);
-            }
-            if (pos == 0) { bv[0] = cv; bz[0] = cz; bi[0] = ci; }
-          }
-        }
-      }
-      // scores and weights of the selected experts
-      float w[kMaxTopK];
-#pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) w[j] = 0.f;
-      if (p.norm == MOE_NORM_SOFTMAX_SELECTED) {
-        float s = 0.f, msel = bz[0];
-#pragma unroll
-        for (int j = 1; j < kMaxTopK; ++j)
-          if (j < p.K) msel = fmaxf(msel, bz[j]);
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-          if (j < p.K) { w[j] = expf(bz[j] - msel); s += w[j]; }
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-          if (j < p.K) w[j] /= s;
-      } else {
-        if (p.score == MOE_SCORE_SOFTMAX) {
-          // pass 2: softmax denominator over all N experts (unbiased logits)
-          const float m = zmax;
-          float s = 0.f;
-          for (int c0 = 0; c0 < p.N; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(taddr + c0, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c0 + i < p.N) s += expf(__uint_as_float(r[i]) + s_bias[c0 + i] - m);
-          }
-#pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j)
-            if (j < p.K) w[j] = expf(bz[j] - m) / s;
-        } else {
-#pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j)
-            if (j < p.K) w[j] = 1.f / (1.f + expf(-bz[j]));
-        }
-        if (p.norm == MOE_NORM_L1_SELECTED) {
-          float s = 0.f;
-#pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j)
-            if (j < p.K) s += w[j];
-#pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j)
-            if (j < p.K) w[j] /= s;
-        } else if (p.norm == MOE_NORM_LP_SELECTED) {
-          lp_normalise(w, p.K, p.norm_p);
-        }
-      }
-      float shared = 0.f;
-      if (p.shared_mode == MOE_SHARED_CONST) {
-        shared = p.shared_gain;
-      } else if (p.shared_mode == MOE_SHARED_SIGMOID_GATE) {
+      float gate_raw = 0.f;
+      if (p.shared_mode == MOE_SHARED_SIGMOID_GATE) {
         uint32_t r[32];
         tmem_ld32(taddr + a.n_pad, r);
-        shared = 1.f / (1.f + expf(-__uint_as_float(r[0])));
+        gate_raw = __uint_as_float(r[0]);
       }
-      if (valid) {
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-          if (j < p.K) {
-            p.topk_idx[t * p.K + j] = bi[j];
-            p.topk_w[t * p.K + j] = p.alpha * w[j];
-          }
-        if (p.shared_coef) p.shared_coef[t] = shared;
-      }
+      route_one_token(p, s_bias, s_sel, t, valid,
+                      [&](int c0, uint32_t(&r)[32]) { tmem_ld32(taddr + c0, r); }, gate_raw);
     }
     }
   }
