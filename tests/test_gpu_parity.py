@@ -47,6 +47,11 @@ SMALL = {
     # pair tiles over segments of at most two 256-row tiles (~256 rows per expert): the
     # expert GEMMs run a segment's second row tile on the same pair right after its first
     "pair_short_s": C["dsv3"].replace(T=2048, d_model=512, N=64, d_expert=256, d_shared=128),
+    # router shapes off the power-of-two grid: 40 experts (48 padded columns read as two
+    # 32-column chunks) with a partial last K block (d = 456), and the learned shared gate
+    # with an odd number of K blocks (d = 320)
+    "olmo_n40_s": C["olmo"].replace(T=1300, d_model=456, N=40, d_expert=128, d_shared=128),
+    "qwen2_d320_s": C["qwen2"].replace(T=900, d_model=320, d_expert=128, d_shared=128),
     # L_p normalisation of the selected weights (Table 52, MegaBlocks row) on both routers:
     # the tensor-core bf16 router (softmax, p = 2; sigmoid, p = 8) and the fp32 one (p = 3)
     "olmo_lp2": C["olmo"].replace(T=500, d_model=256, d_expert=128, d_shared=128, norm="lp",
