@@ -252,31 +252,42 @@ __global__ void __launch_bounds__(256) place_kernel(PermuteParams p) {
 }
 
 // One warp per token: each 16-byte piece of x[t] is read once and written to the
-// packed rows of all of t's kept routes.
+// packed rows of all of t's kept routes.  A lane issues four loads before their stores
+// (the source and destination never overlap), so each warp keeps several reads in flight.
 __global__ void __launch_bounds__(256) gather_kernel(PermuteParams p) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + warp;
   if (t >= p.T) return;
   const int64_t cap = p.T * p.K;
-  int64_t dst[kMaxTopK];
-  int n = 0;
+  int64_t dst[kMaxTopK];   // packed row of slot k, or -1 (dropped or no slot)
 #pragma unroll
   for (int k = 0; k < kMaxTopK; ++k) {
     dst[k] = -1;
     if (k < p.K) {
       const int32_t pos = p.route_pos[t * p.K + k];
       if (pos >= cap) set_status(p.status, MOE_ERR_DEVICE_BOUNDS);
-      else if (pos >= 0) dst[n++] = pos;
+      else if (pos >= 0) dst[k] = pos;
     }
   }
   const int64_t nvec = static_cast<int64_t>(p.d) * p.elem_bytes / 16;
-  const int4* src = reinterpret_cast<const int4*>(static_cast<const char*>(p.x) + t * nvec * 16);
-  int4* out = static_cast<int4*>(p.x_perm);
-  for (int64_t v = lane; v < nvec; v += 32) {
-    const int4 val = src[v];
+  const int4* __restrict__ src =
+      reinterpret_cast<const int4*>(static_cast<const char*>(p.x) + t * nvec * 16);
+  int4* __restrict__ out = static_cast<int4*>(p.x_perm);
+  constexpr int U = 4;
+  for (int64_t v0 = lane; v0 < nvec; v0 += 32 * U) {
+    int4 val[U];
 #pragma unroll
-    for (int k = 0; k < kMaxTopK; ++k)
-      if (k < n) out[dst[k] * nvec + v] = val;
+    for (int u = 0; u < U; ++u)
+      if (v0 + u * 32 < nvec) val[u] = src[v0 + u * 32];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = v0 + u * 32;
+      if (v < nvec) {
+#pragma unroll
+        for (int k = 0; k < kMaxTopK; ++k)
+          if (dst[k] >= 0) out[dst[k] * nvec + v] = val[u];
+      }
+    }
   }
 }
 
