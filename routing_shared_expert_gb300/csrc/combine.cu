@@ -7,7 +7,9 @@
 // 2^-9 of the largest |f| per element, most of a 1.5e-2 relative budget).
 // One CTA per token; each thread owns 16 bytes of a row (4 fp32) and
 // accumulates in fp32 in a fixed order (slot 0..K-1, then the shared term), so
-// the result does not depend on scheduling.  Loads and stores are 16-byte vectors.
+// the result does not depend on scheduling.  Loads and stores are 16-byte vectors;
+// the pieces of all kept routes and of g are first requested into L2 together, so
+// the in-order loads that follow do not each wait out a DRAM round trip.
 #include "common.cuh"
 #include "internal.h"
 
@@ -40,6 +42,10 @@ struct Vec<float> {
   }
 };
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 template <typename T>
 __global__ void __launch_bounds__(1024) combine_kernel(CombineParams p) {
   constexpr int V = Vec<T>::N;
@@ -60,6 +66,9 @@ __global__ void __launch_bounds__(1024) combine_kernel(CombineParams p) {
   const T* g = static_cast<const T*>(p.g);
   const float s = (g != nullptr && p.shared_coef != nullptr) ? p.shared_coef[t] : 0.f;
   for (int c = threadIdx.x * V; c < p.d; c += blockDim.x * V) {
+    for (int k = 0; k < p.K; ++k)
+      if (s_pos[k] >= 0) prefetch_l2(f + static_cast<int64_t>(s_pos[k]) * p.d + c);
+    if (g != nullptr && p.shared_coef != nullptr) prefetch_l2(g + t * p.d + c);
     float acc[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0.f;
