@@ -667,19 +667,20 @@ moe_status layer_backward(const moe_config* cfg, const moe_weights* w, const voi
   rp.dy = dy;
   rp.counts_keep = fwd->counts_keep;
   rp.offsets = fwd->offsets;
-  rp.perm_src = fwd->perm_src;
+  rp.topk_idx = fwd->topk_idx;
   rp.route_pos = fwd->route_pos;
   rp.topk_w = fwd->topk_w;
   rp.seg_pad = seg_pad;
   rp.x_pad = at<__nv_bfloat16>(ws, L.x_pad);
   rp.gf = at<__nv_bfloat16>(ws, L.gf);
   rp.r_pad = at<float>(ws, L.r_pad);
+  rp.rows_cap = L.rows_cap;
   rp.T = c.T;
   rp.d = c.d_model;
   rp.N = c.N;
   rp.K = c.K;
   rp.status = status;
-  if (!ok(launch_bwd_rows(rp, L.rows_cap, st))) return MOE_ERR_CUDA;
+  if (!ok(launch_bwd_rows(rp, st))) return MOE_ERR_CUDA;
   s = bwd_family(c, true, seg_pad, L.rows_cap, rp.x_pad, rp.gf, rp.r_pad,
                  router ? at<float>(ws, L.dot) : nullptr, at<float>(ws, L.ab),
                  at<__nv_bfloat16>(ws, L.dab), at<__nv_bfloat16>(ws, L.h), at<float>(ws, L.dxr),

@@ -35,60 +35,78 @@ __global__ void pad_offsets_kernel(const int32_t* counts_keep, int N, int32_t* s
   }
 }
 
-// One warp per padded row: the row of x, the upstream gradient dy of its token (bf16,
-// unscaled) and the route's coefficient r (applied in the GEMM epilogues), or zeros for a
-// padding row.
+// One warp per token: the row of x and the upstream gradient dy (as bf16, unscaled) are
+// read once and written to the padded rows of all of the token's kept routes, with each
+// route's coefficient r (applied in the GEMM epilogues).  Reading per token rather than
+// per padded row fetches x and dy once instead of once per route.
 __global__ void __launch_bounds__(256) bwd_rows_kernel(BwdRowsParams p) {
   __shared__ int32_t s_pad[kMaxExperts + 1];
   for (int i = threadIdx.x; i <= p.N; i += blockDim.x) s_pad[i] = p.seg_pad[i];
   __syncthreads();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t pp = static_cast<int64_t>(blockIdx.x) * 8 + warp;
-  if (pp >= s_pad[p.N]) return;
-  int lo = 0, hi = p.N;   // s_pad[lo] <= pp < s_pad[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (s_pad[mid] <= pp) lo = mid; else hi = mid;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (t >= p.T) return;
+  int64_t dst[kMaxTopK];   // padded row of slot k, or -1 (dropped or no slot)
+#pragma unroll
+  for (int k = 0; k < kMaxTopK; ++k) {
+    dst[k] = -1;
+    if (k < p.K) {
+      const int32_t pos = p.route_pos[t * p.K + k];
+      if (pos < 0) continue;
+      const int32_t e = p.topk_idx[t * p.K + k];
+      if (e < 0 || e >= p.N) {
+        if (lane == 0) set_status(p.status, MOE_ERR_DEVICE_BOUNDS);
+        continue;
+      }
+      const int64_t local = static_cast<int64_t>(pos) - p.offsets[e];
+      const int64_t row = s_pad[e] + local;
+      if (local < 0 || local >= p.counts_keep[e] || row >= s_pad[e + 1] || row < 0 ||
+          row >= p.rows_cap) {
+        if (lane == 0) set_status(p.status, MOE_ERR_DEVICE_BOUNDS);
+        continue;
+      }
+      dst[k] = row;
+      if (lane == 0) p.r_pad[dst[k]] = p.topk_w[t * p.K + k];
+    }
   }
-  const int e = lo;
-  const int64_t local = pp - s_pad[e];
-  uint4* xo = reinterpret_cast<uint4*>(p.x_pad + pp * p.d);
-  uint4* go = reinterpret_cast<uint4*>(p.gf + pp * p.d);
   const int vecs = p.d / 8;
-  if (local >= p.counts_keep[e]) {
-    for (int v = lane; v < vecs; v += 32) {
-      xo[v] = make_uint4(0, 0, 0, 0);
-      go[v] = make_uint4(0, 0, 0, 0);
-    }
-    if (lane == 0) p.r_pad[pp] = 0.f;
-    return;
-  }
-  const int64_t pos = p.offsets[e] + local;
-  const int32_t t = p.perm_src[pos];
-  if (t < 0 || t >= p.T) {
-    if (lane == 0) set_status(p.status, MOE_ERR_DEVICE_BOUNDS);
-    return;
-  }
-  float r = 0.f;
-  bool found = false;
-  for (int k = 0; k < p.K; ++k)
-    if (p.route_pos[static_cast<int64_t>(t) * p.K + k] == pos) {
-      r = p.topk_w[static_cast<int64_t>(t) * p.K + k];
-      found = true;
-    }
-  if (!found) {
-    if (lane == 0) set_status(p.status, MOE_ERR_DEVICE_BOUNDS);
-    return;
-  }
-  const uint4* xi = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.x) + static_cast<int64_t>(t) * p.d);
-  const float4* dyi = reinterpret_cast<const float4*>(p.dy + static_cast<int64_t>(t) * p.d);
+  const uint4* __restrict__ xi =
+      reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.x) + t * p.d);
+  const float4* __restrict__ dyi = reinterpret_cast<const float4*>(p.dy + t * p.d);
+  uint4* __restrict__ xo = reinterpret_cast<uint4*>(p.x_pad);
+  uint4* __restrict__ go = reinterpret_cast<uint4*>(p.gf);
   for (int v = lane; v < vecs; v += 32) {
-    xo[v] = xi[v];
+    const uint4 xv = xi[v];
     const float4 a = dyi[2 * v], b = dyi[2 * v + 1];
-    go[v] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
-                       pack_bf16x2(b.z, b.w));
+    const uint4 gv = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                                pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k)
+      if (dst[k] >= 0) {
+        xo[dst[k] * vecs + v] = xv;
+        go[dst[k] * vecs + v] = gv;
+      }
   }
-  if (lane == 0) p.r_pad[pp] = r;
+}
+
+// The padding rows of each expert's segment (from its kept count up to the next multiple
+// of 64): zeros and r = 0.  One warp per (expert, padding row) pair.
+__global__ void __launch_bounds__(256) bwd_pad_rows_kernel(BwdRowsParams p) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t w = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  const int e = static_cast<int>(w / 64);
+  if (e >= p.N) return;
+  const int32_t kept = p.counts_keep[e];
+  const int64_t row = static_cast<int64_t>(p.seg_pad[e]) + kept + (w % 64);
+  if (kept < 0 || p.seg_pad[e] < 0 || row >= p.seg_pad[e + 1] || row >= p.rows_cap) return;
+  const int vecs = p.d / 8;
+  uint4* xo = reinterpret_cast<uint4*>(p.x_pad + row * p.d);
+  uint4* go = reinterpret_cast<uint4*>(p.gf + row * p.d);
+  for (int v = lane; v < vecs; v += 32) {
+    xo[v] = make_uint4(0, 0, 0, 0);
+    go[v] = make_uint4(0, 0, 0, 0);
+  }
+  if (lane == 0) p.r_pad[row] = 0.f;
 }
 
 // gs[t] = dy_t (bf16) and s_pad[t] = s_t (0 for the rows up to T rounded to 64), one
@@ -332,9 +350,13 @@ cudaError_t launch_pad_offsets(const int32_t* counts_keep, int N, int32_t* seg_p
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_rows(const BwdRowsParams& p, int64_t rows_cap, cudaStream_t s) {
-  if (rows_cap <= 0) return cudaSuccess;
-  bwd_rows_kernel<<<static_cast<unsigned>((rows_cap + 7) / 8), 256, 0, s>>>(p);
+cudaError_t launch_bwd_rows(const BwdRowsParams& p, cudaStream_t s) {
+  if (p.T > 0) {
+    bwd_rows_kernel<<<static_cast<unsigned>((p.T + 7) / 8), 256, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  bwd_pad_rows_kernel<<<static_cast<unsigned>(p.N * 8), 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -187,13 +187,14 @@ struct BwdRowsParams {
   const float* dy;            // [T][d]
   const int32_t* counts_keep; // [N]
   const int32_t* offsets;     // [N+1] packed offsets of the forward
-  const int32_t* perm_src;    // [K*T]
+  const int32_t* topk_idx;    // [T][K]
   const int32_t* route_pos;   // [T][K]
   const float* topk_w;        // [T][K]
   const int32_t* seg_pad;     // [N+1] padded offsets
   __nv_bfloat16* x_pad;       // [rows][d]
   __nv_bfloat16* gf;          // [rows][d] dy of the row's token (bf16)
   float* r_pad;               // [rows] the row's coefficient r (0 for padding rows)
+  int64_t rows_cap;           // rows of x_pad, gf and r_pad
   int64_t T;
   int32_t d, N, K;
   int32_t* status;
@@ -237,7 +238,7 @@ cudaError_t launch_router_bwd(const RouterBwdParams& p, cudaStream_t s);
 cudaError_t launch_dws(const float* du, const void* x, int64_t T, int d, float* part, float* dws,
                        cudaStream_t s);
 cudaError_t launch_pad_offsets(const int32_t* counts_keep, int N, int32_t* seg_pad, cudaStream_t s);
-cudaError_t launch_bwd_rows(const BwdRowsParams& p, int64_t rows_cap, cudaStream_t s);
+cudaError_t launch_bwd_rows(const BwdRowsParams& p, cudaStream_t s);
 cudaError_t launch_shared_scale(const float* dy, const float* sc, int64_t T, int64_t t_pad, int d,
                                 __nv_bfloat16* gs, float* s_pad, cudaStream_t s);
 cudaError_t launch_dx_combine(const BwdCombineParams& p, cudaStream_t s);
