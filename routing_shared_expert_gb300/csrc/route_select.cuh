@@ -21,15 +21,17 @@ namespace moe {
 // every thread of the warp (the tensor-memory load it may wrap is warp-collective).
 // gate_raw is the shared-gate logit w_s . x when the layer has a learned gate.  s_bias and
 // s_sel hold the logit bias and the selection-only bias per expert (zeros when absent).
-template <class Load32>
+// L is the length of the sorted list, any L >= K (the list's first K entries are the
+// selection whatever L is; a shorter list takes fewer and shorter insertions).
+template <int L, class Load32>
 __device__ __forceinline__ void route_one_token(const RouteParams& p, const float* s_bias,
                                                 const float* s_sel, int64_t t, bool valid,
                                                 Load32&& load32, float gate_raw) {
   constexpr int EMPTY = 0x7fffffff;
-  float bv[kMaxTopK], bz[kMaxTopK];   // selection key and unbiased logit of each slot
-  int bi[kMaxTopK];
+  float bv[L], bz[L];   // selection key and unbiased logit of each slot
+  int bi[L];
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) { bv[j] = 0.f; bz[j] = 0.f; bi[j] = EMPTY; }
+  for (int j = 0; j < L; ++j) { bv[j] = 0.f; bz[j] = 0.f; bi[j] = EMPTY; }
   float zmax = -INFINITY;
   const bool sel = p.selection_bias != nullptr;
   float* lrow = (p.logits && valid) ? p.logits + t * p.N : nullptr;
@@ -59,16 +61,16 @@ __device__ __forceinline__ void route_one_token(const RouteParams& p, const floa
       const float cv = sel ? z[i] + s_sel[c0 + i] : z[i];
       const float cz = z[i];
       const int ci = c0 + i;
-      if (bi[kMaxTopK - 1] == EMPTY || cv > bv[kMaxTopK - 1]) {
+      if (bi[L - 1] == EMPTY || cv > bv[L - 1]) {
         // The kept keys are a descending prefix of the list; the new key goes behind
         // every kept key it does not exceed (an equal later expert never displaces an
         // earlier one).  Its place is a count and the shift is per slot, so one
         // insertion is a few dependent steps rather than a chain along the list.
         int pos = 0;
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) pos += (bi[j] != EMPTY && !(cv > bv[j])) ? 1 : 0;
+        for (int j = 0; j < L; ++j) pos += (bi[j] != EMPTY && !(cv > bv[j])) ? 1 : 0;
 #pragma unroll
-        for (int j = kMaxTopK - 1; j > 0; --j) {
+        for (int j = L - 1; j > 0; --j) {
           const bool shift = j > pos, here = j == pos;
           bv[j] = shift ? bv[j - 1] : (here ? cv : bv[j]);
           bz[j] = shift ? bz[j - 1] : (here ? cz : bz[j]);
@@ -79,19 +81,19 @@ __device__ __forceinline__ void route_one_token(const RouteParams& p, const floa
     }
   }
   // scores and weights of the selected experts
-  float w[kMaxTopK];
+  float w[L];
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) w[j] = 0.f;
+  for (int j = 0; j < L; ++j) w[j] = 0.f;
   if (p.norm == MOE_NORM_SOFTMAX_SELECTED) {
     float s = 0.f, msel = bz[0];
 #pragma unroll
-    for (int j = 1; j < kMaxTopK; ++j)
+    for (int j = 1; j < L; ++j)
       if (j < p.K) msel = fmaxf(msel, bz[j]);
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j)
+    for (int j = 0; j < L; ++j)
       if (j < p.K) { w[j] = expf(bz[j] - msel); s += w[j]; }
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j)
+    for (int j = 0; j < L; ++j)
       if (j < p.K) w[j] /= s;
   } else {
     if (p.score == MOE_SCORE_SOFTMAX) {
@@ -106,20 +108,20 @@ __device__ __forceinline__ void route_one_token(const RouteParams& p, const floa
           if (c0 + i < p.N) s += expf(__uint_as_float(r[i]) + s_bias[c0 + i] - m);
       }
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j)
+      for (int j = 0; j < L; ++j)
         if (j < p.K) w[j] = expf(bz[j] - m) / s;
     } else {
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j)
+      for (int j = 0; j < L; ++j)
         if (j < p.K) w[j] = 1.f / (1.f + expf(-bz[j]));
     }
     if (p.norm == MOE_NORM_L1_SELECTED) {
       float s = 0.f;
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j)
+      for (int j = 0; j < L; ++j)
         if (j < p.K) s += w[j];
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j)
+      for (int j = 0; j < L; ++j)
         if (j < p.K) w[j] /= s;
     } else if (p.norm == MOE_NORM_LP_SELECTED) {
       lp_normalise(w, p.K, p.norm_p);
@@ -133,7 +135,7 @@ __device__ __forceinline__ void route_one_token(const RouteParams& p, const floa
   }
   if (valid) {
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j)
+    for (int j = 0; j < L; ++j)
       if (j < p.K) {
         p.topk_idx[t * p.K + j] = bi[j];
         p.topk_w[t * p.K + j] = p.alpha * w[j];

@@ -13,7 +13,8 @@
 //     column N_pad).  With few experts a CTA takes a quarter of the SM's shared
 //     memory and TMEM, so several run per SM;
 //   - warps 2-5 read the accumulators with tcgen05.ld, one token row per
-//     thread, so the selection runs in registers: a sorted top-8 list with
+//     thread, so the selection runs in registers: a sorted list of 2, 4 or 8
+//     entries (the smallest that holds K) with
 //     strict comparisons (an equal later expert never displaces an earlier one,
 //     which gives the lower-index tie rule) on the key z (+ the Eq. 35
 //     selection-only bias), then the scores of the selected experts from the
@@ -44,6 +45,9 @@ struct RouteTcArgs {
   uint32_t tmem_cols;  // power of two >= n_pad (+16 when gated)
 };
 
+// L: length of the per-token sorted list (2, 4 or 8, the smallest that holds K); one
+// kernel per length, so each carries only its own selection code.
+template <int L>
 __global__ void __launch_bounds__(THREADS, 1)
     route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmG, const RouteTcArgs a) {
@@ -179,8 +183,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(taddr + a.n_pad, r);
         gate_raw = __uint_as_float(r[0]);
       }
-      route_one_token(p, s_bias, s_sel, t, valid,
-                      [&](int c0, uint32_t(&r)[32]) { tmem_ld32(taddr + c0, r); }, gate_raw);
+      route_one_token<L>(p, s_bias, s_sel, t, valid,
+                         [&](int c0, uint32_t(&r)[32]) { tmem_ld32(taddr + c0, r); }, gate_raw);
     }
     }
   }
@@ -233,10 +237,14 @@ cudaError_t launch_route_tc(const RouteParams& p, cudaStream_t s) {
   if (a.stages < 2) a.stages = 2;
   const size_t smem = 1024 + static_cast<size_t>(a.stages) * a.stage_bytes + 8 * 20 + 16 +
                       2 * sizeof(float) * kMaxExperts + 64;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(route_tc_kernel), smem);
+  using Kernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const RouteTcArgs);
+  const Kernel kern = p.K <= 2   ? static_cast<Kernel>(route_tc_kernel<2>)
+                      : p.K <= 4 ? static_cast<Kernel>(route_tc_kernel<4>)
+                                 : static_cast<Kernel>(route_tc_kernel<kMaxTopK>);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>((p.T + rows - 1) / rows);
-  route_tc_kernel<<<grid, THREADS, smem, s>>>(mX, mW, mG, a);
+  kern<<<grid, THREADS, smem, s>>>(mX, mW, mG, a);
   return cudaGetLastError();
 }
 
