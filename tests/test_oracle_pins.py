@@ -501,3 +501,127 @@ def test_eq35_selection_bias_moves_selection_not_weights():
     assert biased.topk_idx[0].tolist() == [3, 0]           # keys (1.0, 0.9, -1.0, 1.5)
     e = np.exp(np.array([0.0, 1.0]))
     np.testing.assert_allclose(biased.topk_w[0], e / e.sum(), rtol=1e-15)
+
+
+# ------------------------------- Section 10.7.1: sigmoid scores in the LBL term --
+
+def _sigmoid_lbl_case():
+    """Six tokens, two experts, top-1, sigmoid routing.  Two tokens have logits (ln 3, 0),
+    so sigma = (3/4, 1/2) and the scores normalised across the experts are (3/5, 2/5); four
+    tokens have logits (0, ln 3) and normalised scores (2/5, 3/5).  Expert 0 wins the first
+    two tokens, expert 1 the other four: C = (2, 4), f = (1/3, 2/3),
+    P = ((2 * 3/5 + 4 * 2/5) / 6, (2 * 2/5 + 4 * 3/5) / 6) = (7/15, 8/15) and
+    L = 2 (1/3 * 7/15 + 2/3 * 8/15) = 46/45 (Eq. 30, Eq. 38)."""
+    l3 = math.log(3.0)
+    z = np.array([[l3, 0.0]] * 2 + [[0.0, l3]] * 4)
+    return z, (2, 4), (1 / 3, 2 / 3), (7 / 15, 8 / 15), 46 / 45
+
+
+def _check_sigmoid_lbl(normalized_scores):
+    z, C, f_want, P_want, L_want = _sigmoid_lbl_case()
+    p = normalized_scores(z, "sigmoid")
+    np.testing.assert_allclose(p[0], [3 / 5, 2 / 5], rtol=1e-14)
+    np.testing.assert_allclose(p[2], [2 / 5, 3 / 5], rtol=1e-14)
+    # three experts by hand: sigma(ln 3, 0, -ln 3) = (3/4, 1/2, 1/4), sum 3/2
+    l3 = math.log(3.0)
+    np.testing.assert_allclose(normalized_scores(np.array([[l3, 0.0, -l3]]), "sigmoid")[0],
+                               [1 / 2, 1 / 3, 1 / 6], rtol=1e-14)
+    idx = O.select_topk(z, 1)
+    assert O.requested_counts(idx, 2).tolist() == list(C)
+    f, P, L = O.lbl_statistics(p, idx, 2)
+    np.testing.assert_allclose(f, f_want, rtol=1e-14)
+    np.testing.assert_allclose(P, P_want, rtol=1e-14)
+    assert abs(L - L_want) < 1e-14
+    # Eq. 38: P is a probability vector for sigmoid routing too
+    rng = np.random.default_rng(11)
+    zr = rng.normal(size=(40, 7))
+    assert abs(O.lbl_statistics(normalized_scores(zr, "sigmoid"), O.select_topk(zr, 2), 7)[1]
+               .sum() - 1.0) < 1e-13
+
+
+def test_section10_7_1_sigmoid_scores_normalised_across_experts():
+    """Section 10.7.1: for sigmoid routing the LBL's soft term uses the sigmoid scores divided
+    by their sum over the experts of the token; worked by hand on a six-token example."""
+    _check_sigmoid_lbl(O.normalized_scores)
+    # softmax scores are used as they are (already normalised)
+    z = np.array([[0.0, math.log(3.0)]])
+    np.testing.assert_allclose(O.normalized_scores(z, "softmax")[0], [1 / 4, 3 / 4], rtol=1e-15)
+
+
+@pytest.mark.parametrize("mistake", ["unnormalised", "divided_by_N", "softmax_of_sigmoid"])
+def test_sigmoid_lbl_pin_catches_plausible_mistakes(mistake):
+    """The pin above fails for each plausible misreading of the normalisation (mistakes planted
+    in a copy of the oracle function, on the CPU): sigmoid scores left unnormalised
+    (L = 23/18), divided by N instead of their sum (L = 23/36), or a softmax over them."""
+    def wrong(z, score):
+        if score == "softmax":
+            return O.softmax_all(z)
+        q = O.sigmoid(z)
+        if mistake == "unnormalised":
+            return q
+        if mistake == "divided_by_N":
+            return q / q.shape[1]
+        return O.softmax_all(q)
+    with pytest.raises(AssertionError):
+        _check_sigmoid_lbl(wrong)
+
+
+# ------------------------------------------- the additive per-expert logit bias --
+
+def _bias_layer():
+    """One token, d = 1, three experts, K = 2, softmax scores kept without renormalisation
+    (the Qwen row of Table 52).  Projection logits x W_r^T = (ln 4, ln 2, 0); the logit bias
+    (0, ln 4, 0) makes z = (ln 4, ln 8, 0), whose softmax is (4, 8, 1) / 13."""
+    inputs = {
+        "x": np.array([[1.0]]),
+        "W_router": np.array([[math.log(4.0)], [math.log(2.0)], [0.0]]),
+        "router_bias": np.array([0.0, math.log(4.0), 0.0]),
+        "W_gate": np.ones((3, 1, 1)), "W_up": np.ones((3, 1, 1)), "W_down": np.ones((3, 1, 1)),
+    }
+    cfg = Cfg(N=3, K=2, T=1, score="softmax", norm="none", alpha=1.0, shared_mode="none")
+    return cfg, inputs
+
+
+# expected by hand, and what each misreading of the bias would give instead
+BIAS_EXPECTED = ([1, 0], [8 / 13, 4 / 13])
+BIAS_MISREADINGS = {
+    "bias ignored": ([0, 1], [4 / 7, 2 / 7]),
+    "bias in the selection only": ([1, 0], [2 / 7, 4 / 7]),
+    "bias in the scores only": ([0, 1], [4 / 13, 8 / 13]),
+}
+
+
+def _check_bias(oracle_module, check_logits=True):
+    cfg, inputs = _bias_layer()
+    if check_logits:
+        z = oracle_module.router_logits(inputs["x"], inputs["W_router"], inputs["router_bias"])
+        np.testing.assert_allclose(z[0], np.log([4.0, 8.0, 1.0]), rtol=1e-15)
+    y, rt, _ = oracle_module.moe_forward(cfg, inputs)
+    assert rt.topk_idx[0].tolist() == BIAS_EXPECTED[0]
+    np.testing.assert_allclose(rt.topk_w[0], BIAS_EXPECTED[1], rtol=1e-14)
+    # routed mass 12/13 < 1 (Table 52, no renormalisation)
+    assert abs(rt.topk_w[0].sum() - 12 / 13) < 1e-15
+    # experts are identity-like: f_i(1) = SiLU(1) * 1 * 1, so y = (12/13) SiLU(1)
+    assert abs(y[0, 0] - 12 / 13 / (1 + math.exp(-1.0))) < 1e-14
+
+
+def test_logit_bias_enters_selection_and_scores():
+    """An additive per-expert logit bias (the Qwen2- and Mixtral-shaped layers' recipe) is part
+    of the logit: it moves both the selected set and the softmax weights.  Worked by hand: the
+    bias turns the selection from (0, 1) into (1, 0) and the weights into (8/13, 4/13)."""
+    _check_bias(O)
+    # the hand values of every misreading differ from the expected ones in the selection,
+    # the weights, or both, so the pin above rejects each of them
+    for idx, w in BIAS_MISREADINGS.values():
+        assert idx != BIAS_EXPECTED[0] or not np.allclose(w, BIAS_EXPECTED[1])
+
+
+def test_logit_bias_pin_catches_a_dropped_bias(monkeypatch):
+    """A mistake planted in the oracle on the CPU: a router projection that drops the bias
+    fails the pin, both on the logits and through the whole forward."""
+    real = O.moe_oracle.router_logits
+    monkeypatch.setattr(O.moe_oracle, "router_logits", lambda x, W, b=None: real(x, W, None))
+    with pytest.raises(AssertionError):
+        _check_bias(O.moe_oracle)
+    with pytest.raises(AssertionError):
+        _check_bias(O.moe_oracle, check_logits=False)
