@@ -50,3 +50,23 @@ def read_golden(name):
 @pytest.fixture
 def golden():
     return read_golden
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print every parity case's measured error next to its bar (and write the table to the
+    file named by MOE_PARITY_LOG, when set)."""
+    mod = sys.modules.get("tests.gpu_helpers")
+    rows = getattr(mod, "ERRORS", None) if mod is not None else None
+    if not rows:
+        return
+    lines = ["parity: max|y - y_ref| / rms(y_ref) against the bar",
+             f"{'case':<44} {'error':>10} {'bar':>9} {'error/bar':>9}"]
+    for case, err, bar in rows:
+        lines.append(f"{case:<44} {err:10.3e} {bar:9.1e} {err / bar:9.2f}")
+    terminalreporter.write_line("")
+    for ln in lines:
+        terminalreporter.write_line(ln)
+    path = os.environ.get("MOE_PARITY_LOG")
+    if path:
+        with open(path, "w") as fh:
+            fh.write("\n".join(lines) + "\n")

@@ -6,7 +6,8 @@ import pytest
 import torch
 
 import oracle as O
-from tests.gpu_helpers import TOL, check_routing_exact, host, layer_error, oracle_y, run_layer
+from tests.gpu_helpers import (TOL, check_routing_exact, host, layer_error, oracle_y, record_error,
+                               run_layer)
 from workloads import CONFIGS, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -40,6 +41,7 @@ def test_selection_bias_moves_selection_only(name):
     hin = host(inp)
     y_ref, _ = oracle_y(spec, hin, rt, np.arange(spec.T))
     err = layer_error(spec, layer.out["y"].cpu().double().numpy(), y_ref, rt.route_pos)
+    record_error(f"{name} with selection bias", err, TOL[spec.dtype])
     assert err <= TOL[spec.dtype]
 
 
@@ -78,8 +80,14 @@ def test_bias_update_matches_oracle_bit_for_bit():
     import routing_shared_expert_gb300 as moe
     g = torch.Generator().manual_seed(11)
     for N in (8, 60, 256):
-        counts = torch.randint(0, 50, (N,), generator=g, dtype=torch.int32)
-        counts[: N // 8] = int(counts.float().mean().round())   # some exactly-average experts... maybe
+        # counts whose mean is exactly m = 25: n0 experts at m (sign 0 in Eq. 37), the rest in
+        # pairs m + delta, m - delta (sign -1 and +1)
+        m = 25
+        n0 = N // 8 + (N - N // 8) % 2
+        delta = torch.randint(1, m + 1, ((N - n0) // 2,), generator=g, dtype=torch.int32)
+        counts = torch.cat([torch.full((n0,), m, dtype=torch.int32), m + delta, m - delta])
+        counts = counts[torch.randperm(N, generator=g)]
+        assert int(counts.sum()) == m * N
         bias = torch.randn(N, generator=g)
         want = O.bias_update(bias.numpy(), counts.numpy(), 0.001)
         b = bias.to("cuda")

@@ -11,7 +11,7 @@ import torch
 
 import oracle as O
 from tests.gpu_helpers import (TOL, check_logits, check_routing_exact, host, layer_error, oracle_y,
-                               rel_err, run_layer)
+                               record_error, rel_err, run_layer)
 from workloads import CONFIGS, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -83,6 +83,7 @@ def test_layer_small(name):
     np.testing.assert_allclose(layer.out["shared_coef"].cpu().double().numpy(), s_ref, rtol=1e-5,
                                atol=1e-6)
     err = layer_error(spec, layer.out["y"].cpu().double().numpy(), y_ref, rt.route_pos)
+    record_error(name, err, TOL[spec.dtype])
     assert err <= TOL[spec.dtype], f"{name}: rel err {err:.3e}"
     if spec.cap_policy != "none":
         assert rt.drops["dropped_routes"] > 0, "capacity case should drop routes"
@@ -140,7 +141,9 @@ def test_equal_logits_ties_and_dense_reduction():
     Wu = torch.cat([hin["W_up"][e] for e in range(K)] + [hin["Ws_up"]], 0)
     Wd = torch.cat([hin["W_down"][e] for e in range(K)] + [hin["Ws_down"]], 1)
     dense = O.swiglu(hin["x"], Wg, Wu, Wd)
-    assert rel_err(layer.out["y"].cpu().double().numpy(), dense) <= TOL["bf16"]
+    err = rel_err(layer.out["y"].cpu().double().numpy(), dense)
+    record_error("olmo_s all-equal logits = dense (Eq. 81)", err, TOL["bf16"])
+    assert err <= TOL["bf16"]
 
 
 def test_empty_batch():
@@ -163,7 +166,9 @@ def test_single_token_and_single_row_experts():
     rt = check_routing_exact(layer, spec)
     assert (rt.counts_keep <= 1).all() and rt.counts_keep.sum() == spec.K
     y_ref, _ = oracle_y(spec, host(inp), rt, np.arange(1))
-    assert rel_err(layer.out["y"].cpu().double().numpy(), y_ref) <= TOL["bf16"]
+    err = rel_err(layer.out["y"].cpu().double().numpy(), y_ref)
+    record_error("dsv3_s T=1", err, TOL["bf16"])
+    assert err <= TOL["bf16"]
 
 
 def test_merge_shared_on_device():
@@ -191,7 +196,9 @@ def test_merge_shared_on_device():
                                      lambda e: (hin["W_gate"][e], hin["W_up"][e], hin["W_down"][e]),
                                      None, np.zeros(spec.T))
     y_ref = y_ref + sum(O.swiglu(x, p[0].cpu(), p[1].cpu(), p[2].cpu()) for p in parts)
-    assert rel_err(layer.out["y"].cpu().double().numpy(), y_ref) <= TOL["f32"]
+    err = rel_err(layer.out["y"].cpu().double().numpy(), y_ref)
+    record_error("tiny merged shared (Eq. 76)", err, TOL["f32"])
+    assert err <= TOL["f32"]
 
 
 @pytest.mark.parametrize("name", ["olmo_s", "mixtral_s"])
@@ -252,6 +259,7 @@ def test_layer_full_size_sampled(name):
         shared, s)
     y_dev = layer.out["y"][torch.as_tensor(tokens, device="cuda")].cpu().double().numpy()
     err = layer_error(spec, y_dev, y_ref, rt.route_pos[tokens])
+    record_error(f"{name} full size, {n} sampled tokens", err, TOL["bf16"])
     assert err <= TOL["bf16"], f"{name}: rel err {err:.3e}"
     if spec.cap_policy != "none":
         assert rt.drops["dropped_routes"] > 0
