@@ -1,11 +1,13 @@
 """Benchmark of the routed + shared-expert MoE layer forward on GB300.
 
-Default: one GPU, the Olmo-shaped bf16 layer (T=8192, d=2560, N=32 experts of
-width 2560, top-4, one shared expert of width 1280), synthetic seeded inputs.
-Prints ONE JSON line.  ``--impl reference`` times the CPU oracle instead (on
-bounded samples of the same workload).  Under torchrun each rank runs its own
-replica on its own batch (weak scaling, no collective on the data path); rank 0
-prints the line with the max time over ranks.
+Default: one GPU, the DeepSeek-V3-shaped bf16 layer (T=8192, d=7168, N=256 experts
+of width 2048, top-8 sigmoid routing renormalised with alpha=2.5, one shared expert
+of width 2048), the largest of the benchmark layers, synthetic seeded inputs.  The
+Olmo-, Qwen2- and Mixtral-shaped layers are timed the same way and reported in the
+line's ``per_config`` block.  Prints ONE JSON line.  ``--impl reference`` times the
+CPU oracle instead (on bounded samples of the same workload).  Under torchrun each
+rank runs its own replica on its own batch (weak scaling, no collective on the data
+path); rank 0 prints the line with the max time over ranks.
 """
 from __future__ import annotations
 
@@ -29,9 +31,9 @@ NOMINAL_HBM_GBS = 8000.0
 
 # DRAM traffic of the dominant stage (the routed gate/up and down launches of one
 # moe_grouped_swiglu call), dram__bytes_read.sum + dram__bytes_write.sum summed over the
-# two launches, from one `ncu --set full` capture per workload (profiles/grouped_gemm_olmo.md).
-# It is reported only while the kernel sources hash to the value they had at capture time.
-STAGE_TRAFFIC = {"olmo": {"sources_sha256": "6d2e3c4d5b628963", "bytes": 2054847280}}
+# two launches, from one ncu capture per workload.  It is reported only while the kernel
+# sources hash to the value they had at capture time.
+STAGE_TRAFFIC = {}
 TRAFFIC_SOURCES = ("routing_shared_expert_gb300/csrc/gemm_tc2.cu", "routing_shared_expert_gb300/csrc/common.cuh")
 
 
@@ -162,12 +164,14 @@ def job_tokens_per_s(world: int, tokens_per_rank: int, steps: int, total_ms: flo
 # ----------------------------------------------------------------- oracle timing
 
 class ExpertsF64:
-    """Per-expert float64 copies of a [N, ...] weight tensor, converted on first use and
-    kept (up to a host-memory cap): the oracle's inputs held resident in its own number
-    format, as the GPU arm's are held resident in HBM.  The conversion is input
-    preparation, so timed oracle runs are repeated until no conversion happens in them."""
+    """Per-expert float64 host copies of a [N, ...] weight tensor (on the device or the
+    host), converted on first use and kept up to a host-memory cap: the oracle's inputs held
+    resident in its own number format, as the GPU arm's are held resident in HBM.  The
+    conversion is input preparation, so timed oracle runs are repeated (at most twice)
+    while they convert; weights beyond the cap are converted inside the timed run, and the
+    count of such conversions is reported with the sample."""
 
-    CAP_BYTES = 24 << 30
+    CAP_BYTES = 8 << 30
     held = 0            # bytes cached over all instances
     conversions = 0     # conversions so far (a timed run must add none)
 
@@ -201,7 +205,8 @@ def oracle_inputs(inp_host: dict) -> dict:
 
 def oracle_seconds(spec, inp_host, S: int) -> float:
     """Wall time of the oracle's full layer forward on the first S tokens, its weights
-    already converted (the run is repeated, at most twice more, while it converted any)."""
+    already converted where they fit the cache (the run is repeated, at most twice more,
+    while it converted any); ``oracle_seconds.converted`` holds the last run's conversions."""
     sub = spec.replace(T=S)
     d = dict(inp_host)
     d["x"] = inp_host["x"][:S]
@@ -211,9 +216,13 @@ def oracle_seconds(spec, inp_host, S: int) -> float:
         t0 = time.perf_counter()
         O.moe_forward(sub, d)
         t = time.perf_counter() - t0
-        if ExpertsF64.conversions == c0:
+        oracle_seconds.converted = ExpertsF64.conversions - c0
+        if oracle_seconds.converted == 0:
             break
     return t
+
+
+oracle_seconds.converted = 0
 
 
 def time_oracle(spec, inp_host, budget_s: float, min_tokens: int = 64):
@@ -269,6 +278,7 @@ def sweep_entropy(args, spec):
     inp = make_inputs(spec, dev)
     cfg = moe.config_from_spec(spec)
     ws = moe.alloc_workspace(cfg, dev)
+    W_down = moe.pack_weights(inp["W_down"]) if cfg.h_format == 1 else inp["W_down"]
     R = spec.T * spec.K
     g = torch.Generator(device=dev)
     g.manual_seed(1)
@@ -281,14 +291,14 @@ def sweep_entropy(args, spec):
         assert sum(counts) == R and len(counts) == spec.N
         offs = torch.tensor([0] + list(__import__("itertools").accumulate(counts)), dtype=torch.int32, device=dev)
         for _ in range(3):
-            moe.moe_grouped_swiglu(cfg, x_perm, offs, None, inp["W_gate"], inp["W_up"], inp["W_down"], f, ws)
+            moe.moe_grouped_swiglu(cfg, x_perm, offs, None, inp["W_gate"], inp["W_up"], W_down, f, ws)
         torch.cuda.synchronize()
         ms = 0.0
         for _ in range(args.steps):
             flush.add_(1)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            moe.moe_grouped_swiglu(cfg, x_perm, offs, None, inp["W_gate"], inp["W_up"], inp["W_down"], f, ws)
+            moe.moe_grouped_swiglu(cfg, x_perm, offs, None, inp["W_gate"], inp["W_up"], W_down, f, ws)
             b.record()
             torch.cuda.synchronize()
             ms += a.elapsed_time(b)
@@ -371,13 +381,95 @@ def bench_backward(args, spec, layer, x, config, dev):
 
 # ----------------------------------------------------------------- main
 
+def time_forward(spec, args, dev, world: int, rank: int, flush, stream, clocks_on: bool = True):
+    """Warm up, then time args.steps moe_layer_forward calls of one layer (the fused call a
+    user makes), with four events recorded inside each by the library after router,
+    permutation, routed experts and combine (the shared expert runs on the library's second
+    stream beside the first three; the last interval holds the wait for it and the combine).
+    The steps are queued back to back (no host sync between them); a 256 MiB buffer is
+    written between a step's last event and the next step's first (flushes the 129 MB L2).
+    Returns the layer, its inputs and the timings (max over ranks)."""
+    import torch
+    import routing_shared_expert_gb300 as moe
+    from workloads import make_inputs
+    inp = make_inputs(spec, dev, seed=0)
+    if world > 1:
+        # each rank its own batch of tokens (weak scaling); weights are the same replica
+        inp["x"] = make_inputs(spec.replace(N=1, d_expert=64, d_shared=0), dev, seed=rank)["x"]
+    layer = moe.MoELayer(moe.config_from_spec(spec), inp, dev)
+    x = inp["x"]
+    for _ in range(max(args.warmup, 3)):
+        layer.forward(x, logits=False)
+        flush.add_(1)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device()) if clocks_on else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    stage_names = ("route", "permute", "grouped_swiglu", "join_combine")
+    stage_ms = {k: 0.0 for k in stage_names}
+    events = []
+    w0 = time.time()
+    for _ in range(args.steps):
+        flush.add_(1)                        # write 256 MiB (> L2) between steps
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        layer.forward_profiled(x, ev, stream)
+        events.append(ev)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clk = clocks.stop(w0, w1) if clocks else None
+    step_ms = 0.0
+    for ev in events:
+        step_ms += ev[0].elapsed_time(ev[4])
+        for i, k in enumerate(stage_names):
+            stage_ms[k] += ev[i].elapsed_time(ev[i + 1])
+    vals = max_over_ranks([step_ms] + [stage_ms[k] for k in stage_names], dev, world)
+    assert layer.status() == 0, f"device status word set while timing {spec.name}"
+    kept = int(layer.out["counts_keep"].sum())
+    return {"layer": layer, "inp": inp, "x": x, "total_ms": vals[0],
+            "stage_ms": {k: v / args.steps for k, v in zip(stage_names, vals[1:])},
+            "clocks": clk, "kept": kept}
+
+
+def summarize(spec, r, args, world: int, pk):
+    """Throughput, executed TFLOP/s and the grouped stage's roofline of one timed layer."""
+    kept = r["kept"]
+    ms = r["total_ms"] / args.steps
+    flops = spec.expert_flops(kept)
+    tflops = world * flops / (ms / 1e3) / 1e12
+    g_ms = r["stage_ms"]["grouped_swiglu"]
+    g_tf = 6.0 * spec.d_model * spec.d_expert * kept / (g_ms / 1e3) / 1e12
+    return {"ms_per_step": ms, "tokens_per_s": job_tokens_per_s(world, spec.T, args.steps, r["total_ms"]),
+            "tflops": tflops, "pct_bf16_peak": 100.0 * tflops / pk["bf16_tflops"],
+            "grouped_tflops": g_tf, "grouped_frac": g_tf / pk["bf16_tflops"],
+            "stages_ms": r["stage_ms"], "kept_routes": kept}
+
+
+def workload_config(spec):
+    return {"workload": spec.name, "T": spec.T, "d_model": spec.d_model, "N": spec.N,
+            "d_expert": spec.d_expert, "K": spec.K, "d_shared": spec.d_shared,
+            "score": spec.score, "norm": spec.norm, "alpha": spec.alpha,
+            "shared": spec.shared_mode, "capacity": spec.cap_policy,
+            "intermediate": ("h fp16, down projections packed to fp16 once (moe_pack_weights)"
+                             if spec.dtype == "bf16" else "fp32")}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="olmo")
+    ap.add_argument("--config", default="dsv3")
+    ap.add_argument("--per-config", default="olmo,qwen2,mixtral",
+                    help="other workloads timed the same way and reported in per_config ('none': skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--sweep", choices=["entropy"], default=None,
@@ -407,16 +499,16 @@ def main():
     if args.sweep == "entropy":
         return sweep_entropy(args, spec)
     cores = len(os.sched_getaffinity(0))
-    config = {"workload": spec.name, "T": spec.T, "d_model": spec.d_model, "N": spec.N,
-              "d_expert": spec.d_expert, "K": spec.K, "d_shared": spec.d_shared,
-              "score": spec.score, "norm": spec.norm, "alpha": spec.alpha,
-              "shared": spec.shared_mode, "capacity": spec.cap_policy}
+    config = workload_config(spec)
 
     if args.impl == "reference":
         if rank != 0:
             return 0
         import torch
-        inp = oracle_inputs(make_inputs(spec, "cpu"))
+        # the same seeded tensors as the GPU arm (drawn on the device when there is one,
+        # then read by the oracle on the host cores)
+        src = "cuda" if torch.cuda.is_available() else "cpu"
+        inp = oracle_inputs(make_inputs(spec, src))
         # one bounded sample size S for every step, sized so the whole run takes a few minutes
         per_step = min(args.cpu_budget, max(0.05, 150.0 / (args.warmup + args.steps)))
         S, _ = time_oracle(spec, inp, budget_s=per_step, min_tokens=16)
@@ -447,15 +539,11 @@ def main():
     dev = torch.device("cuda", local)
 
     import routing_shared_expert_gb300 as moe
-    inp = make_inputs(spec, dev, seed=0)
-    if world > 1:
-        # each rank its own batch of tokens (weak scaling); weights are the same replica
-        inp["x"] = make_inputs(spec.replace(N=1, d_expert=64, d_shared=0), dev, seed=rank)["x"]
-    layer = moe.MoELayer(moe.config_from_spec(spec), inp, dev)
-    x = inp["x"]
     if args.forward_only > 0:
+        inp = make_inputs(spec, dev, seed=0)
+        layer = moe.MoELayer(moe.config_from_spec(spec), inp, dev)
         for _ in range(args.forward_only):
-            layer.forward(x, logits=False)
+            layer.forward(inp["x"], logits=False)
         torch.cuda.synchronize()
         if layer.status() != 0:
             raise RuntimeError(f"layer status {layer.status()}")
@@ -464,44 +552,16 @@ def main():
         return 0
     stream = torch.cuda.current_stream()
     if args.mode == "backward":
-        return bench_backward(args, spec, layer, x, config, dev)
+        inp = make_inputs(spec, dev, seed=0)
+        layer = moe.MoELayer(moe.config_from_spec(spec), inp, dev)
+        return bench_backward(args, spec, layer, inp["x"], config, dev)
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    for _ in range(max(args.warmup, 3)):
-        layer.forward(x, logits=False)
-        flush.add_(1)
-    torch.cuda.synchronize()
-
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
-    time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    # Timed region: the fused layer call a user makes (moe_layer_forward), with four events
-    # recorded inside it by the library after router, permutation, routed experts and
-    # combine (the shared expert runs on the library's second stream beside the first
-    # three; the last interval holds the wait for it and the combine).  The steps are queued back to back (no host sync between
-    # them); the L2 flush sits between a step's last event and the next step's first.
-    stage_names = ("route", "permute", "grouped_swiglu", "join_combine")
-    stage_ms = {k: 0.0 for k in stage_names}
-    events = []
-    w0 = time.time()
-    for _ in range(args.steps):
-        flush.add_(1)                        # write 256 MiB (> L2) between steps
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-        layer.forward_profiled(x, ev)
-        events.append(ev)
-    torch.cuda.synchronize()
-    w1 = time.time()
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop(w0, w1)
-    step_ms = []
-    for ev in events:
-        step_ms.append(ev[0].elapsed_time(ev[4]))
-        for i, k in enumerate(stage_names):
-            stage_ms[k] += ev[i].elapsed_time(ev[i + 1])
+    pk = peaks()
+    r = time_forward(spec, args, dev, world, rank, flush, stream)
+    layer, inp, x = r["layer"], r["inp"], r["x"]
+    head = summarize(spec, r, args, world, pk)
+    head_clocks = r["clocks"]
 
     # End to end through the public call: every step copies its x from pinned host memory,
     # runs moe_layer_forward and copies y back to pinned host memory, all inside the timed
@@ -544,57 +604,78 @@ def main():
     s_out.wait_event(ev_out[args.steps - 1])
     t_b.record(s_out)
     torch.cuda.synchronize()
-    e2e = [t_a.elapsed_time(t_b)]
+    e2e_ms = max_over_ranks([t_a.elapsed_time(t_b)], dev, world)[0]
     assert torch.equal(y_host[(args.steps - 1) % 2], layer.forward(x, logits=False).cpu()), \
         "end-to-end result differs from the device result"
-
-    total_ms, e2e_ms = max_over_ranks([sum(step_ms), sum(e2e)], dev, world)
-
     assert layer.status() == 0, "device status word set during the benchmark"
-    kept = int(layer.out["counts_keep"].sum())
-    ms = total_ms / args.steps
-    tokens_per_s = job_tokens_per_s(world, spec.T, args.steps, total_ms)
-    flops = spec.expert_flops(kept)
-    tflops = world * flops / (ms / 1e3) / 1e12
-    pk = peaks()
-    g_ms = stage_ms["grouped_swiglu"] / args.steps
-    g_flops = 6.0 * spec.d_model * spec.d_expert * kept
-    g_tf = g_flops / (g_ms / 1e3) / 1e12
+    kept = head["kept_routes"]
+    e2e = {"value": job_tokens_per_s(world, spec.T, args.steps, e2e_ms), "unit": "tokens/s",
+           "h2d_bytes_per_step": x.numel() * x.element_size(),
+           "d2h_bytes_per_step": layer.out["y"].numel() * 4,
+           "method": "pinned host x -> device, moe_layer_forward, y -> pinned host every step; "
+                     "copies on their own streams overlap the neighbouring steps' compute",
+           "l2": f"no flush: every step reads {weight_bytes / 1e9:.2f} GB of weights (> L2) "
+                 "and a freshly copied x"}
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the oracle reads each expert's weights from the device copy and converts it to
+        # float64 on first use (held up to the cache's cap)
+        hin = oracle_inputs(inp)
+        S, t = time_oracle(spec, hin, budget_s=args.cpu_budget)
+        conv = oracle_seconds.converted
+        cpu_baseline = {"value": S / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                        "sample": f"first {S} of {spec.T} tokens of the {spec.name} layer, "
+                                  f"full forward in float64 ({t:.1f} s"
+                                  + (f", including {conv} expert weight conversions to float64 "
+                                     "that did not fit the 8 GB host cache)" if conv else ")")}
+        del hin
+    del layer, inp, x, r, x_host, y_host, x_dev, y_dev, outs
+    torch.cuda.empty_cache()
+
+    # the other bf16 workloads, each timed the same way (same steps, warm-up, L2 flush)
+    per_config = {}
+    names = [] if args.per_config in ("", "none") else args.per_config.split(",")
+    for name in names:
+        if name == spec.name or name not in CONFIGS:
+            continue
+        sp = CONFIGS[name]
+        rr = time_forward(sp, args, dev, world, rank, flush, stream)
+        sm = summarize(sp, rr, args, world, pk)
+        clk = rr["clocks"] or {}
+        per_config[name] = {"ms_per_step": sm["ms_per_step"], "tokens_per_s": sm["tokens_per_s"],
+                            "tflops": sm["tflops"], "pct_bf16_peak": sm["pct_bf16_peak"],
+                            "grouped_frac": sm["grouped_frac"], "stages_ms": sm["stages_ms"],
+                            "kept_routes": sm["kept_routes"],
+                            "clocks": {k: clk.get(k) for k in ("sm_mhz", "reasons", "samples")}}
+        del rr
+        torch.cuda.empty_cache()
 
     line = {
-        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
+        "metric": METRIC, "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
+        "data": "synthetic",
         "config": dict(config, l2="256 MiB buffer written between timed steps (flushes the 129 MB L2)",
                        timing="CUDA events on the launching stream around each moe_layer_forward call, "
                               "stage events recorded inside it"),
-        "tflops": tflops, "pct_bf16_peak": 100.0 * tflops / pk["bf16_tflops"],
-        "stages_ms": {k: v / args.steps for k, v in stage_ms.items()},
+        "tflops": head["tflops"], "pct_bf16_peak": head["pct_bf16_peak"],
+        "stages_ms": head["stages_ms"],
         "roofline": {"kernel": "grouped_swiglu stage (tcgen05 gate/up + down GEMM launches over packed segments)",
-                     "bound": "tensor", "achieved": g_tf, "peak": pk["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": g_tf / pk["bf16_tflops"],
-                     "frac_sustained": g_tf / pk["bf16_tflops_sustained"],
+                     "bound": "tensor", "achieved": head["grouped_tflops"], "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": head["grouped_frac"],
+                     "frac_sustained": head["grouped_tflops"] / pk["bf16_tflops_sustained"],
                      "peak_source": pk["source"], "traffic": stage_traffic(spec.name),
                      "traffic_unit": "bytes per stage (gate/up + down launches)",
                      "algorithmic_bytes": stage_algorithmic_bytes(spec, kept)},
-        "e2e": {"value": job_tokens_per_s(world, spec.T, args.steps, e2e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": x.numel() * x.element_size(),
-                "d2h_bytes_per_step": layer.out["y"].numel() * 4,
-                "method": "pinned host x -> device, moe_layer_forward, y -> pinned host every step; "
-                          "copies on their own streams overlap the neighbouring steps' compute",
-                "l2": f"no flush: every step reads {weight_bytes / 1e9:.2f} GB of weights (> L2) "
-                      "and a freshly copied x"},
+        "e2e": e2e,
         "gpu_launches": launches_per_step(spec) * args.steps,
-        "clocks": clk,
+        "clocks": head_clocks,
         "kept_routes": kept,
+        "per_config": per_config,
     }
-
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        hin = oracle_inputs({k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp.items()})
-        S, t = time_oracle(spec, hin, budget_s=args.cpu_budget)
-        line["cpu_baseline"] = {"value": S / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                "sample": f"first {S} of {spec.T} tokens of the {spec.name} layer, "
-                                          f"full forward in float64 ({t:.1f} s)"}
+    if cpu_baseline is not None:
+        line["cpu_baseline"] = cpu_baseline
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -23,6 +23,10 @@
  *   coefficient, the expert outputs f, the shared output g and y are fp32
  *   for every dtype (the bf16 path rounds only the expert inputs and the
  *   intermediate h, which feed the tensor cores).  Indices and counts are int32.
+ * - Intermediate format of bf16 layers (cfg->h_format, see moe_h_format): h is
+ *   rounded to bf16 and multiplied by the bf16 down projections as given, or
+ *   rounded to fp16 and multiplied by down projections packed to fp16 once by
+ *   moe_pack_weights.
  * - Weight storage: W_router [N][d] (one row per expert, z = x W_router^T);
  *   W_gate, W_up [N][d_expert][d] (one row per intermediate unit, the columns
  *   of W_g / W_u of Eq. 74); W_down [N][d][d_expert] (one row per output
@@ -57,7 +61,13 @@ typedef enum {
   MOE_ERR_WORKSPACE_TOO_SMALL = -4,
   MOE_ERR_TIMEOUT = -5,            /* device status: a bounded wait inside a kernel ran out */
   MOE_ERR_DEVICE_BOUNDS = -6,      /* device status: a kernel saw an index out of range */
-  MOE_ERR_MISALIGNED = -7          /* a pointer is not 16-byte aligned */
+  MOE_ERR_MISALIGNED = -7,         /* a pointer is not 16-byte aligned */
+  MOE_ERR_RANGE = -8,              /* device status: an fp16 intermediate h left the fp16 range
+                                    * (|h| 2^-h_scale_log2 >= 65520), or a packed weight tensor
+                                    * held a non-finite value; the outputs are not valid */
+  MOE_ERR_BAD_PACK = -9            /* device status: a down-projection pointer of an MOE_H_F16
+                                    * call is not a complete moe_pack_weights buffer of the
+                                    * layer's size */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
@@ -89,6 +99,21 @@ typedef enum { MOE_SHARED_NONE = 0, MOE_SHARED_CONST = 1, MOE_SHARED_SIGMOID_GAT
  * requests in token order. */
 typedef enum { MOE_CAP_NONE = 0, MOE_CAP_PER_EXPERT = 1, MOE_CAP_RANK_WIDE = 2 } moe_cap_policy;
 
+/* Format of the expert intermediate h = SiLU(x W_g) * (x W_u) of bf16 layers (Section 20,
+ * Eq. 74), which is the A operand of the down projection f = h W_d on the tensor cores.
+ * Both operands of one tensor-core product share one type, so the format also fixes how
+ * W_down and Ws_down are passed:
+ *   MOE_H_BF16  h rounded to bf16 (8 significant bits, the range of fp32); W_down and
+ *               Ws_down are the bf16 tensors of the layout above.
+ *   MOE_H_F16   h 2^-h_scale_log2 rounded to fp16 (11 significant bits: eight times less
+ *               rounding error, at the same tensor-core rate); W_down and Ws_down are
+ *               buffers written by moe_pack_weights (fp16 copies scaled by a power of two,
+ *               exact for bf16 weights).  |h| 2^-h_scale_log2 must stay below 65520: a
+ *               larger value becomes an infinity and the call leaves MOE_ERR_RANGE in the
+ *               status word (raise h_scale_log2, or use MOE_H_BF16).
+ * The fp32 layers keep h in fp32 and ignore the field. */
+typedef enum { MOE_H_BF16 = 0, MOE_H_F16 = 1 } moe_h_format;
+
 typedef struct moe_config {
   int64_t T;              /* tokens in the batch, >= 0 */
   int32_t d_model;        /* d */
@@ -107,10 +132,13 @@ typedef struct moe_config {
   int32_t num_ranks;      /* M_E >= 1: destination ranks of rho (Eq. 20) */
   const int32_t* rho;     /* HOST [N], values in [0, num_ranks); NULL means rho(i) = i mod num_ranks */
   float norm_p;           /* p of MOE_NORM_LP_SELECTED, finite, 1 <= p <= 64; ignored otherwise */
+  int32_t h_format;       /* moe_h_format (bf16 layers); 0 = MOE_H_BF16 */
+  int32_t h_scale_log2;   /* MOE_H_F16: h is stored as fp16(h 2^-h_scale_log2), -64..64; usually 0 */
 } moe_config;
 
 /* Weights of one layer (device pointers, layouts above).  router_bias, selection_bias and
- * shared_gate_w [d] may be NULL; shared weights are ignored when d_shared == 0. */
+ * shared_gate_w [d] may be NULL; shared weights are ignored when d_shared == 0.  With
+ * h_format MOE_H_F16, W_down and Ws_down are moe_pack_weights buffers of the same tensors. */
 typedef struct moe_weights {
   const void* W_router;
   const float* router_bias;       /* [N] fp32 logit bias (enters selection and scores), or NULL */
@@ -200,6 +228,25 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32
                                int32_t* R_req, int32_t* R_keep, int32_t* drop_stats,
                                cudaStream_t stream);
 
+/* Bytes of the buffer moe_pack_weights writes for a tensor of `elements` values (host only). */
+moe_status moe_packed_weights_size(int64_t elements, size_t* bytes);
+
+/* Pack one bf16 down-projection tensor (W_down [N][d][d_expert], N * d * d_expert elements,
+ * or Ws_down [d][d_shared], d * d_shared elements) for the fp16 intermediate (MOE_H_F16).
+ * No counterpart on the pages: a storage conversion done once per layer, before the first
+ * forward call.  Writes into `packed` (device, 256-byte aligned, moe_packed_weights_size
+ * bytes, caller-owned): a 256-byte header (a magic word, the scale exponent k, 2^-k, the
+ * element count, a flag for non-finite weights), then the fp16 values W 2^k in the order of
+ * W, with k = 15 - e for the largest magnitude max |W| in [2^(e-1), 2^e) (so the largest
+ * packed value lies in [2^14, 2^15)): bf16 weights convert exactly down to about
+ * max |W| 2^-31.  The expert GEMMs read k from the header and scale their accumulators
+ * by 2^-k.  W [elements] bf16 device, 16-byte aligned; W and packed must not overlap.
+ * Asynchronous on the stream; no host synchronisation.  Errors: MOE_ERR_INVALID_ARG (NULL,
+ * negative count, packed_bytes too small), MOE_ERR_MISALIGNED, MOE_ERR_CUDA.  A non-finite
+ * weight is flagged in the header, and a forward call that reads it reports MOE_ERR_RANGE. */
+moe_status moe_pack_weights(const void* W, int64_t elements, void* packed, size_t packed_bytes,
+                            cudaStream_t stream);
+
 /* Routed experts over densely packed segments (Section 20.1 Eq. 74 per segment; Section 10.3,
  * Eq. 26: packed rows [offsets[e], offsets[e+1]) belong to expert e, nothing else is computed).
  *   offsets [N+1] (device; read on the device, never copied to the host).
@@ -210,14 +257,16 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32
  *                   2.7x slower on bf16 layers (32 four-row TMA gathers per K step), so
  *                   moe_layer_forward uses the packed form.
  * Out: f [K*T][d] fp32: f[row] = SwiGLU_e(packed row) for rows < offsets[N].
- * The intermediate h = SiLU(x W_g) * (x W_u) is kept in the workspace (dtype). */
+ * The intermediate h = SiLU(x W_g) * (x W_u) is kept in the workspace (bf16 or fp16 per
+ * cfg->h_format; W_down is a moe_pack_weights buffer under MOE_H_F16). */
 moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_rows, const int32_t* offsets,
                               const int32_t* perm_src, const void* W_gate, const void* W_up,
                               const void* W_down, void* f, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream);
 
 /* The one (merged) shared expert over all tokens (Section 20.1, Eq. 74-76).
- *   x [T][d]; Ws_gate, Ws_up [d_shared][d]; Ws_down [d][d_shared].
+ *   x [T][d]; Ws_gate, Ws_up [d_shared][d]; Ws_down [d][d_shared] (a moe_pack_weights
+ *   buffer under MOE_H_F16).
  * Out: g [T][d] fp32.  Requires d_shared > 0. */
 moe_status moe_shared_mlp(const moe_config* cfg, const void* x, const void* Ws_gate,
                           const void* Ws_up, const void* Ws_down, void* g,
@@ -310,7 +359,8 @@ moe_status moe_bias_update(int32_t N, const int32_t* counts, float gamma, float*
  * and for a learned shared gate dw_s = sum_t ds_t s_t (1 - s_t) x_t, dx += that times w_s.
  * bf16 layers only, with d_model, d_expert and d_shared multiples of 128 (others:
  * MOE_ERR_UNSUPPORTED); GEMM operands are bf16 (dy, da, db, r h and dz rounded once),
- * accumulation fp32. */
+ * accumulation fp32.  The backward takes the down projections as bf16 tensors: call it with
+ * h_format MOE_H_BF16 (an MOE_H_F16 configuration returns MOE_ERR_UNSUPPORTED). */
 typedef struct moe_grads {
   float* dx;        /* [T][d] fp32 */
   float* dW_gate;   /* [N][d_r][d] fp32 (overwritten) */

@@ -18,12 +18,13 @@ LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
 MOE_OK = 0
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA",
           -4: "MOE_ERR_WORKSPACE_TOO_SMALL", -5: "MOE_ERR_TIMEOUT", -6: "MOE_ERR_DEVICE_BOUNDS",
-          -7: "MOE_ERR_MISALIGNED"}
+          -7: "MOE_ERR_MISALIGNED", -8: "MOE_ERR_RANGE", -9: "MOE_ERR_BAD_PACK"}
 DTYPES = {"f32": 0, "bf16": 1}
 SCORES = {"softmax": 0, "sigmoid": 1}
 NORMS = {"none": 0, "l1": 1, "softmax_selected": 2, "lp": 3}
 SHARED_MODES = {"none": 0, "const": 1, "gate": 2}
 CAP_POLICIES = {"none": 0, "per_expert": 1, "rank_wide": 2}
+H_FORMATS = {"bf16": 0, "f16": 1}
 
 
 class MoEError(RuntimeError):
@@ -38,7 +39,7 @@ class moe_config(ctypes.Structure):
                 ("score", c_int32), ("norm", c_int32), ("alpha", c_float),
                 ("shared_mode", c_int32), ("shared_gain", c_float), ("cap_policy", c_int32),
                 ("capacity_factor", c_double), ("num_ranks", c_int32), ("rho", POINTER(c_int32)),
-                ("norm_p", c_float)]
+                ("norm_p", c_float), ("h_format", c_int32), ("h_scale_log2", c_int32)]
 
 
 class moe_weights(ctypes.Structure):
@@ -74,6 +75,8 @@ def _load():
         "moe_status_string": ([c_int32], c_char_p),
         "moe_workspace_size": ([C, POINTER(c_size_t)], c_int32),
         "moe_workspace_init": ([P, c_size_t, P], c_int32),
+        "moe_packed_weights_size": ([c_int64, POINTER(c_size_t)], c_int32),
+        "moe_pack_weights": ([P, c_int64, P, c_size_t, P], c_int32),
         "moe_route": ([C, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
         "moe_balance_stats": ([C, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
         "moe_bias_update": ([c_int32, P, c_float, P, P], c_int32),
@@ -118,7 +121,8 @@ def _enum(table, v):
 
 def make_config(T, d_model, N, K, d_expert, d_shared, dtype="bf16", score="softmax", norm="l1",
                 alpha=1.0, shared_mode="const", shared_gain=1.0, cap_policy="none",
-                capacity_factor=1.0, num_ranks=1, rho=None, norm_p=2.0) -> moe_config:
+                capacity_factor=1.0, num_ranks=1, rho=None, norm_p=2.0, h_format="bf16",
+                h_scale_log2=0) -> moe_config:
     """Build a ``moe_config``; ``rho`` (host list) is kept alive on the returned object."""
     c = moe_config()
     c.T, c.d_model, c.N, c.K = int(T), int(d_model), int(N), int(K)
@@ -133,10 +137,23 @@ def make_config(T, d_model, N, K, d_expert, d_shared, dtype="bf16", score="softm
     c.capacity_factor = float(capacity_factor)
     c.num_ranks = int(num_ranks)
     c.norm_p = float(norm_p)
+    c.h_format = _enum(H_FORMATS, h_format)
+    c.h_scale_log2 = int(h_scale_log2)
     if rho is not None:
         arr = (c_int32 * len(rho))(*[int(v) for v in rho])
         c._rho_keepalive = arr
         c.rho = ctypes.cast(arr, POINTER(c_int32))
+    return c
+
+
+def copy_config(cfg: moe_config, **changes) -> moe_config:
+    """A copy of ``cfg`` (sharing its host ``rho`` array) with some fields changed."""
+    c = moe_config()
+    ctypes.memmove(ctypes.byref(c), ctypes.byref(cfg), ctypes.sizeof(moe_config))
+    if hasattr(cfg, "_rho_keepalive"):
+        c._rho_keepalive = cfg._rho_keepalive
+    for k, v in changes.items():
+        setattr(c, k, v)
     return c
 
 
@@ -180,6 +197,26 @@ def alloc_workspace(cfg: moe_config, device="cuda", stream=None):
     ws = torch.empty(max(moe_workspace_size(cfg), 256), dtype=torch.uint8, device=device)
     moe_workspace_init(ws, stream)
     return ws
+
+
+def moe_packed_weights_size(elements: int) -> int:
+    n = c_size_t(0)
+    _check("moe_packed_weights_size", _lib.moe_packed_weights_size(int(elements), ctypes.byref(n)))
+    return int(n.value)
+
+
+def moe_pack_weights(W, packed, stream=None):
+    """Pack the bf16 tensor W into ``packed`` (uint8 device tensor) for the fp16 intermediate."""
+    _check("moe_pack_weights", _lib.moe_pack_weights(_ptr(W), W.numel(), _ptr(packed), packed.numel(),
+                                                     _stream(stream)))
+
+
+def pack_weights(W, stream=None):
+    """A new packed buffer (uint8 device tensor) holding W for the fp16 intermediate."""
+    import torch
+    packed = torch.empty(moe_packed_weights_size(W.numel()), dtype=torch.uint8, device=W.device)
+    moe_pack_weights(W, packed, stream)
+    return packed
 
 
 def moe_route(cfg, x, W_router, router_bias, selection_bias, shared_gate_w, topk_idx, topk_w,

@@ -39,6 +39,8 @@ moe_status check_cfg(const moe_config* c) {
       (!std::isfinite(c->capacity_factor) || c->capacity_factor <= 0.0))
     return MOE_ERR_INVALID_ARG;
   if (c->num_ranks < 1 || c->num_ranks > kMaxExperts) return MOE_ERR_INVALID_ARG;
+  if (c->h_format != MOE_H_BF16 && c->h_format != MOE_H_F16) return MOE_ERR_INVALID_ARG;
+  if (c->h_scale_log2 < -64 || c->h_scale_log2 > 64) return MOE_ERR_INVALID_ARG;
   if (c->rho) {
     for (int i = 0; i < c->N; ++i)
       if (c->rho[i] < 0 || c->rho[i] >= c->num_ranks) return MOE_ERR_INVALID_ARG;
@@ -146,6 +148,13 @@ moe_status do_permute(const moe_config& c, const Layout& L, void* ws, const void
   return cuda_status(launch_permute(p, st));
 }
 
+// The intermediate format of a bf16 layer's expert GEMMs (moe_h_format).
+void set_h_format(const moe_config& c, MlpParams* p) {
+  p->h_f16 = c.dtype == MOE_BF16 && c.h_format == MOE_H_F16;
+  p->h_scale = std::ldexp(1.0f, -c.h_scale_log2);
+  p->out_unscale = std::ldexp(1.0f, c.h_scale_log2);
+}
+
 moe_status do_grouped(const moe_config& c, const Layout& L, void* ws, const void* x_rows,
                       const int32_t* offsets, const int32_t* perm_src, const void* Wg,
                       const void* Wu, const void* Wd, void* f, bool tile_prefix_ready,
@@ -177,6 +186,7 @@ moe_status do_grouped(const moe_config& c, const Layout& L, void* ws, const void
   p.h = at<void>(ws, L.h);
   p.out = static_cast<float*>(f);
   p.status = status;
+  set_h_format(c, &p);
   if (c.dtype == MOE_F32) return cuda_status(launch_mlp_f32(p, st));
   return cuda_status(use_pair_tiles(c.T * c.K, c.N) ? launch_mlp_bf16_pair(p, st)
                                                     : launch_mlp_bf16(p, st));
@@ -204,6 +214,7 @@ moe_status do_shared(const moe_config& c, const Layout& L, void* ws, const void*
   p.h = at<void>(ws, L.hs);
   p.out = static_cast<float*>(g);
   p.status = at<int32_t>(ws, L.status);
+  set_h_format(c, &p);
   if (c.dtype == MOE_F32) return cuda_status(launch_mlp_f32(p, st));
   return cuda_status(use_pair_tiles(c.T, 1) ? launch_mlp_bf16_pair(p, st) : launch_mlp_bf16(p, st));
 }
@@ -296,8 +307,30 @@ const char* moe_status_string(int32_t s) {
     case MOE_ERR_TIMEOUT: return "device wait timed out";
     case MOE_ERR_DEVICE_BOUNDS: return "device index out of range";
     case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case MOE_ERR_RANGE: return "a value left the range of the fp16 intermediate format";
+    case MOE_ERR_BAD_PACK: return "down projection is not a packed buffer of the layer's size";
     default: return "unknown status";
   }
+}
+
+moe_status moe_packed_weights_size(int64_t elements, size_t* bytes) {
+  if (elements < 0 || !bytes || elements > (int64_t{1} << 40)) return MOE_ERR_INVALID_ARG;
+  *bytes = moe::kPackHeaderBytes + ((static_cast<size_t>(elements) * 2 + 255) & ~size_t{255});
+  return MOE_OK;
+}
+
+moe_status moe_pack_weights(const void* W, int64_t elements, void* packed, size_t packed_bytes,
+                            cudaStream_t stream) {
+  size_t need = 0;
+  moe_status s = moe_packed_weights_size(elements, &need);
+  if (s != MOE_OK) return s;
+  if (!packed || (elements > 0 && !W) || packed_bytes < need) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(packed) & 255u) != 0 || (reinterpret_cast<uintptr_t>(W) & 15u))
+    return MOE_ERR_MISALIGNED;
+  const char* w0 = static_cast<const char*>(W);
+  const char* p0 = static_cast<const char*>(packed);
+  if (elements > 0 && w0 < p0 + need && p0 < w0 + elements * 2) return MOE_ERR_INVALID_ARG;
+  return moe::launch_pack_f16(W, elements, packed, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
@@ -536,6 +569,7 @@ moe_status check_bwd_cfg(const moe_config* c) {
   moe_status s = check_cfg(c);
   if (s != MOE_OK) return s;
   if (c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c->h_format != MOE_H_BF16) return MOE_ERR_UNSUPPORTED;   // needs the bf16 down projections
   if (c->d_model % 128 != 0 || c->d_expert % 128 != 0 || c->d_shared % 128 != 0)
     return MOE_ERR_UNSUPPORTED;
   return MOE_OK;

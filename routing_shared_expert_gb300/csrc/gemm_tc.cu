@@ -60,6 +60,12 @@ struct TcArgs {
   const int32_t* gather_src;   // non-null: A rows are gathered from x through this table
   int64_t gather_cap;
   int64_t src_rows;
+  // fp16 intermediate: SwiGLU mode stores fp16(h * h_scale); plain mode reads the packed
+  // weights' header and writes accumulator * out_unscale * 2^-k
+  float h_scale;
+  float out_unscale;
+  const PackHeader* down_hdr;
+  int64_t down_elements;
 };
 
 struct Tile {
@@ -97,7 +103,7 @@ __device__ __forceinline__ bool tile_coords(const TcArgs& a, const int* s_tp, co
   return true;
 }
 
-template <bool SWIGLU, bool GATHER>
+template <bool SWIGLU, bool GATHER, bool H16>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
@@ -229,7 +235,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = SWIGLU ? idesc_bf16_f32(BM, 128) : idesc_bf16_f32(BM, 256);
+      // gate/up multiply bf16 x by bf16 weights; the down GEMM of the fp16 intermediate
+      // multiplies fp16 h by the packed fp16 weights
+      constexpr uint32_t idesc =
+          SWIGLU ? idesc_bf16_f32(BM, 128) : idesc_f32acc<H16>(BM, 256);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -280,6 +289,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quarter this warp may access
+    // plain mode of the fp16 intermediate: the packed weights' scale, checked once
+    float out_mul = 1.f;
+    if (H16 && !SWIGLU) {
+      const PackHeader* hd = args.down_hdr;
+      out_mul = args.out_unscale * hd->inv_scale;
+      if (lane == 0 && (hd->magic != kPackMagic || hd->elements != args.down_elements))
+        set_status(args.status, MOE_ERR_BAD_PACK);
+      if (lane == 0 && (hd->flags & kPackNonFinite)) set_status(args.status, MOE_ERR_RANGE);
+    }
     Tile tl;
     int64_t local = 0;
     for (int64_t t = blockIdx.x; tile_coords(args, s_tp, s_off, n_tiles, t, tl);
@@ -295,8 +313,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int64_t row = static_cast<int64_t>(tl.seg_start) + tl.m * BM + q * 32 + lane;
       const bool valid = row < tl.seg_end && row < args.out_rows;
-      __nv_bfloat16* out_row =
-          static_cast<__nv_bfloat16*>(args.out) + (valid ? row : 0) * args.ldo;
+      uint16_t* out_row = static_cast<uint16_t*>(args.out) + (valid ? row : 0) * args.ldo;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(buf * 256);
       if (SWIGLU) {
@@ -307,12 +324,21 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int col0 = tl.n * 128 + c * 32;
           if (valid) {
             uint32_t pk[16];
+            float amax = 0.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float g0 = __uint_as_float(gr[2 * i]), g1 = __uint_as_float(gr[2 * i + 1]);
               const float u0 = __uint_as_float(ur[2 * i]), u1 = __uint_as_float(ur[2 * i + 1]);
-              pk[i] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
+              if constexpr (H16) {
+                const float s0 = silu(g0) * u0 * args.h_scale, s1 = silu(g1) * u1 * args.h_scale;
+                amax = fmaxf(amax, fmaxf(fabsf(s0), fabsf(s1)));
+                pk[i] = pack_f16x2(s0, s1);
+              } else {
+                pk[i] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
+              }
             }
+            // an h value past the fp16 range became an infinity: report it
+            if (H16 && !(amax < kF16RoundsToInf)) set_status(args.status, MOE_ERR_RANGE);
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               if (col0 + v * 8 + 8 <= args.n_out)
@@ -327,6 +353,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < 4; ++c) {
           uint32_t ar[32], br[32];
           tmem_ld32x2(taddr + c * 64, taddr + c * 64 + 32, ar, br);
+          if constexpr (H16) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              ar[i] = __float_as_uint(__uint_as_float(ar[i]) * out_mul);
+              br[i] = __float_as_uint(__uint_as_float(br[i]) * out_mul);
+            }
+          }
           const int col0 = tl.n * 256 + c * 64;
           if (valid) {
 #pragma unroll
@@ -381,12 +414,12 @@ size_t smem_bytes(int groups) {
   return 1024 + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5) + 16 + 8 * (groups + 1) + 64;
 }
 
-template <bool SWIGLU, bool GATHER>
+template <bool SWIGLU, bool GATHER, bool H16>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                        const TcArgs& args, int64_t max_tiles, cudaStream_t s) {
   if (max_tiles <= 0) return cudaSuccess;
   const size_t smem = smem_bytes(args.groups);
-  auto kern = tc_grouped_gemm<SWIGLU, GATHER>;
+  auto kern = tc_grouped_gemm<SWIGLU, GATHER, H16>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int sms = device_sm_count();
@@ -464,6 +497,13 @@ bool make_bf16_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ro
                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// fp16 [rows][inner]: the same boxes as make_bf16_map (fp16 intermediate h and packed
+// down-projection weights).
+bool make_f16_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, inner, rows, BK, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 // fp32 [rows][inner], box 32 x 32 (128-byte rows), 128-byte swizzle: the output blocks the
 // expert GEMM epilogues store with TMA.
 bool make_f32_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows) {
@@ -516,7 +556,10 @@ int device_sm_count() {
   return n;
 }
 
-cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {
+namespace {
+
+template <bool H16>
+cudaError_t run_one(const MlpParams& p, cudaStream_t s) {
   const bool dense = p.offsets == nullptr;
   const int64_t rows_cap = p.a_rows;
   if (rows_cap == 0 || (dense && p.dense_rows == 0)) return cudaSuccess;
@@ -528,8 +571,10 @@ cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {
   if (!make_bf16_map(&mA, p.A, p.d, gather ? p.src_rows : rows_cap, gather ? 1 : BM) ||
       !make_bf16_map(&mG, p.W_gate, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
       !make_bf16_map(&mU, p.W_up, p.d, static_cast<uint64_t>(p.groups) * p.width, 128) ||
-      !make_bf16_map(&mH, p.h, p.width, rows_cap, BM) ||
-      !make_bf16_map(&mD, p.W_down, p.width, static_cast<uint64_t>(p.groups) * p.d, 256))
+      !(H16 ? make_f16_map(&mH, p.h, p.width, rows_cap, BM)
+            : make_bf16_map(&mH, p.h, p.width, rows_cap, BM)) ||
+      !(H16 ? make_f16_map(&mD, down_values(p), p.width, static_cast<uint64_t>(p.groups) * p.d, 256)
+            : make_bf16_map(&mD, p.W_down, p.width, static_cast<uint64_t>(p.groups) * p.d, 256)))
     return cudaErrorInvalidValue;
 
   TcArgs a{};
@@ -542,6 +587,10 @@ cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {
   a.gather_src = p.gather_src;
   a.gather_cap = rows_cap;
   a.src_rows = p.src_rows;
+  a.h_scale = p.h_scale;
+  a.out_unscale = p.out_unscale;
+  a.down_hdr = H16 ? static_cast<const PackHeader*>(p.W_down) : nullptr;
+  a.down_elements = static_cast<int64_t>(p.groups) * p.d * p.width;
 
   // gate/up + SiLU -> h
   a.k_dim = p.d;
@@ -550,8 +599,8 @@ cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {
   a.out = p.h;
   a.ldo = p.width;
   const int64_t gu_tiles = mt_ub * ((p.width + 127) / 128);
-  cudaError_t e = gather ? launch_one<true, true>(mA, mG, mU, a, gu_tiles, s)
-                         : launch_one<true, false>(mA, mG, mU, a, gu_tiles, s);
+  cudaError_t e = gather ? launch_one<true, true, H16>(mA, mG, mU, a, gu_tiles, s)
+                         : launch_one<true, false, H16>(mA, mG, mU, a, gu_tiles, s);
   if (e != cudaSuccess) return e;
 
   // down -> out (h is packed)
@@ -561,7 +610,13 @@ cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {
   a.b_rows_per_group = p.d;
   a.out = p.out;
   a.ldo = p.d;
-  return launch_one<false, false>(mH, mD, mD, a, mt_ub * ((p.d + 255) / 256), s);
+  return launch_one<false, false, H16>(mH, mD, mD, a, mt_ub * ((p.d + 255) / 256), s);
+}
+
+}  // namespace
+
+cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s) {
+  return p.h_f16 ? run_one<true>(p, s) : run_one<false>(p, s);
 }
 
 }  // namespace moe

@@ -80,6 +80,12 @@ struct PairArgs {
   const int32_t* gather_src; // non-null: A rows are gathered from x through this table
   int64_t gather_cap;        // entries of gather_src
   int64_t src_rows;          // rows of x
+  // fp16 intermediate: SwiGLU mode stores fp16(h * h_scale); plain mode reads the packed
+  // weights' header and writes accumulator * out_unscale * 2^-k
+  float h_scale;
+  float out_unscale;
+  const PackHeader* down_hdr;
+  int64_t down_elements;     // elements the packed tensor must hold
 };
 
 // Epilogue modes of the pair kernel.
@@ -135,7 +141,7 @@ __device__ __forceinline__ void load_b(uint32_t sB, bool half, bool leader, cons
   }
 }
 
-template <int MODE, bool GATHER, int KSUB>
+template <int MODE, bool GATHER, int KSUB, bool H16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_pair_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA64,
                  const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
@@ -325,8 +331,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (leader && lane == 0) {
-      constexpr uint32_t idesc_full = idesc_bf16_f32(PM, 256);
-      constexpr uint32_t idesc_half = idesc_bf16_f32(2 * HM, 256);
+      // gate/up multiply bf16 x by bf16 weights; the down GEMM of the fp16 intermediate
+      // multiplies fp16 h by the packed fp16 weights
+      constexpr bool kF16Ops = H16 && !SWIGLU;
+      constexpr uint32_t idesc_full = idesc_f32acc<kF16Ops>(PM, 256);
+      constexpr uint32_t idesc_half = idesc_f32acc<kF16Ops>(2 * HM, 256);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -377,6 +386,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
     uint32_t* stg = epi + (warp - 2) * EPI_WARP_WORDS;
+    // plain mode of the fp16 intermediate: the packed weights' scale, checked once
+    float out_mul = 1.f;
+    if (H16 && !SWIGLU) {
+      const PackHeader* hd = args.down_hdr;
+      out_mul = args.out_unscale * hd->inv_scale;
+      if (lane == 0 && (hd->magic != kPackMagic || hd->elements != args.down_elements))
+        set_status(args.status, MOE_ERR_BAD_PACK);
+      if (lane == 0 && (hd->flags & kPackNonFinite)) set_status(args.status, MOE_ERR_RANGE);
+    }
     Tile tl;
     int64_t local = 0;
     for (int64_t t = pair_id; pair_tile(s_tp, s_off, G, n_tiles, t, tl); t += n_pairs, ++local) {
@@ -401,7 +419,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (SWIGLU) {
         // full tile: gate of h column j in TMEM column j, up in 128 + j; half tile: the
         // warp's 64 h columns with gate in TMEM columns [0,64) and up in [64,128)
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+        uint16_t* out = static_cast<uint16_t*>(args.out);
+        float amax = 0.f;
         const int chunks = tl.half ? 2 : 4;
         const int up_off = tl.half ? 64 : 128;
 #pragma unroll 1
@@ -415,8 +434,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int e = 8 * v + 2 * i;
-              w4[i] = pack_bf16x2(silu(__uint_as_float(gr[e])) * __uint_as_float(ur[e]),
-                                  silu(__uint_as_float(gr[e + 1])) * __uint_as_float(ur[e + 1]));
+              const float h0 = silu(__uint_as_float(gr[e])) * __uint_as_float(ur[e]);
+              const float h1 = silu(__uint_as_float(gr[e + 1])) * __uint_as_float(ur[e + 1]);
+              if constexpr (H16) {
+                const float s0 = h0 * args.h_scale, s1 = h1 * args.h_scale;
+                amax = fmaxf(amax, fmaxf(fabsf(s0), fabsf(s1)));
+                w4[i] = pack_f16x2(s0, s1);
+              } else {
+                w4[i] = pack_bf16x2(h0, h1);
+              }
             }
             *reinterpret_cast<uint4*>(stg + lane * EPI_LD + 4 * v) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
@@ -433,6 +459,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           __syncwarp();
         }
+        // an h value of this lane's row past the fp16 range became an infinity: report it
+        // (rows past the segment's end are never stored, and are not checked)
+        if (H16 && row0 + lane < row_end && !(amax < kF16RoundsToInf))
+          set_status(args.status, MOE_ERR_RANGE);
       } else {
         // One 32 x 32 fp32 block per chunk, staged in the 128-byte swizzled layout of the
         // output map (16-byte piece v of row r at piece v ^ (r mod 8): conflict-free) and
@@ -448,6 +478,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int c = 0; c < chunks; ++c) {
           uint32_t ar[32];
           tmem_ld32(taddr + c * 32, ar);
+          if constexpr (H16) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ar[i] = __float_as_uint(__uint_as_float(ar[i]) * out_mul);
+          }
           const int col0 = col_base + c * 32;
           if (lane == 0) bulk_wait_read_all();   // the previous block has been read out
           __syncwarp();
@@ -500,14 +534,14 @@ size_t pair_smem_bytes(int groups) {
          8 * (static_cast<size_t>(groups) + 1) + 64;
 }
 
-template <int MODE, bool GATHER, int KSUB>
+template <int MODE, bool GATHER, int KSUB, bool H16>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a64, const CUtensorMap& b0,
                         const CUtensorMap& b1, const CUtensorMap& b0h, const CUtensorMap& b1h,
                         const CUtensorMap& out, const PairArgs& args, int64_t max_pair_tiles,
                         cudaStream_t s) {
   if (max_pair_tiles <= 0) return cudaSuccess;
   const size_t smem = pair_smem_bytes(args.offsets ? args.groups : 1);
-  auto kern = tc_pair_gemm<MODE, GATHER, KSUB>;
+  auto kern = tc_pair_gemm<MODE, GATHER, KSUB, H16>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int64_t pairs_max = device_sm_count() >= 2 ? device_sm_count() / 2 : 1;
@@ -518,7 +552,8 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a64, const CUte
 
 }  // namespace
 
-cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
+template <bool H16>
+cudaError_t run_pair(const MlpParams& p, cudaStream_t s) {
   const bool dense = p.offsets == nullptr;
   const int64_t rows_cap = p.a_rows;
   if (rows_cap == 0 || (dense && p.dense_rows == 0)) return cudaSuccess;
@@ -535,9 +570,12 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
       !make_bf16_map(&mU, p.W_up, p.d, w_rows, 128) ||
       !make_bf16_map(&mG64, p.W_gate, p.d, w_rows, HM) ||
       !make_bf16_map(&mU64, p.W_up, p.d, w_rows, HM) ||
-      !make_bf16_map(&mH, p.h, p.width, rows_cap, BM) ||
-      !make_bf16_map(&mH64, p.h, p.width, rows_cap, HM) ||
-      !make_bf16_map(&mD, p.W_down, p.width, static_cast<uint64_t>(p.groups) * p.d, 128))
+      !(H16 ? make_f16_map(&mH, p.h, p.width, rows_cap, BM)
+            : make_bf16_map(&mH, p.h, p.width, rows_cap, BM)) ||
+      !(H16 ? make_f16_map(&mH64, p.h, p.width, rows_cap, HM)
+            : make_bf16_map(&mH64, p.h, p.width, rows_cap, HM)) ||
+      !(H16 ? make_f16_map(&mD, down_values(p), p.width, static_cast<uint64_t>(p.groups) * p.d, 128)
+            : make_bf16_map(&mD, p.W_down, p.width, static_cast<uint64_t>(p.groups) * p.d, 128)))
     return cudaErrorInvalidValue;
   if (gather) mA64 = mA;
 
@@ -550,6 +588,10 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.gather_src = p.gather_src;
   a.gather_cap = rows_cap;
   a.src_rows = p.src_rows;
+  a.h_scale = p.h_scale;
+  a.out_unscale = p.out_unscale;
+  a.down_hdr = H16 ? static_cast<const PackHeader*>(p.W_down) : nullptr;
+  a.down_elements = static_cast<int64_t>(p.groups) * p.d * p.width;
   // Two K blocks per ring stage when the average group has at least 512 rows (each
   // weight byte feeds enough rows for the tensor pipe to bound the launch); one
   // otherwise, and for gathered A rows.
@@ -562,9 +604,9 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   a.ldo = p.width;
   const int64_t gu_tiles = mt_ub * ((p.width + 127) / 128);
   cudaError_t e =
-      gather ? launch_pair<kSwiGLU, true, 1>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s)
-      : wide ? launch_pair<kSwiGLU, false, 2>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s)
-             : launch_pair<kSwiGLU, false, 1>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s);
+      gather ? launch_pair<kSwiGLU, true, 1, H16>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s)
+      : wide ? launch_pair<kSwiGLU, false, 2, H16>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s)
+             : launch_pair<kSwiGLU, false, 1, H16>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s);
   if (e != cudaSuccess) return e;
 
   a.k_dim = p.width;
@@ -576,8 +618,12 @@ cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
   const int64_t d_tiles = mt_ub * ((p.d + 255) / 256);
   CUtensorMap mF;
   if (!make_f32_map(&mF, p.out, p.d, rows_cap)) return cudaErrorInvalidValue;
-  return wide ? launch_pair<kPlain, false, 2>(mH, mH64, mD, mD, mD, mD, mF, a, d_tiles, s)
-              : launch_pair<kPlain, false, 1>(mH, mH64, mD, mD, mD, mD, mF, a, d_tiles, s);
+  return wide ? launch_pair<kPlain, false, 2, H16>(mH, mH64, mD, mD, mD, mD, mF, a, d_tiles, s)
+              : launch_pair<kPlain, false, 1, H16>(mH, mH64, mD, mD, mD, mD, mF, a, d_tiles, s);
+}
+
+cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s) {
+  return p.h_f16 ? run_pair<true>(p, s) : run_pair<false>(p, s);
 }
 
 }  // namespace moe

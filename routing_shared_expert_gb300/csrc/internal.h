@@ -129,10 +129,38 @@ struct MlpParams {
   const void* W_gate;         // [groups][width][d]
   const void* W_up;           // [groups][width][d]
   const void* W_down;         // [groups][d][width]
-  void* h;                    // [a_rows][width] intermediate (workspace), layer dtype
+  void* h;                    // [a_rows][width] intermediate (workspace), 2-byte elements
   float* out;                 // [a_rows][d] fp32
   int32_t* status;
+  // fp16 intermediate (MOE_H_F16): h is stored as fp16(h * h_scale) and W_down points at a
+  // packed buffer (PackHeader, then fp16 W * 2^k); f = accumulator * out_unscale * 2^-k.
+  bool h_f16;
+  float h_scale;              // 2^-h_scale_log2
+  float out_unscale;          // 2^h_scale_log2
 };
+
+// Header of a packed fp16 down-projection tensor (moe_pack_weights): the first
+// kPackHeaderBytes bytes of the buffer; elements fp16 values W * 2^k follow.
+struct PackHeader {
+  uint32_t magic;             // kPackMagic once the pack is complete
+  uint32_t absmax_bits;       // fp32 bits of max |W| (reduced by the pack)
+  int32_t k;                  // scale exponent: packed value = W * 2^k
+  float inv_scale;            // 2^-k
+  int64_t elements;
+  int32_t flags;              // kPackNonFinite: a weight was infinite or NaN
+};
+constexpr uint32_t kPackMagic = 0x3631444du;   // "MD16"
+constexpr int32_t kPackNonFinite = 1;
+constexpr size_t kPackHeaderBytes = 256;
+// Largest magnitude an fp16 intermediate may hold before rounding to infinity.
+constexpr float kF16RoundsToInf = 65520.f;
+
+cudaError_t launch_pack_f16(const void* W, int64_t elements, void* packed, cudaStream_t s);
+// The fp16 values of a packed down-projection tensor (after its header).
+inline const void* down_values(const struct MlpParams& p) {
+  return static_cast<const char*>(p.W_down) + kPackHeaderBytes;
+}
+bool make_f16_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 cudaError_t launch_mlp_bf16(const MlpParams& p, cudaStream_t s);        // 1-SM, 128-row tiles
 cudaError_t launch_mlp_bf16_pair(const MlpParams& p, cudaStream_t s);   // CTA pairs, 256-row tiles
 

@@ -12,8 +12,11 @@
 // library, for the life of the process.  In host code its name is only a
 // host-side stand-in for the symbol, so the host never passes it to a kernel:
 // the first call on each device looks up the array's device address with
-// cudaGetSymbolAddress (with that device current) and caches it.  That first
-// call should therefore come before any stream capture on that device.
+// cudaGetSymbolAddress (with that device current) and caches it together with
+// the device's current CUDA context.  That first call should therefore come
+// before any stream capture on that device.  A device reset replaces the
+// context (and may move the array): a call that finds another context looks the
+// address up again, so that call too should come before any stream capture.
 //
 // Every call on a device shares the array and leaves its last contents in it.
 // Nothing in it needs clearing: each call overwrites every histogram entry and
@@ -38,19 +41,46 @@ static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocPrefixInts + 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 int32_t* g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up once per device).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// The driver's cuCtxGetCurrent, found through the runtime (the library does not link the
+// driver library itself).
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Device address of the scratch array on the current device, looked up once per device
+// and context.
 cudaError_t scratch_on_current_device(int32_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get) return cudaErrorDeviceUninitialized;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (ctx == nullptr || g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
+    // the lookup binds the device's primary context to this thread if nothing has yet
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
     g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
   return cudaSuccess;
@@ -73,8 +103,9 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
   const moe_config& c = *cfg;
   const int64_t tiles = (c.T + kHistTile - 1) / kHistTile;
   if (tiles * c.N > kNoAllocHistInts) return MOE_ERR_UNSUPPORTED;   // beyond the static scratch
-  if (c.T > 0 && (!x || !topk_idx || !route_pos || !perm_src || !x_perm))
-    return MOE_ERR_INVALID_ARG;
+  // the same argument rules as moe_permute: x is needed only to fill x_perm
+  if (c.T > 0 && (!topk_idx || !route_pos || !perm_src)) return MOE_ERR_INVALID_ARG;
+  if (c.T > 0 && x_perm && !x) return MOE_ERR_INVALID_ARG;
   if (!counts_keep || !offsets) return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(x_perm) & 15u))
     return MOE_ERR_MISALIGNED;

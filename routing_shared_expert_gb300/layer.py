@@ -3,6 +3,9 @@
 Marshalling only.  ``forward`` is one ``moe_layer_forward`` call; ``forward_staged``
 runs the same five entry points one by one (optionally recording CUDA events
 between them on the launching stream, which is how per-kernel times are taken).
+With the fp16 intermediate (the default for bf16 layers) the down projections are
+packed once, at construction, by ``moe_pack_weights``; the backward pass reads the
+bf16 tensors as given.
 """
 from __future__ import annotations
 
@@ -13,15 +16,22 @@ import torch
 from . import _native as nat
 
 
-def config_from_spec(spec, T: Optional[int] = None) -> nat.moe_config:
-    """A ``moe_config`` from any object with the layer's fields (T, d_model, N, K, ...)."""
+def config_from_spec(spec, T: Optional[int] = None, h_format: Optional[str] = None,
+                     h_scale_log2: int = 0) -> nat.moe_config:
+    """A ``moe_config`` from any object with the layer's fields (T, d_model, N, K, ...).
+
+    ``h_format`` defaults to the spec's own field if it has one, else "f16" (the fp16
+    intermediate with packed down projections) for bf16 layers."""
+    if h_format is None:
+        h_format = getattr(spec, "h_format", None) or ("f16" if spec.dtype == "bf16" else "bf16")
     return nat.make_config(
         T=spec.T if T is None else T, d_model=spec.d_model, N=spec.N, K=spec.K,
         d_expert=spec.d_expert, d_shared=spec.d_shared, dtype=spec.dtype, score=spec.score,
         norm=spec.norm, alpha=spec.alpha, shared_mode=spec.shared_mode,
         shared_gain=spec.shared_gain, cap_policy=spec.cap_policy,
         capacity_factor=spec.capacity_factor, num_ranks=spec.num_ranks,
-        rho=[i % spec.num_ranks for i in range(spec.N)], norm_p=getattr(spec, "norm_p", 2.0))
+        rho=[i % spec.num_ranks for i in range(spec.N)], norm_p=getattr(spec, "norm_p", 2.0),
+        h_format=h_format, h_scale_log2=h_scale_log2)
 
 
 STAGES = ("route", "permute", "grouped_swiglu", "shared_mlp", "combine")
@@ -33,10 +43,13 @@ class MoELayer:
         self.cfg = cfg
         self.device = torch.device(device)
         self.weights = weights
-        self.w = nat.make_weights(weights["W_router"], weights.get("router_bias"),
-                                  weights.get("shared_gate_w"), weights["W_gate"], weights["W_up"],
-                                  weights["W_down"], weights.get("Ws_gate"), weights.get("Ws_up"),
-                                  weights.get("Ws_down"), weights.get("selection_bias"))
+        self.h_f16 = cfg.dtype == nat.DTYPES["bf16"] and cfg.h_format == nat.H_FORMATS["f16"]
+        # the down projections the forward reads: packed fp16 buffers for the fp16 intermediate
+        self.down = {"W_down": weights["W_down"], "Ws_down": weights.get("Ws_down")}
+        if self.h_f16:
+            self.down = {k: (nat.pack_weights(v) if v is not None else None)
+                         for k, v in self.down.items()}
+        self.w = self._weights(self.down)
         self.ws = nat.alloc_workspace(cfg, device)
         T, d, N, K, M = cfg.T, cfg.d_model, cfg.N, cfg.K, cfg.num_ranks
         i32 = dict(dtype=torch.int32, device=device)
@@ -65,6 +78,12 @@ class MoELayer:
                 "f": torch.empty((T * K, d), dtype=torch.float32, device=device),
                 "g": torch.empty((T, d), dtype=torch.float32, device=device) if cfg.d_shared > 0 else None,
             }
+
+    def _weights(self, down):
+        w = self.weights
+        return nat.make_weights(w["W_router"], w.get("router_bias"), w.get("shared_gate_w"),
+                                w["W_gate"], w["W_up"], down["W_down"], w.get("Ws_gate"),
+                                w.get("Ws_up"), down["Ws_down"], w.get("selection_bias"))
 
     def forward(self, x: torch.Tensor, stream=None, logits: bool = True) -> torch.Tensor:
         outs = self.outputs if logits else self._no_logits()
@@ -102,10 +121,11 @@ class MoELayer:
                         o["drop_stats"], self.ws, st)
         rec(2)
         nat.moe_grouped_swiglu(c, s["x_perm"], o["offsets"], None, w["W_gate"], w["W_up"],
-                               w["W_down"], s["f"], self.ws, st)
+                               self.down["W_down"], s["f"], self.ws, st)
         rec(3)
         if c.d_shared > 0:
-            nat.moe_shared_mlp(c, x, w["Ws_gate"], w["Ws_up"], w["Ws_down"], s["g"], self.ws, st)
+            nat.moe_shared_mlp(c, x, w["Ws_gate"], w["Ws_up"], self.down["Ws_down"], s["g"],
+                               self.ws, st)
         rec(4)
         nat.moe_combine(c, s["f"], o["route_pos"], o["topk_w"], s["g"],
                         o["shared_coef"] if c.d_shared > 0 else None, o["y"], st)
@@ -118,7 +138,12 @@ class MoELayer:
         forward call (which must have written the logits when ``router_grad``); returns dx
         and the weight gradients (fp32).  ``router_grad`` adds the gradient through the
         router coefficients (dW_router, and dshared_gate_w for a learned shared gate)."""
-        c = self.cfg
+        if not hasattr(self, "cfg_bwd"):
+            # the backward reads the bf16 down projections: a configuration that says so
+            self.cfg_bwd = nat.copy_config(self.cfg, h_format=nat.H_FORMATS["bf16"])
+            self.w_bwd = self._weights({"W_down": self.weights["W_down"],
+                                        "Ws_down": self.weights.get("Ws_down")})
+        c = self.cfg_bwd
         if getattr(self, "_bwd_router", None) != router_grad:
             self.bwd_ws = None
             self._bwd_router = router_grad
@@ -140,7 +165,7 @@ class MoELayer:
                 if c.shared_mode == nat.SHARED_MODES["gate"]:
                     self.grads["dshared_gate_w"] = torch.empty((d,), **f32)
             self.grads_c = nat.make_grads(**self.grads)
-        nat.moe_layer_backward(c, self.w, x, self.outputs, dy, self.grads_c, self.bwd_ws, stream)
+        nat.moe_layer_backward(c, self.w_bwd, x, self.outputs, dy, self.grads_c, self.bwd_ws, stream)
         return self.grads
 
     def backward_status(self) -> int:

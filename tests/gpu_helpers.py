@@ -11,9 +11,10 @@ ensure_built()
 TOL = {"f32": 1e-5, "bf16": 1.5e-2}
 
 
-def run_layer(spec, inp, staged=False):
+def run_layer(spec, inp, staged=False, h_format=None, h_scale_log2=0):
     import routing_shared_expert_gb300 as moe
-    layer = moe.MoELayer(moe.config_from_spec(spec), inp, "cuda")
+    cfg = moe.config_from_spec(spec, h_format=h_format, h_scale_log2=h_scale_log2)
+    layer = moe.MoELayer(cfg, inp, "cuda")
     if staged:
         layer.forward_staged(inp["x"])
     else:
@@ -99,3 +100,31 @@ ERRORS = []
 
 def record_error(case, err, bar):
     ERRORS.append((case, float(err), float(bar)))
+
+
+def emulated_y(spec, inp_host, rt, tokens, h_dtype):
+    """Eq. 80 in float64 with one rounding added where the device takes it: each expert's
+    intermediate h = SiLU(x W_g) * (x W_u) rounded to ``h_dtype`` (torch.bfloat16 or
+    torch.float16) before the down projection.  Checks the kernels' arithmetic, not the
+    method (the oracle does that)."""
+    x = torch.as_tensor(inp_host["x"])[torch.as_tensor(tokens)].double()
+
+    def expert(Wg, Wu, Wd, xr):
+        a = xr @ Wg.double().T
+        b = xr @ Wu.double().T
+        h = (a * torch.sigmoid(a) * b).to(h_dtype).double()
+        return (h @ Wd.double().T).numpy()
+
+    y = np.zeros((len(tokens), spec.d_model))
+    idx = rt.topk_idx[tokens]
+    kept = rt.route_pos[tokens] >= 0
+    r = rt.topk_w[tokens]
+    for e in np.unique(idx[kept]):
+        rows, slots = np.nonzero((idx == e) & kept)
+        y[rows] += r[rows, slots][:, None] * expert(inp_host["W_gate"][e], inp_host["W_up"][e],
+                                                    inp_host["W_down"][e], x[rows])
+    if spec.d_shared > 0:
+        s = O.shared_coefficient(x.numpy(), spec.shared_mode, spec.shared_gain,
+                                 inp_host.get("shared_gate_w"))
+        y += s[:, None] * expert(inp_host["Ws_gate"], inp_host["Ws_up"], inp_host["Ws_down"], x)
+    return y

@@ -98,13 +98,49 @@ def test_backward_rejects_unsupported_layers(nat):
         with pytest.raises(nat.MoEError) as e:
             nat.moe_backward_workspace_size(c)
         assert e.value.status == -2
-    assert nat.moe_backward_workspace_size(_olmo()) > nat.moe_workspace_size(_olmo())
+    # the backward reads bf16 down projections: a layer configured for packed fp16 ones is
+    # rejected, the same layer with the bf16 intermediate is accepted
+    with pytest.raises(nat.MoEError) as e:
+        nat.moe_backward_workspace_size(_olmo(h_format=1))
+    assert e.value.status == -2
+    assert nat.moe_backward_workspace_size(_olmo(h_format=0)) > nat.moe_workspace_size(_olmo())
+
+
+def test_intermediate_format_fields_validated(nat):
+    for kw in (dict(h_format=2), dict(h_format=-1), dict(h_scale_log2=65), dict(h_scale_log2=-65)):
+        with pytest.raises(nat.MoEError) as e:
+            nat.moe_workspace_size(_olmo(**kw))
+        assert e.value.status == -1
+    assert nat.moe_workspace_size(_olmo(h_format=1, h_scale_log2=-64)) > 0
+
+
+def test_pack_weights_size_and_argument_checks(nat):
+    import ctypes
+    lib = nat.library()
+    # a 256-byte header, then 2 bytes per element rounded up to 256 bytes
+    assert nat.moe_packed_weights_size(0) == 256
+    assert nat.moe_packed_weights_size(1) == 512
+    assert nat.moe_packed_weights_size(128) == 512
+    assert nat.moe_packed_weights_size(129) == 768
+    n = ctypes.c_size_t(0)
+    assert lib.moe_packed_weights_size(-1, ctypes.byref(n)) == -1
+    assert lib.moe_packed_weights_size(8, None) == -1
+    # null output, too small a buffer, misaligned pointers: rejected before anything is enqueued
+    assert lib.moe_pack_weights(ctypes.c_void_p(4096), 64, None, 512, None) == -1
+    assert lib.moe_pack_weights(ctypes.c_void_p(4096), 64, ctypes.c_void_p(1 << 20), 256, None) == -1
+    assert lib.moe_pack_weights(None, 64, ctypes.c_void_p(1 << 20), 512, None) == -1
+    assert lib.moe_pack_weights(ctypes.c_void_p(4096), 64, ctypes.c_void_p((1 << 20) + 16), 512,
+                                None) == -7
+    assert lib.moe_pack_weights(ctypes.c_void_p(4098), 64, ctypes.c_void_p(1 << 20), 512, None) == -7
+    # overlapping input and output
+    assert lib.moe_pack_weights(ctypes.c_void_p((1 << 20) + 256), 64, ctypes.c_void_p(1 << 20), 512,
+                                None) == -1
 
 
 def test_backward_rejects_null_arguments_before_cuda(nat):
     import ctypes
     lib = nat.library()
-    c = _olmo(T=64)
+    c = _olmo(T=64, h_format=0)
     n = nat.moe_backward_workspace_size(c)
     assert n > 0
     w = nat.moe_weights()

@@ -59,6 +59,10 @@ SMALL = {
     "dsv3_lp8": C["dsv3"].replace(T=400, d_model=448, d_expert=128, d_shared=128, norm="lp",
                                   norm_p=8.0),
     "tiny_lp3": C["tiny"].replace(norm="lp", norm_p=3.0),
+    # K between the selection-list lengths: K = 3 keeps a 4-entry list with a spare slot,
+    # K = 6 an 8-entry list with two
+    "olmo_k3": C["olmo"].replace(T=700, d_model=256, d_expert=128, d_shared=128, K=3, alpha=3.0),
+    "dsv3_k6": C["dsv3"].replace(T=500, d_model=448, d_expert=128, d_shared=128, K=6),
 }
 
 
@@ -113,9 +117,9 @@ def test_gathered_rows_equal_packed_rows(name):
     f_packed = torch.zeros((T * K, d), dtype=torch.float32, device="cuda")
     f_gather = torch.zeros((T * K, d), dtype=torch.float32, device="cuda")
     moe.moe_grouped_swiglu(c, x_perm, o["offsets"], None, inp["W_gate"], inp["W_up"],
-                           inp["W_down"], f_packed, layer.ws)
+                           layer.down["W_down"], f_packed, layer.ws)
     moe.moe_grouped_swiglu(c, inp["x"], o["offsets"], o["perm_src"], inp["W_gate"], inp["W_up"],
-                           inp["W_down"], f_gather, layer.ws)
+                           layer.down["W_down"], f_gather, layer.ws)
     torch.cuda.synchronize()
     kept = int(o["offsets"][-1])
     assert kept > 0

@@ -76,10 +76,41 @@ def test_permute_noalloc_matches_workspace_version_twice():
             assert int(got["drop_stats"][0]) > 0
 
 
+def test_permute_noalloc_at_the_size_limit_and_without_row_copy():
+    """ceil(T / 256) * N == 65536 exactly (T = 65536 at N = 256) uses the last histogram row of
+    the static array; the result equals moe_permute's bit for bit.  A second call without
+    x_perm (and without x: no rows copied, the expert GEMM can gather through perm_src)
+    gives the same routing tables."""
+    ensure_built()
+    import routing_shared_expert_gb300 as moe
+    spec = CONFIGS["dsv3"].replace(T=65536, d_model=64, d_expert=64, d_shared=64)
+    cfg = moe.config_from_spec(spec)
+    inp = make_inputs(spec, "cuda")
+    idx, ws = _route(moe, cfg, inp)
+    ref = _outputs(cfg, spec)
+    moe.moe_permute(cfg, inp["x"], idx, ref["counts_req"], ref["counts_keep"], ref["offsets"],
+                    ref["route_pos"], ref["perm_src"], ref["x_perm"], ref["R_req"], ref["R_keep"],
+                    ref["drop_stats"], ws)
+    got = _outputs(cfg, spec)
+    moe.moe_permute_noalloc(cfg, inp["x"], idx, got["counts_req"], got["counts_keep"],
+                            got["offsets"], got["route_pos"], got["perm_src"], got["x_perm"],
+                            got["R_req"], got["R_keep"], got["drop_stats"])
+    torch.cuda.synchronize()
+    assert _compare(ref, got) == spec.T * spec.K
+    bare = _outputs(cfg, spec)
+    moe.moe_permute_noalloc(cfg, None, idx, bare["counts_req"], bare["counts_keep"],
+                            bare["offsets"], bare["route_pos"], bare["perm_src"], None,
+                            bare["R_req"], bare["R_keep"], bare["drop_stats"])
+    torch.cuda.synchronize()
+    bare["x_perm"] = ref["x_perm"]
+    _compare(ref, bare)
+
+
 def test_permute_noalloc_rejects_layers_beyond_its_scratch():
     ensure_built()
     import routing_shared_expert_gb300 as moe
-    spec = CONFIGS["dsv3"].replace(T=65536 + 1)     # ceil(T / 256) * 256 experts > 65536
+    # one counting tile past the limit: ceil(T / 256) * 256 experts = 65792 > 65536
+    spec = CONFIGS["dsv3"].replace(T=65536 + 1)
     cfg = moe.config_from_spec(spec)
     with pytest.raises(moe.MoEError) as e:
         moe.moe_permute_noalloc(cfg, None, None, None, None, None, None, None, None, None, None,
