@@ -283,7 +283,8 @@ def sweep_entropy(args, spec):
     g = torch.Generator(device=dev)
     g.manual_seed(1)
     x_perm = torch.randn((R, spec.d_model), generator=g, device=dev).to(spec.torch_dtype)
-    f = torch.empty((R, spec.d_model), dtype=torch.float32, device=dev)
+    f = torch.empty((R, spec.d_model), dtype=torch.float16 if cfg.h_format == 1 else torch.float32,
+                    device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     flops = 6.0 * spec.d_model * spec.d_expert * R
     rows = []
@@ -315,10 +316,11 @@ def sweep_entropy(args, spec):
 
 def stage_algorithmic_bytes(spec, kept: int) -> int:
     """Bytes the grouped stage must move at least once: packed rows x_perm and the routed
-    weights (gate, up, down) read, h written and read, fp32 f written."""
+    weights (gate, up, down) read, h written and read, f written (fp16 for bf16 layers,
+    whose intermediate format is fp16; fp32 for fp32 layers)."""
     b = spec.elem_bytes
     d, dr, N = spec.d_model, spec.d_expert, spec.N
-    return int(kept * d * b + 3 * N * d * dr * b + 2 * kept * dr * b + kept * d * 4)
+    return int(kept * d * b + 3 * N * d * dr * b + 2 * kept * dr * b + kept * d * b)
 
 
 def launches_per_step(spec) -> int:
@@ -457,8 +459,8 @@ def workload_config(spec):
             "d_expert": spec.d_expert, "K": spec.K, "d_shared": spec.d_shared,
             "score": spec.score, "norm": spec.norm, "alpha": spec.alpha,
             "shared": spec.shared_mode, "capacity": spec.cap_policy,
-            "intermediate": ("h fp16, down projections packed to fp16 once (moe_pack_weights)"
-                             if spec.dtype == "bf16" else "fp32")}
+            "intermediate": ("h, f and g fp16; down projections packed to fp16 once "
+                             "(moe_pack_weights); fp32 accumulation" if spec.dtype == "bf16" else "fp32")}
 
 
 def main():

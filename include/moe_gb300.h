@@ -20,13 +20,13 @@
  *   at least moe_workspace_size() bytes, 256-byte aligned.
  * - Tensors are dense row-major.  Element type of activations and weights is
  *   cfg->dtype (fp32 or bf16).  Router logits, coefficients, the shared
- *   coefficient, the expert outputs f, the shared output g and y are fp32
- *   for every dtype (the bf16 path rounds only the expert inputs and the
- *   intermediate h, which feed the tensor cores).  Indices and counts are int32.
+ *   coefficient and y are fp32 for every dtype.  Indices and counts are int32.
  * - Intermediate format of bf16 layers (cfg->h_format, see moe_h_format): h is
- *   rounded to bf16 and multiplied by the bf16 down projections as given, or
- *   rounded to fp16 and multiplied by down projections packed to fp16 once by
- *   moe_pack_weights.
+ *   rounded to bf16 and multiplied by the bf16 down projections as given, with the
+ *   expert outputs f and the shared output g in fp32; or h is rounded to fp16 and
+ *   multiplied by down projections packed to fp16 once by moe_pack_weights, with f
+ *   and g in fp16 holding f 2^-h_scale_log2 and g 2^-h_scale_log2.  fp32 layers keep
+ *   h, f and g in fp32.
  * - Weight storage: W_router [N][d] (one row per expert, z = x W_router^T);
  *   W_gate, W_up [N][d_expert][d] (one row per intermediate unit, the columns
  *   of W_g / W_u of Eq. 74); W_down [N][d][d_expert] (one row per output
@@ -62,9 +62,10 @@ typedef enum {
   MOE_ERR_TIMEOUT = -5,            /* device status: a bounded wait inside a kernel ran out */
   MOE_ERR_DEVICE_BOUNDS = -6,      /* device status: a kernel saw an index out of range */
   MOE_ERR_MISALIGNED = -7,         /* a pointer is not 16-byte aligned */
-  MOE_ERR_RANGE = -8,              /* device status: an fp16 intermediate h left the fp16 range
-                                    * (|h| 2^-h_scale_log2 >= 65520), or a packed weight tensor
-                                    * held a non-finite value; the outputs are not valid */
+  MOE_ERR_RANGE = -8,              /* device status: a value of the fp16 intermediate format
+                                    * (h, f or g) left the fp16 range (|v| 2^-h_scale_log2 >=
+                                    * 65520), or a packed weight tensor held a non-finite
+                                    * value; the outputs are not valid */
   MOE_ERR_BAD_PACK = -9            /* device status: a down-projection pointer of an MOE_H_F16
                                     * call is not a complete moe_pack_weights buffer of the
                                     * layer's size */
@@ -108,10 +109,13 @@ typedef enum { MOE_CAP_NONE = 0, MOE_CAP_PER_EXPERT = 1, MOE_CAP_RANK_WIDE = 2 }
  *   MOE_H_F16   h 2^-h_scale_log2 rounded to fp16 (11 significant bits: eight times less
  *               rounding error, at the same tensor-core rate); W_down and Ws_down are
  *               buffers written by moe_pack_weights (fp16 copies scaled by a power of two,
- *               exact for bf16 weights).  |h| 2^-h_scale_log2 must stay below 65520: a
- *               larger value becomes an infinity and the call leaves MOE_ERR_RANGE in the
- *               status word (raise h_scale_log2, or use MOE_H_BF16).
- * The fp32 layers keep h in fp32 and ignore the field. */
+ *               exact for bf16 weights).  The expert outputs f and g go to the combine in
+ *               fp16 as f 2^-h_scale_log2 and g 2^-h_scale_log2 (half the bytes of fp32;
+ *               rounding error 2^-12 of each value).  |h|, |f| and |g| times
+ *               2^-h_scale_log2 must stay below 65520: a larger value becomes an infinity
+ *               and the call leaves MOE_ERR_RANGE in the status word (raise h_scale_log2,
+ *               or use MOE_H_BF16).
+ * The fp32 layers keep h, f and g in fp32 and ignore the field. */
 typedef enum { MOE_H_BF16 = 0, MOE_H_F16 = 1 } moe_h_format;
 
 typedef struct moe_config {
@@ -256,9 +260,10 @@ moe_status moe_pack_weights(const void* W, int64_t elements, void* packed, size_
  *                   needed.  Same results bit for bit; on a GB300 this form measured about
  *                   2.7x slower on bf16 layers (32 four-row TMA gathers per K step), so
  *                   moe_layer_forward uses the packed form.
- * Out: f [K*T][d] fp32: f[row] = SwiGLU_e(packed row) for rows < offsets[N].
- * The intermediate h = SiLU(x W_g) * (x W_u) is kept in the workspace (bf16 or fp16 per
- * cfg->h_format; W_down is a moe_pack_weights buffer under MOE_H_F16). */
+ * Out: f [K*T][d]: f[row] = SwiGLU_e(packed row) for rows < offsets[N], fp32 (fp16 holding
+ * f 2^-h_scale_log2 under MOE_H_F16).  The intermediate h = SiLU(x W_g) * (x W_u) is kept
+ * in the workspace (bf16 or fp16 per cfg->h_format; W_down is a moe_pack_weights buffer
+ * under MOE_H_F16). */
 moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_rows, const int32_t* offsets,
                               const int32_t* perm_src, const void* W_gate, const void* W_up,
                               const void* W_down, void* f, void* workspace,
@@ -267,15 +272,18 @@ moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_rows, const i
 /* The one (merged) shared expert over all tokens (Section 20.1, Eq. 74-76).
  *   x [T][d]; Ws_gate, Ws_up [d_shared][d]; Ws_down [d][d_shared] (a moe_pack_weights
  *   buffer under MOE_H_F16).
- * Out: g [T][d] fp32.  Requires d_shared > 0. */
+ * Out: g [T][d] fp32 (fp16 holding g 2^-h_scale_log2 under MOE_H_F16).  Requires
+ * d_shared > 0. */
 moe_status moe_shared_mlp(const moe_config* cfg, const void* x, const void* Ws_gate,
                           const void* Ws_up, const void* Ws_down, void* g,
                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Weighted combine, Eq. 80: y_t = sum_{k: route_pos[t][k] >= 0} topk_w[t][k] * f[route_pos[t][k]]
  *   + shared_coef[t] * g_t, accumulated in fp32 in slot order, then the shared term.
- *   f [K*T][d] fp32; route_pos, topk_w [T][K]; g [T][d] fp32 and shared_coef [T] may both be NULL
- *   (no shared term).  Out: y [T][d] fp32.  Dropped routes add nothing and the kept
+ *   f [K*T][d] and g [T][d] as moe_grouped_swiglu / moe_shared_mlp write them (fp32, or fp16
+ *   holding f 2^-h_scale_log2 under MOE_H_F16: the combine multiplies the coefficients by
+ *   2^h_scale_log2); route_pos, topk_w [T][K]; g and shared_coef [T] may both be NULL (no
+ *   shared term).  Out: y [T][d] fp32.  Dropped routes add nothing and the kept
  *   coefficients are not renormalised. */
 moe_status moe_combine(const moe_config* cfg, const void* f, const int32_t* route_pos,
                        const float* topk_w, const void* g, const float* shared_coef, float* y,

@@ -150,9 +150,8 @@ moe_status do_permute(const moe_config& c, const Layout& L, void* ws, const void
 
 // The intermediate format of a bf16 layer's expert GEMMs (moe_h_format).
 void set_h_format(const moe_config& c, MlpParams* p) {
-  p->h_f16 = c.dtype == MOE_BF16 && c.h_format == MOE_H_F16;
+  p->h_f16 = h_f16(c);
   p->h_scale = std::ldexp(1.0f, -c.h_scale_log2);
-  p->out_unscale = std::ldexp(1.0f, c.h_scale_log2);
 }
 
 moe_status do_grouped(const moe_config& c, const Layout& L, void* ws, const void* x_rows,
@@ -184,7 +183,7 @@ moe_status do_grouped(const moe_config& c, const Layout& L, void* ws, const void
   p.W_up = Wu;
   p.W_down = Wd;
   p.h = at<void>(ws, L.h);
-  p.out = static_cast<float*>(f);
+  p.out = f;
   p.status = status;
   set_h_format(c, &p);
   if (c.dtype == MOE_F32) return cuda_status(launch_mlp_f32(p, st));
@@ -212,7 +211,7 @@ moe_status do_shared(const moe_config& c, const Layout& L, void* ws, const void*
   p.W_up = Wu;
   p.W_down = Wd;
   p.h = at<void>(ws, L.hs);
-  p.out = static_cast<float*>(g);
+  p.out = g;
   p.status = at<int32_t>(ws, L.status);
   set_h_format(c, &p);
   if (c.dtype == MOE_F32) return cuda_status(launch_mlp_f32(p, st));
@@ -228,6 +227,8 @@ moe_status do_combine(const moe_config& c, const void* f, const int32_t* route_p
   if (!aligned16(f) || !aligned16(y) || (g && !aligned16(g))) return MOE_ERR_MISALIGNED;
   CombineParams p{};
   p.f = f;
+  p.f16 = h_f16(c);
+  p.out_scale = std::ldexp(1.0f, c.h_scale_log2);
   p.route_pos = route_pos;
   p.topk_w = topk_w;
   p.g = g;
@@ -282,9 +283,9 @@ Layout make_layout(const moe_config& c) {
   L.score_partial = take(static_cast<size_t>(L.hist_tiles) * N * 4);
   L.x_perm = take(T * K * d * eb);
   L.h = take(T * K * dr * eb);
-  L.f = take(T * K * d * 4);
+  L.f = take(T * K * d * out_bytes(c));
   L.hs = take(T * ds * eb);
-  L.g = take(T * d * 4);
+  L.g = take(T * d * out_bytes(c));
   L.total = o;
   return L;
 }

@@ -3,8 +3,10 @@
 // Dropped routes add nothing and the kept coefficients are not renormalised
 // (Section 10.3: combine masks the tail-dropped routes).
 //
-// f and g are fp32 for every layer dtype (rounding them to bf16 would cost about
-// 2^-9 of the largest |f| per element, most of a 1.5e-2 relative budget).
+// f and g are fp32, or fp16 under the fp16 intermediate of bf16 layers, where they hold
+// f 2^-h_scale_log2 (the scale is folded into the coefficients here: exact, a power of
+// two).  Rounding them to bf16 instead would cost about 2^-9 of the largest |f| per
+// element, most of a 1.5e-2 relative budget; fp16 costs 2^-12.
 // One CTA per token; each thread owns 16 bytes of a row (4 fp32) and
 // accumulates in fp32 in a fixed order (slot 0..K-1, then the shared term), so
 // the result does not depend on scheduling.  Loads and stores are 16-byte vectors;
@@ -28,6 +30,21 @@ struct Vec<__nv_bfloat16> {
     for (int i = 0; i < 4; ++i) {
       __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
       const float2 f = __bfloat1622float2(b);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+};
+template <>
+struct Vec<__half> {
+  static constexpr int N = 8;
+  __device__ static void load(const __half* p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 b = *reinterpret_cast<const __half2*>(&w[i]);
+      const float2 f = __half22float2(b);
       v[2 * i] = f.x;
       v[2 * i + 1] = f.y;
     }
@@ -59,12 +76,12 @@ __global__ void __launch_bounds__(1024) combine_kernel(CombineParams p) {
       pos = -1;
     }
     s_pos[threadIdx.x] = pos;
-    s_w[threadIdx.x] = p.topk_w[t * p.K + threadIdx.x];
+    s_w[threadIdx.x] = p.topk_w[t * p.K + threadIdx.x] * p.out_scale;
   }
   __syncthreads();
   const T* f = static_cast<const T*>(p.f);
   const T* g = static_cast<const T*>(p.g);
-  const float s = (g != nullptr && p.shared_coef != nullptr) ? p.shared_coef[t] : 0.f;
+  const float s = (g != nullptr && p.shared_coef != nullptr) ? p.shared_coef[t] * p.out_scale : 0.f;
   for (int c = threadIdx.x * V; c < p.d; c += blockDim.x * V) {
     for (int k = 0; k < p.K; ++k)
       if (s_pos[k] >= 0) prefetch_l2(f + static_cast<int64_t>(s_pos[k]) * p.d + c);
@@ -108,7 +125,7 @@ cudaError_t launch_t(const CombineParams& p, cudaStream_t s) {
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   if (p.T == 0) return cudaSuccess;
-  return launch_t<float>(p, s);
+  return p.f16 ? launch_t<__half>(p, s) : launch_t<float>(p, s);
 }
 
 }  // namespace moe

@@ -167,7 +167,7 @@ cudaError_t launch_mlp_f32(const MlpParams& p, cudaStream_t s) {
   a.n_out = p.d;
   a.B0 = static_cast<const float*>(p.W_down);
   a.B1 = nullptr;
-  a.out = p.out;
+  a.out = static_cast<float*>(p.out);   // fp32 layers: fp32 outputs
   dim3 g2((p.d + CB - 1) / CB, static_cast<unsigned>(rb_ub));
   f32_mlp_kernel<false><<<g2, THREADS, 0, s>>>(a);
   return cudaGetLastError();

@@ -61,9 +61,8 @@ struct TcArgs {
   int64_t gather_cap;
   int64_t src_rows;
   // fp16 intermediate: SwiGLU mode stores fp16(h * h_scale); plain mode reads the packed
-  // weights' header and writes accumulator * out_unscale * 2^-k
+  // weights' header and writes fp16(accumulator * 2^-k)
   float h_scale;
-  float out_unscale;
   const PackHeader* down_hdr;
   int64_t down_elements;
 };
@@ -289,11 +288,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quarter this warp may access
-    // plain mode of the fp16 intermediate: the packed weights' scale, checked once
+    // plain mode of the fp16 intermediate: the packed weights' scale, checked once; the
+    // output holds f 2^-h_scale_log2 = accumulator 2^-k in fp16
     float out_mul = 1.f;
     if (H16 && !SWIGLU) {
       const PackHeader* hd = args.down_hdr;
-      out_mul = args.out_unscale * hd->inv_scale;
+      out_mul = hd->inv_scale;
       if (lane == 0 && (hd->magic != kPackMagic || hd->elements != args.down_elements))
         set_status(args.status, MOE_ERR_BAD_PACK);
       if (lane == 0 && (hd->flags & kPackNonFinite)) set_status(args.status, MOE_ERR_RANGE);
@@ -347,20 +347,38 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       } else {
-        // plain mode: fp32 output rows (the expert outputs f stay in fp32 up to the combine)
+        // plain mode: output rows, fp32 (or fp16 of the fp16 intermediate, where they hold
+        // f 2^-h_scale_log2)
         float* out_f = static_cast<float*>(args.out) + (valid ? row : 0) * args.ldo;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t ar[32], br[32];
           tmem_ld32x2(taddr + c * 64, taddr + c * 64 + 32, ar, br);
-          if constexpr (H16) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              ar[i] = __float_as_uint(__uint_as_float(ar[i]) * out_mul);
-              br[i] = __float_as_uint(__uint_as_float(br[i]) * out_mul);
-            }
-          }
           const int col0 = tl.n * 256 + c * 64;
+          if constexpr (H16) {
+            if (valid) {
+              uint16_t* orow = static_cast<uint16_t*>(args.out) + row * args.ldo;
+              float m = 0.f;
+              uint32_t pk[32];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float a0 = __uint_as_float(ar[2 * i]) * out_mul;
+                const float a1 = __uint_as_float(ar[2 * i + 1]) * out_mul;
+                const float b0 = __uint_as_float(br[2 * i]) * out_mul;
+                const float b1 = __uint_as_float(br[2 * i + 1]) * out_mul;
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))));
+                pk[i] = pack_f16x2(a0, a1);
+                pk[16 + i] = pack_f16x2(b0, b1);
+              }
+              if (!(m < kF16RoundsToInf)) set_status(args.status, MOE_ERR_RANGE);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                if (col0 + v * 8 + 8 <= args.n_out)
+                  *reinterpret_cast<uint4*>(orow + col0 + v * 8) =
+                      make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+            continue;
+          }
           if (valid) {
 #pragma unroll
             for (int v = 0; v < 8; ++v)
@@ -504,6 +522,13 @@ bool make_f16_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t row
                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// fp16 [rows][inner], box 32 x 32 (64-byte rows), 64-byte swizzle: the fp16 output blocks
+// (expert outputs of the fp16 intermediate) the expert GEMM epilogues store with TMA.
+bool make_f16_store_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows) {
+  return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, inner, rows, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 // fp32 [rows][inner], box 32 x 32 (128-byte rows), 128-byte swizzle: the output blocks the
 // expert GEMM epilogues store with TMA.
 bool make_f32_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows) {
@@ -588,7 +613,6 @@ cudaError_t run_one(const MlpParams& p, cudaStream_t s) {
   a.gather_cap = rows_cap;
   a.src_rows = p.src_rows;
   a.h_scale = p.h_scale;
-  a.out_unscale = p.out_unscale;
   a.down_hdr = H16 ? static_cast<const PackHeader*>(p.W_down) : nullptr;
   a.down_elements = static_cast<int64_t>(p.groups) * p.d * p.width;
 

@@ -81,9 +81,8 @@ struct PairArgs {
   int64_t gather_cap;        // entries of gather_src
   int64_t src_rows;          // rows of x
   // fp16 intermediate: SwiGLU mode stores fp16(h * h_scale); plain mode reads the packed
-  // weights' header and writes accumulator * out_unscale * 2^-k
+  // weights' header and writes fp16(accumulator * 2^-k)
   float h_scale;
-  float out_unscale;
   const PackHeader* down_hdr;
   int64_t down_elements;     // elements the packed tensor must hold
 };
@@ -386,11 +385,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
     uint32_t* stg = epi + (warp - 2) * EPI_WARP_WORDS;
-    // plain mode of the fp16 intermediate: the packed weights' scale, checked once
+    // plain mode of the fp16 intermediate: the packed weights' scale, checked once; the
+    // output holds f 2^-h_scale_log2 = accumulator 2^-k in fp16
     float out_mul = 1.f;
     if (H16 && !SWIGLU) {
       const PackHeader* hd = args.down_hdr;
-      out_mul = args.out_unscale * hd->inv_scale;
+      out_mul = hd->inv_scale;
       if (lane == 0 && (hd->magic != kPackMagic || hd->elements != args.down_elements))
         set_status(args.status, MOE_ERR_BAD_PACK);
       if (lane == 0 && (hd->flags & kPackNonFinite)) set_status(args.status, MOE_ERR_RANGE);
@@ -478,11 +478,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int c = 0; c < chunks; ++c) {
           uint32_t ar[32];
           tmem_ld32(taddr + c * 32, ar);
-          if constexpr (H16) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ar[i] = __float_as_uint(__uint_as_float(ar[i]) * out_mul);
-          }
           const int col0 = col_base + c * 32;
+          if constexpr (H16) {
+            // fp16 32 x 32 block, staged in the 64-byte swizzled layout of the output map
+            // (16-byte piece v of row r at piece v ^ ((r / 2) mod 4)) and written by one TMA
+            // store inside the segment and the width; else each lane stores its own row
+            uint32_t pk[16];
+            float m = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float v0 = __uint_as_float(ar[2 * i]) * out_mul;
+              const float v1 = __uint_as_float(ar[2 * i + 1]) * out_mul;
+              m = fmaxf(m, fmaxf(fabsf(v0), fabsf(v1)));
+              pk[i] = pack_f16x2(v0, v1);
+            }
+            const int64_t row = row0 + lane;
+            if (row < row_end && !(m < kF16RoundsToInf)) set_status(args.status, MOE_ERR_RANGE);
+            if (rows_in && col0 + 32 <= args.n_out) {
+              if (lane == 0) bulk_wait_read_all();   // the previous block has been read out
+              __syncwarp();
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                *reinterpret_cast<uint4*>(blk + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16)) =
+                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmOut, col0, static_cast<int32_t>(row0), smem_u32(blk));
+                bulk_commit();
+              }
+            } else if (row < row_end) {
+              uint16_t* orow = static_cast<uint16_t*>(args.out) + row * args.ldo;
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                if (col0 + 8 * v + 8 <= args.n_out)
+                  __stcs(reinterpret_cast<uint4*>(orow + col0 + 8 * v),
+                         make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]));
+            }
+            continue;
+          }
           if (lane == 0) bulk_wait_read_all();   // the previous block has been read out
           __syncwarp();
 #pragma unroll
@@ -589,7 +623,6 @@ cudaError_t run_pair(const MlpParams& p, cudaStream_t s) {
   a.gather_cap = rows_cap;
   a.src_rows = p.src_rows;
   a.h_scale = p.h_scale;
-  a.out_unscale = p.out_unscale;
   a.down_hdr = H16 ? static_cast<const PackHeader*>(p.W_down) : nullptr;
   a.down_elements = static_cast<int64_t>(p.groups) * p.d * p.width;
   // Two K blocks per ring stage when the average group has at least 512 rows (each
@@ -617,7 +650,8 @@ cudaError_t run_pair(const MlpParams& p, cudaStream_t s) {
   a.gather_src = nullptr;    // h is packed
   const int64_t d_tiles = mt_ub * ((p.d + 255) / 256);
   CUtensorMap mF;
-  if (!make_f32_map(&mF, p.out, p.d, rows_cap)) return cudaErrorInvalidValue;
+  if (!(H16 ? make_f16_store_map(&mF, p.out, p.d, rows_cap) : make_f32_map(&mF, p.out, p.d, rows_cap)))
+    return cudaErrorInvalidValue;
   return wide ? launch_pair<kPlain, false, 2, H16>(mH, mH64, mD, mD, mD, mD, mF, a, d_tiles, s)
               : launch_pair<kPlain, false, 1, H16>(mH, mH64, mD, mD, mD, mD, mF, a, d_tiles, s);
 }

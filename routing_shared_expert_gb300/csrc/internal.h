@@ -33,6 +33,11 @@ Layout make_layout(const moe_config& c);
 int32_t capacity_budget(const moe_config& c);
 
 inline size_t elem_bytes(const moe_config& c) { return c.dtype == MOE_F32 ? 4 : 2; }
+// The fp16 intermediate format of a bf16 layer (MOE_H_F16): h, f and g are fp16.
+inline bool h_f16(const moe_config& c) { return c.dtype == MOE_BF16 && c.h_format == MOE_H_F16; }
+// Bytes of one element of the expert outputs f and g: fp16 (holding f 2^-h_scale_log2)
+// under the fp16 intermediate, fp32 otherwise.
+inline size_t out_bytes(const moe_config& c) { return h_f16(c) ? 2 : 4; }
 
 // ---- routing -----------------------------------------------------------------
 struct RouteParams {
@@ -60,6 +65,7 @@ cudaError_t launch_route_tc(const RouteParams& p, cudaStream_t s);
 bool make_bf16_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 bool make_f32_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows);
 bool make_bf16_store_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows);
+bool make_f16_store_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows);
 
 // Raise a kernel's dynamic shared-memory limit once per device (host-side cache).
 cudaError_t set_smem_once(const void* func, size_t bytes);
@@ -99,7 +105,9 @@ cudaError_t launch_tile_prefix(const int32_t* offsets, int32_t N, int32_t* tile_
 
 // ---- combine -------------------------------------------------------------------
 struct CombineParams {
-  const void* f;
+  const void* f;              // fp32, or fp16 holding f 2^-out_log2 (f16 set); g likewise
+  bool f16;
+  float out_scale;            // 2^out_log2: multiplies the fp16 f and g
   const int32_t* route_pos;
   const float* topk_w;
   const void* g;
@@ -130,13 +138,13 @@ struct MlpParams {
   const void* W_up;           // [groups][width][d]
   const void* W_down;         // [groups][d][width]
   void* h;                    // [a_rows][width] intermediate (workspace), 2-byte elements
-  float* out;                 // [a_rows][d] fp32
+  void* out;                  // [a_rows][d] fp32, or fp16 holding out 2^-h_scale_log2 (h_f16)
   int32_t* status;
-  // fp16 intermediate (MOE_H_F16): h is stored as fp16(h * h_scale) and W_down points at a
-  // packed buffer (PackHeader, then fp16 W * 2^k); f = accumulator * out_unscale * 2^-k.
+  // fp16 intermediate (MOE_H_F16): h is stored as fp16(h * h_scale), W_down points at a
+  // packed buffer (PackHeader, then fp16 W * 2^k) and out holds fp16(accumulator * 2^-k),
+  // which is the output times h_scale.
   bool h_f16;
   float h_scale;              // 2^-h_scale_log2
-  float out_unscale;          // 2^h_scale_log2
 };
 
 // Header of a packed fp16 down-projection tensor (moe_pack_weights): the first

@@ -73,10 +73,12 @@ class MoELayer:
         self.staged = None
         if staged_buffers:
             dt = torch.float32 if cfg.dtype == nat.DTYPES["f32"] else torch.bfloat16
+            # expert outputs: fp16 (holding f 2^-h_scale_log2) under the fp16 intermediate
+            ft = torch.float16 if self.h_f16 else torch.float32
             self.staged = {
                 "x_perm": torch.empty((T * K, d), dtype=dt, device=device),
-                "f": torch.empty((T * K, d), dtype=torch.float32, device=device),
-                "g": torch.empty((T, d), dtype=torch.float32, device=device) if cfg.d_shared > 0 else None,
+                "f": torch.empty((T * K, d), dtype=ft, device=device),
+                "g": torch.empty((T, d), dtype=ft, device=device) if cfg.d_shared > 0 else None,
             }
 
     def _weights(self, down):

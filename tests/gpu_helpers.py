@@ -102,18 +102,22 @@ def record_error(case, err, bar):
     ERRORS.append((case, float(err), float(bar)))
 
 
-def emulated_y(spec, inp_host, rt, tokens, h_dtype):
-    """Eq. 80 in float64 with one rounding added where the device takes it: each expert's
-    intermediate h = SiLU(x W_g) * (x W_u) rounded to ``h_dtype`` (torch.bfloat16 or
-    torch.float16) before the down projection.  Checks the kernels' arithmetic, not the
-    method (the oracle does that)."""
+def emulated_y(spec, inp_host, rt, tokens, h_dtype, out_dtype=None):
+    """Eq. 80 in float64 with the roundings the device takes: each expert's intermediate
+    h = SiLU(x W_g) * (x W_u) rounded to ``h_dtype`` (torch.bfloat16 or torch.float16)
+    before the down projection, and, with ``out_dtype``, each expert's output f and the
+    shared output g rounded to it before the merge.  Checks the kernels' arithmetic, not
+    the method (the oracle does that)."""
     x = torch.as_tensor(inp_host["x"])[torch.as_tensor(tokens)].double()
 
     def expert(Wg, Wu, Wd, xr):
         a = xr @ Wg.double().T
         b = xr @ Wu.double().T
         h = (a * torch.sigmoid(a) * b).to(h_dtype).double()
-        return (h @ Wd.double().T).numpy()
+        f = h @ Wd.double().T
+        if out_dtype is not None:
+            f = f.to(out_dtype).double()
+        return f.numpy()
 
     y = np.zeros((len(tokens), spec.d_model))
     idx = rt.topk_idx[tokens]

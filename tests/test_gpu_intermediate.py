@@ -2,8 +2,9 @@
 
 The down projection f = h W_d (Section 20, Eq. 74) multiplies the intermediate h by
 the down weights on the tensor cores, both in one 16-bit type.  MOE_H_F16 (the default
-of the layer holder) keeps h in fp16 and reads W_d from a buffer moe_pack_weights wrote
-once (fp16 W 2^k); MOE_H_BF16 keeps h in bf16 and reads W_d as given.
+of the layer holder) keeps h in fp16, reads W_d from a buffer moe_pack_weights wrote
+once (fp16 W 2^k) and hands the expert outputs f and g to the combine in fp16;
+MOE_H_BF16 keeps h in bf16, reads W_d as given and keeps f and g in fp32.
 
 - The packing is exact for bf16 weights: packed * 2^-k equals W bit for bit, for
   ordinary, tiny, huge and ragged tensors; a non-finite weight is flagged.
@@ -94,12 +95,13 @@ def test_pack_of_zeros_and_flags_of_non_finite_weights():
 @pytest.mark.parametrize("name", BF16_CASES)
 @pytest.mark.parametrize("fmt", ["f16", "bf16"])
 def test_kernels_follow_their_rounding(name, fmt):
-    """y of each format against Eq. 80 in float64 with h rounded to that format, by the rms
-    of the difference relative to rms(y).  The device forms h in fp32 (relative error about
-    2e-6), so about 2e-6 / ulp of h elements round the other way than in the emulation, each
-    by one ulp: an rms difference of about 2e-4 for bf16 h and 7e-5 for fp16 h.  The bars
-    sit well below what rounding h to the other format would give (1.6e-3 from bf16
-    rounding, 2e-4 from fp16)."""
+    """y of each format against Eq. 80 in float64 with h rounded to that format (and, for
+    fp16, the expert outputs f and g as well), by the rms of the difference relative to
+    rms(y).  The device forms h and f in fp32 (relative error about 2e-6), so about
+    2e-6 / ulp of the h elements (and, for fp16, of f and g) round the other way than in the
+    emulation, each by one ulp: an rms difference of about 2e-4 for bf16 h, and 1-2e-4
+    measured for fp16 h, f and g.  The bars sit well below what rounding h to bf16 would
+    give in the fp16 format (1.6e-3)."""
     spec = SMALL[name]
     inp = make_inputs(spec, "cuda")
     layer = run_layer(spec, inp, h_format=fmt)
@@ -108,9 +110,10 @@ def test_kernels_follow_their_rounding(name, fmt):
     rt = check_routing_exact(layer, spec)
     tokens = np.arange(spec.T)
     y = layer.out["y"].cpu().double().numpy()
-    y_emu = emulated_y(spec, hin, rt, tokens, torch.float16 if fmt == "f16" else torch.bfloat16)
+    y_emu = (emulated_y(spec, hin, rt, tokens, torch.float16, torch.float16) if fmt == "f16"
+             else emulated_y(spec, hin, rt, tokens, torch.bfloat16))
     err_emu = float(np.sqrt(((y - y_emu) ** 2).mean() / (y_emu ** 2).mean()))
-    bar = 1.5e-4 if fmt == "f16" else 6e-4
+    bar = 4e-4 if fmt == "f16" else 6e-4
     assert err_emu <= bar, f"{name} {fmt}: rms difference from its own rounding {err_emu:.3e}"
     if fmt == "bf16":
         # the optional bf16 intermediate against the oracle, reported beside the bar

@@ -114,8 +114,9 @@ def test_gathered_rows_equal_packed_rows(name):
     x_perm = torch.zeros((T * K, d), dtype=spec.torch_dtype, device="cuda")
     moe.moe_permute(c, inp["x"], o["topk_idx"], None, o["counts_keep"], o["offsets"],
                     o["route_pos"], o["perm_src"], x_perm, None, None, None, layer.ws)
-    f_packed = torch.zeros((T * K, d), dtype=torch.float32, device="cuda")
-    f_gather = torch.zeros((T * K, d), dtype=torch.float32, device="cuda")
+    ft = layer.staged["f"].dtype
+    f_packed = torch.zeros((T * K, d), dtype=ft, device="cuda")
+    f_gather = torch.zeros((T * K, d), dtype=ft, device="cuda")
     moe.moe_grouped_swiglu(c, x_perm, o["offsets"], None, inp["W_gate"], inp["W_up"],
                            layer.down["W_down"], f_packed, layer.ws)
     moe.moe_grouped_swiglu(c, inp["x"], o["offsets"], o["perm_src"], inp["W_gate"], inp["W_up"],
