@@ -410,7 +410,9 @@ moe_status moe_check_wait_bound(void* workspace, size_t workspace_bytes, int64_t
                                 cudaStream_t stream);
 
 /* Read and clear the device status word of a workspace.  Synchronises the stream and copies
- * 4 bytes to the host.  *code (host) receives MOE_OK or the first device-detected error. */
+ * 4 bytes to the host.  *code (host) receives MOE_OK or the first device-detected error.  The
+ * whole 256-byte header of the workspace is reset (as by moe_workspace_init), so a workspace
+ * is ready for the next call after any device-detected error. */
 moe_status moe_read_status(void* workspace, int32_t* code, cudaStream_t stream);
 
 #ifdef __cplusplus

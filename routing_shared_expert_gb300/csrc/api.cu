@@ -145,6 +145,7 @@ moe_status do_permute(const moe_config& c, const Layout& L, void* ws, const void
   p.R_keep = o.R_keep;
   p.drop_stats = o.drops;
   p.status = at<int32_t>(ws, L.status);
+  p.barrier = at<unsigned>(ws, L.status + kBarrierOffset);
   return cuda_status(launch_permute(p, st));
 }
 
@@ -927,7 +928,9 @@ moe_status moe_read_status(void* workspace, int32_t* code, cudaStream_t stream) 
   int32_t host = 0;
   cudaError_t e = cudaMemcpyAsync(&host, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream);
+  // the stream is idle: clear the whole header (the status word and the permutation's
+  // grid-barrier words, which a barrier that ran out may have left set)
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, 256, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   *code = host;

@@ -96,7 +96,12 @@ struct PermuteParams {
   int32_t* R_keep;
   int32_t* drop_stats;
   int32_t* status;
+  // Grid-barrier words of the one-launch permutation (count, then generation, on separate
+  // 64-byte lines of the workspace header, zero after moe_workspace_init); nullptr: the
+  // launch-per-step permutation.
+  unsigned* barrier;
 };
+constexpr size_t kBarrierOffset = 64;   // bytes into the workspace header
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s);
 
 // m-tile prefix of packed segments: tile_prefix[e] = sum_{i<e} ceil((offsets[i+1]-offsets[i]) / 128).
