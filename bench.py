@@ -323,11 +323,13 @@ def stage_algorithmic_bytes(spec, kept: int) -> int:
     return int(kept * d * b + 3 * N * d * dr * b + 2 * kept * dr * b + kept * d * b)
 
 
-def launches_per_step(spec) -> int:
+def launches_per_step(spec, sms: int = 152) -> int:
     """Kernels moe_layer_forward launches for a layer (counted from the library's launch
-    sequence): router 1; permutation 4 (count, scan, place, row copy); routed experts 2;
-    shared expert 2 or 0; combine 1."""
-    return 1 + 4 + 2 + (2 if spec.d_shared > 0 else 0) + 1
+    sequence): router 1; permutation 2 (counting, capacity and placement in one launch while
+    the 256-token tiles fit on the GPU at once, which holds here for up to one tile per SM,
+    else 3; then the row copy); routed experts 2; shared expert 2 or 0; combine 1."""
+    permute = 2 if (spec.T + 255) // 256 <= sms else 4
+    return 1 + permute + 2 + (2 if spec.d_shared > 0 else 0) + 1
 
 
 # ----------------------------------------------------------------- backward
@@ -671,7 +673,8 @@ def main():
                      "traffic_unit": "bytes per stage (gate/up + down launches)",
                      "algorithmic_bytes": stage_algorithmic_bytes(spec, kept)},
         "e2e": e2e,
-        "gpu_launches": launches_per_step(spec) * args.steps,
+        "gpu_launches": launches_per_step(
+            spec, torch.cuda.get_device_properties(dev).multi_processor_count) * args.steps,
         "clocks": head_clocks,
         "kept_routes": kept,
         "per_config": per_config,
