@@ -54,18 +54,36 @@ __device__ __forceinline__ void route_one_token(const RouteParams& p, const floa
           if (c0 + i < p.N) lrow[c0 + i] = z[i];
       }
     }
+    // Candidates that beat the list's last key as it stands at the start of the chunk:
+    // a mask built without branches.  Only those are then inserted, in ascending expert
+    // index (a later candidate with an equal key never displaces an earlier one), each
+    // checked again against the last key, which rises as the list fills.  The tokens of a
+    // warp insert at different candidates, so a branch per candidate would run the
+    // insertion for nearly every candidate of the warp; the mask loop runs as often as the
+    // warp's busiest token has survivors.
+    float cvs[32];
+    uint32_t mask = 0;
+    const bool full = bi[L - 1] != EMPTY;
+    const float thr = bv[L - 1];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      if (c0 + i >= p.N) break;
-      zmax = fmaxf(zmax, z[i]);
-      const float cv = sel ? z[i] + s_sel[c0 + i] : z[i];
-      const float cz = z[i];
-      const int ci = c0 + i;
+      cvs[i] = sel && c0 + i < p.N ? z[i] + s_sel[c0 + i] : z[i];
+      if (c0 + i < p.N) {
+        zmax = fmaxf(zmax, z[i]);
+        if (!full || cvs[i] > thr) mask |= 1u << i;
+      }
+    }
+    while (mask != 0u) {
+      const int i = __ffs(mask) - 1;
+      mask &= mask - 1u;
+      const float cv = cvs[i];
       if (bi[L - 1] == EMPTY || cv > bv[L - 1]) {
+        const float cz = z[i];
+        const int ci = c0 + i;
         // The kept keys are a descending prefix of the list; the new key goes behind
-        // every kept key it does not exceed (an equal later expert never displaces an
-        // earlier one).  Its place is a count and the shift is per slot, so one
-        // insertion is a few dependent steps rather than a chain along the list.
+        // every kept key it does not exceed.  Its place is a count and the shift is per
+        // slot, so one insertion is a few dependent steps rather than a chain along the
+        // list.
         int pos = 0;
 #pragma unroll
         for (int j = 0; j < L; ++j) pos += (bi[j] != EMPTY && !(cv > bv[j])) ? 1 : 0;
