@@ -382,6 +382,55 @@ typedef struct moe_grads {
   float* dshared_gate_w;   /* [d] fp32: with dW_router and a learned shared gate (Eq. 77) */
 } moe_grads;
 
+/* ---- Expert parallelism across ranks (Section 10.3, Eq. 23 and 26, Figure 41) -------------
+ * With M ranks each holding a batch of tokens and the experts rho maps to it, every rank
+ * all-gathers the requested split counts counts[s][e] (the routes of source rank s's tokens to
+ * expert e; C^req of each source's batch from moe_permute) and derives the same keep matrix:
+ * destination rank q, with budget B = max(1, ceil(c K T / M)) for the T tokens of all ranks
+ * (recovered from the counts: K requests per token), flattens its experts in ascending index
+ * and, within an expert, the sources in ascending rank, and admits routes cumulatively until
+ * B is used (MOE_CAP_RANK_WIDE; MOE_CAP_NONE keeps everything); source s keeps the first
+ * keep[s][e] of its requests to e in token order.  Destination q packs, per expert in
+ * ascending index, the rows of source 0, then 1, ...: recv_off[s][e] is the first row of split
+ * (s, e) in q's buffer (Eq. 26 over q's experts), R_req[q] / R_keep[q] its requested and kept
+ * totals (Eq. 20-21).  On one batch the result equals the single-device rank-wide rule applied
+ * to the ranks' batches concatenated in rank order.  The exchange of rows and outputs itself is
+ * the caller's (NCCL or peer stores to recv rows); these entries only plan it.
+ *
+ * moe_ep_keep_matrix: counts, keep, recv_off [M][N] int32 device; R_req, R_keep [M] device or
+ * NULL; rho HOST [N] with values in [0, M).  One kernel on the stream, no host synchronisation.
+ * Errors: MOE_ERR_INVALID_ARG (sizes, rho, NULL), MOE_ERR_UNSUPPORTED (per-expert capacity:
+ * use the rank-wide budget across ranks), MOE_ERR_CUDA. */
+moe_status moe_ep_keep_matrix(int32_t M, int32_t N, int32_t K, const int32_t* rho,
+                              int32_t cap_policy, double capacity_factor, const int32_t* counts,
+                              int32_t* keep, int32_t* recv_off, int32_t* R_req, int32_t* R_keep,
+                              cudaStream_t stream);
+
+/* Destination rows of source rank src_rank's routes: dst_row[t][k] = recv_off[src][e] + (rank of
+ * route (t, k) among the source's requests to its expert e in token order) when that rank is
+ * below keep[src][e], else -1 (dropped); the destination rank is rho[e].  topk_idx, route_pos
+ * and offsets are those of a moe_permute of the source's batch under a configuration without
+ * capacity (route_pos - offsets[e] is the rank); keep and recv_off from moe_ep_keep_matrix.
+ * All device; M is the number of source ranks (rows of keep / recv_off), src_rank in [0, M).
+ * workspace: a workspace of the layer (its status word records an expert id out of range, with
+ * dst_row -1).  Errors: MOE_ERR_INVALID_ARG (sizes, src_rank, NULL), MOE_ERR_CUDA. */
+moe_status moe_ep_place(int32_t M, int32_t src_rank, int64_t T, int32_t N, int32_t K,
+                        const int32_t* topk_idx,
+                        const int32_t* route_pos, const int32_t* offsets, const int32_t* keep,
+                        const int32_t* recv_off, int32_t* dst_row, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
+
+/* The same two steps on HOST arrays, with no CUDA call (the planning logic alone, for hosts that
+ * gather the counts themselves).  moe_ep_place_host ranks the routes itself from topk_idx in
+ * (token, slot) order.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED as above. */
+moe_status moe_ep_keep_matrix_host(int32_t M, int32_t N, int32_t K, const int32_t* rho,
+                                   int32_t cap_policy, double capacity_factor,
+                                   const int32_t* counts, int32_t* keep, int32_t* recv_off,
+                                   int32_t* R_req, int32_t* R_keep);
+moe_status moe_ep_place_host(int32_t M, int32_t src_rank, int64_t T, int32_t N, int32_t K,
+                             const int32_t* topk_idx, const int32_t* keep,
+                             const int32_t* recv_off, int32_t* dst_row);
+
 /* Bytes of scratch moe_layer_backward needs (256-byte aligned; prepare it with
  * moe_workspace_init before its first use). */
 moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);

@@ -92,6 +92,12 @@ def _load():
                               POINTER(c_void_p), POINTER(c_void_p), P, P, P, P], c_int32),
         "moe_read_status": ([P, POINTER(c_int32), P], c_int32),
         "moe_check_wait_bound": ([P, c_size_t, c_int64, P], c_int32),
+        "moe_ep_keep_matrix": ([c_int32, c_int32, c_int32, POINTER(c_int32), c_int32, c_double, P, P,
+                                P, P, P, P], c_int32),
+        "moe_ep_place": ([c_int32, c_int32, c_int64, c_int32, c_int32, P, P, P, P, P, P, P, c_size_t, P], c_int32),
+        "moe_ep_keep_matrix_host": ([c_int32, c_int32, c_int32, POINTER(c_int32), c_int32, c_double, P,
+                                     P, P, P, P], c_int32),
+        "moe_ep_place_host": ([c_int32, c_int32, c_int64, c_int32, c_int32, P, P, P, P], c_int32),
         "moe_backward_workspace_size": ([C, POINTER(c_size_t)], c_int32),
         "moe_layer_backward": ([C, POINTER(moe_weights), P, POINTER(moe_outputs), P, POINTER(moe_grads),
                                 P, c_size_t, P], c_int32),
