@@ -59,6 +59,10 @@ struct RouteParams {
 cudaError_t launch_route(const RouteParams& p, int32_t dtype, cudaStream_t s);
 // bf16 router on the tensor cores (route_tc.cu); launch_route dispatches to it.
 cudaError_t launch_route_tc(const RouteParams& p, cudaStream_t s);
+// The same on CTA pairs for 128 < N <= 256 without a learned shared gate (route_pair.cu);
+// launch_route_tc hands those layers to it.
+bool route_pair_applies(const RouteParams& p);
+cudaError_t launch_route_pair(const RouteParams& p, cudaStream_t s);
 
 // 2-D bf16 tensor map of a dense row-major [rows][inner] tensor: box 64 x box_rows,
 // 128-byte swizzle, zero fill out of bounds.  False if the driver rejects it.

@@ -183,7 +183,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(taddr + a.n_pad, r);
         gate_raw = __uint_as_float(r[0]);
       }
-      route_one_token<L>(p, s_bias, s_sel, t, valid,
+      // the ring is free once the accumulator is complete: two 32-entry scratch rows per
+      // thread, thread-interleaved so that every access is free of bank conflicts
+      float* scratch = reinterpret_cast<float*>(smem) + q * 32 + lane;
+      route_one_token<L>(p, s_bias, s_sel, t, valid, scratch, scratch + 32 * BM, BM,
                          [&](int c0, uint32_t(&r)[32]) { tmem_ld32(taddr + c0, r); }, gate_raw);
     }
     }
@@ -202,6 +205,7 @@ done:
 
 cudaError_t launch_route_tc(const RouteParams& p, cudaStream_t s) {
   if (p.T == 0) return cudaSuccess;
+  if (route_pair_applies(p)) return launch_route_pair(p, s);
   const bool gated = p.shared_mode == MOE_SHARED_SIGMOID_GATE;
   const int n_pad = (p.N + 15) / 16 * 16;
   // Tokens per CTA: the smallest of 32, 64, 128 whose grid fits the SMs at once (two

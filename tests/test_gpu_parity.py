@@ -63,6 +63,16 @@ SMALL = {
     # K = 6 an 8-entry list with two
     "olmo_k3": C["olmo"].replace(T=700, d_model=256, d_expert=128, d_shared=128, K=3, alpha=3.0),
     "dsv3_k6": C["dsv3"].replace(T=500, d_model=448, d_expert=128, d_shared=128, K=6),
+    # more than 128 experts: the router runs on CTA pairs, each token's columns split over
+    # two TMEM lanes whose lists and softmax partial sums are merged.  Softmax scores over
+    # all N with 200 experts (the upper half ends inside a 32-column chunk), softmax with a
+    # per-expert logit bias and no normalisation over 160, and a learned shared gate with 144
+    # experts (that router stays on one CTA per token block)
+    "wide_softmax_s": C["olmo"].replace(T=700, d_model=320, N=200, K=8, alpha=1.0, d_expert=128,
+                                        d_shared=128),
+    "wide_bias_s": C["qwen2"].replace(T=650, d_model=256, N=160, d_expert=128, d_shared=128,
+                                      shared_mode="const"),
+    "wide_gate_s": C["qwen2"].replace(T=500, d_model=256, N=144, d_expert=128, d_shared=128),
 }
 
 
