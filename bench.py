@@ -490,6 +490,9 @@ def main():
                     help="run R untimed layer forwards and exit (a short, fixed launch sequence "
                          "for ncu captures: each forward launches the routed gate/up and down "
                          "GEMMs, then the shared ones)")
+    ap.add_argument("--route-only", type=int, default=0, metavar="R",
+                    help="run R untimed router calls (moe_route alone) on the workload's inputs "
+                         "and exit (the launch sequence of a router capture)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -543,6 +546,19 @@ def main():
     dev = torch.device("cuda", local)
 
     import routing_shared_expert_gb300 as moe
+    if args.route_only > 0:
+        inp = make_inputs(spec, dev, seed=0)
+        layer = moe.MoELayer(moe.config_from_spec(spec), inp, dev, staged_buffers=False)
+        c, o, w = layer.cfg, layer.out, layer.weights
+        for _ in range(args.route_only):
+            moe.moe_route(c, inp["x"], w["W_router"], w.get("router_bias"), w.get("selection_bias"),
+                          w.get("shared_gate_w"), o["topk_idx"], o["topk_w"], o["shared_coef"], None,
+                          layer.ws)
+        torch.cuda.synchronize()
+        if layer.status() != 0:
+            raise RuntimeError(f"layer status {layer.status()}")
+        print(json.dumps({"route_only": args.route_only, "workload": spec.name}), flush=True)
+        return 0
     if args.forward_only > 0:
         inp = make_inputs(spec, dev, seed=0)
         layer = moe.MoELayer(moe.config_from_spec(spec), inp, dev)
