@@ -32,9 +32,11 @@ Sources (page title, then section / equation / table):
   Eq. 39 (requested max/mean), the entropy deficit of Section 10.2.
 
 Readings where the pages are silent or ambiguous are stated beside the code
-that takes them.  Parity unpinned: the exact expert and shared outputs f_i, g
-at the bf16 layer shapes have no outside pin; they rest on this oracle,
-supported by the dense-reduction (Eq. 81) and shared-merge (Eq. 76) pins.
+that takes them.  Every function is pinned by tests/test_oracle_pins.py to values
+the pages print, closed forms, brute force or identities; the expert and shared
+outputs f_i, g and the merged y by hand-evaluated SwiGLU and Eq. 80 tokens and by
+the Eq. 81 dense reduction, written out independently with numpy at a random
+layer.  The full layer shapes run the same shape-generic code.
 """
 from __future__ import annotations
 
