@@ -431,6 +431,59 @@ moe_status moe_ep_place_host(int32_t M, int32_t src_rank, int64_t T, int32_t N, 
                              const int32_t* topk_idx, const int32_t* keep,
                              const int32_t* recv_off, int32_t* dst_row);
 
+/* The exchange buffers of the dispatch (Section 10.3, Figure 41).  Source src_rank's send
+ * buffer holds, for each destination rank in ascending order, the rows it sends there in the
+ * destination's buffer order (its experts ascending, each split's kept prefix in token
+ * order), so a destination receives, per source in ascending rank, one contiguous block.
+ *
+ * moe_ep_send_pos: send_pos[t][k] = the send-buffer row of route (t, k), -1 when dropped;
+ * send_counts[q] (may be NULL) = rows sent to rank q.  topk_idx, dst_row [T][K] (dst_row from
+ * moe_ep_place), keep, recv_off [M][N], send_pos, send_counts: device.  rho HOST [N].
+ * workspace: a layer workspace (its status word records expert ids out of range, with
+ * send_pos -1).  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA.
+ *
+ * moe_ep_recv_rows: for destination dst_rank, recv_row[j] = the row of its packed buffer
+ * (per local expert ascending, sources ascending: recv_off) that row j of its receive
+ * buffer (source blocks in ascending rank) belongs to; R_keep[dst_rank] entries, at most
+ * recv_cap written (more records MOE_ERR_DEVICE_BOUNDS in the workspace).  Device arrays,
+ * rho HOST.  Errors as above.
+ *
+ * moe_rows_copy: for i in [0, n): dst row dst_index[i] (i when dst_index is NULL) = src row
+ * src_index[i] (i / src_div when src_index is NULL; src_div = K maps route t K + k to token
+ * t).  A negative destination skips the row; a negative source writes zeros when
+ * zero_missing is set, else skips.  Rows of row_bytes bytes (a multiple of 16), src and dst
+ * 16-byte aligned and not overlapping; src [src_rows] and dst [dst_rows] rows bound the
+ * indices (an index past them records MOE_ERR_DEVICE_BOUNDS and skips the row).  One warp
+ * per row.  Device arrays.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED (row_bytes not a
+ * multiple of 16), MOE_ERR_MISALIGNED, MOE_ERR_CUDA.
+ *
+ * The _host twins take host arrays, make no CUDA call and return MOE_ERR_INVALID_ARG for an
+ * index out of range. */
+moe_status moe_ep_send_pos(int32_t M, int32_t src_rank, int64_t T, int32_t N, int32_t K,
+                           const int32_t* rho, const int32_t* topk_idx, const int32_t* keep,
+                           const int32_t* recv_off, const int32_t* dst_row, int32_t* send_pos,
+                           int32_t* send_counts, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+moe_status moe_ep_recv_rows(int32_t M, int32_t dst_rank, int32_t N, const int32_t* rho,
+                            const int32_t* keep, const int32_t* recv_off, int32_t* recv_row,
+                            int64_t recv_cap, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+moe_status moe_rows_copy(const void* src, int64_t src_rows, const int32_t* src_index,
+                         int64_t src_div, void* dst, int64_t dst_rows, const int32_t* dst_index,
+                         int64_t n, int64_t row_bytes, int32_t zero_missing, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+moe_status moe_ep_send_pos_host(int32_t M, int32_t src_rank, int64_t T, int32_t N, int32_t K,
+                                const int32_t* rho, const int32_t* topk_idx, const int32_t* keep,
+                                const int32_t* recv_off, const int32_t* dst_row,
+                                int32_t* send_pos, int32_t* send_counts);
+moe_status moe_ep_recv_rows_host(int32_t M, int32_t dst_rank, int32_t N, const int32_t* rho,
+                                 const int32_t* keep, const int32_t* recv_off, int32_t* recv_row,
+                                 int64_t recv_cap);
+moe_status moe_rows_copy_host(const void* src, int64_t src_rows, const int32_t* src_index,
+                              int64_t src_div, void* dst, int64_t dst_rows,
+                              const int32_t* dst_index, int64_t n, int64_t row_bytes,
+                              int32_t zero_missing);
+
 /* Bytes of scratch moe_layer_backward needs (256-byte aligned; prepare it with
  * moe_workspace_init before its first use). */
 moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);

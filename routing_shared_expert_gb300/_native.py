@@ -98,6 +98,18 @@ def _load():
         "moe_ep_keep_matrix_host": ([c_int32, c_int32, c_int32, POINTER(c_int32), c_int32, c_double, P,
                                      P, P, P, P], c_int32),
         "moe_ep_place_host": ([c_int32, c_int32, c_int64, c_int32, c_int32, P, P, P, P], c_int32),
+        "moe_ep_send_pos": ([c_int32, c_int32, c_int64, c_int32, c_int32, POINTER(c_int32), P, P, P,
+                             P, P, P, P, c_size_t, P], c_int32),
+        "moe_ep_recv_rows": ([c_int32, c_int32, c_int32, POINTER(c_int32), P, P, P, c_int64, P,
+                              c_size_t, P], c_int32),
+        "moe_rows_copy": ([P, c_int64, P, c_int64, P, c_int64, P, c_int64, c_int64, c_int32, P,
+                           c_size_t, P], c_int32),
+        "moe_ep_send_pos_host": ([c_int32, c_int32, c_int64, c_int32, c_int32, POINTER(c_int32), P,
+                                  P, P, P, P, P], c_int32),
+        "moe_ep_recv_rows_host": ([c_int32, c_int32, c_int32, POINTER(c_int32), P, P, P, c_int64],
+                                  c_int32),
+        "moe_rows_copy_host": ([P, c_int64, P, c_int64, P, c_int64, P, c_int64, c_int64, c_int32],
+                               c_int32),
         "moe_backward_workspace_size": ([C, POINTER(c_size_t)], c_int32),
         "moe_layer_backward": ([C, POINTER(moe_weights), P, POINTER(moe_outputs), P, POINTER(moe_grads),
                                 P, c_size_t, P], c_int32),

@@ -1,6 +1,8 @@
 // Expert-parallel capacity agreement and dispatch plan (Section 10.3): the keep matrix every
-// rank derives from the all-gathered requested split counts, and each route's destination
-// row (ep_plan.h holds the rules, shared by the device kernels and the host entry points).
+// rank derives from the all-gathered requested split counts, each route's destination row,
+// the send and receive layouts of the exchange, and the indexed row copies that fill and
+// drain the exchange buffers (ep_plan.h holds the rules, shared by the device kernels and
+// the host entry points).
 //
 // The device entries are sync-free: the gathered counts stay on the device, the token
 // count over all sources is recovered from them (K requests per token), and a source's
@@ -53,12 +55,142 @@ __global__ void ep_place_kernel(const int32_t* topk_idx, const int32_t* route_po
   dst_row[r] = ep_place_route(src, N, e, pos - offsets[e], keep, recv_off);
 }
 
+struct EpSendArgs {
+  int32_t rho[kMaxExperts];
+  int32_t M, N, K, src;
+  int64_t routes;
+  const int32_t* topk_idx;
+  const int32_t* keep;
+  const int32_t* recv_off;
+  const int32_t* dst_row;
+  int32_t* send_pos;
+  int32_t* send_counts;
+  int32_t* status;
+};
+
+// One thread per route; every block first lays out the source's send buffer (O(M + N)).
+__global__ void ep_send_pos_kernel(EpSendArgs a) {
+  __shared__ int32_t base[kMaxExperts];
+  if (threadIdx.x == 0)
+    ep_send_base(a.src, a.M, a.N, a.rho, a.keep, base, blockIdx.x == 0 ? a.send_counts : nullptr);
+  __syncthreads();
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r >= a.routes) return;
+  const int e = a.topk_idx[r];
+  if (e < 0 || e >= a.N) {
+    set_status(a.status, MOE_ERR_DEVICE_BOUNDS);
+    a.send_pos[r] = -1;
+    return;
+  }
+  a.send_pos[r] = ep_send_pos_route(a.src, a.N, e, a.dst_row[r], base, a.recv_off);
+}
+
+struct EpRecvArgs {
+  int32_t rho[kMaxExperts];
+  int32_t M, N, q;
+  const int32_t* keep;
+  const int32_t* recv_off;
+  int32_t* recv_row;
+  int64_t cap;
+  int32_t* status;
+};
+
+// One block per split (s, e) of a local expert: the split's rows sit in the receive buffer
+// after the earlier sources' blocks and, within source s, after its earlier local experts.
+__global__ void ep_recv_rows_kernel(EpRecvArgs a) {
+  const int s = blockIdx.x / a.N, e = blockIdx.x % a.N;
+  if (a.rho[e] != a.q) return;
+  __shared__ int64_t j0;
+  if (threadIdx.x == 0) {
+    int64_t j = 0;
+    for (int s2 = 0; s2 < a.M; ++s2)
+      for (int e2 = 0; e2 < a.N; ++e2) {
+        if (a.rho[e2] != a.q) continue;
+        if (s2 == s && e2 == e) { s2 = a.M; break; }
+        j += a.keep[static_cast<int64_t>(s2) * a.N + e2];
+      }
+    j0 = j;
+  }
+  __syncthreads();
+  const int64_t i = static_cast<int64_t>(s) * a.N + e;
+  const int32_t n = a.keep[i];
+  for (int32_t r = threadIdx.x; r < n; r += blockDim.x) {
+    if (j0 + r >= a.cap) {
+      set_status(a.status, MOE_ERR_DEVICE_BOUNDS);
+      return;
+    }
+    a.recv_row[j0 + r] = a.recv_off[i] + r;
+  }
+}
+
+struct RowsCopyArgs {
+  const int4* src;
+  int64_t src_rows;
+  const int32_t* src_index;
+  int64_t src_div;
+  int4* dst;
+  int64_t dst_rows;
+  const int32_t* dst_index;
+  int64_t n;
+  int64_t nvec;   // 16-byte vectors per row
+  int32_t zero_missing;
+  int32_t* status;
+};
+
+// One warp per copied row: dst[dst row] = src[src row], four 16-byte loads in flight per lane.
+__global__ void __launch_bounds__(256) rows_copy_kernel(RowsCopyArgs a) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (i >= a.n) return;
+  const int64_t t = a.dst_index ? a.dst_index[i] : i;
+  if (t < 0) return;
+  const int64_t sr = a.src_index ? a.src_index[i] : i / a.src_div;
+  if (t >= a.dst_rows || sr >= a.src_rows) {
+    if (lane == 0) set_status(a.status, MOE_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  int4* out = a.dst + t * a.nvec;
+  if (sr < 0) {
+    if (a.zero_missing)
+      for (int64_t v = lane; v < a.nvec; v += 32) out[v] = make_int4(0, 0, 0, 0);
+    return;
+  }
+  const int4* __restrict__ in = a.src + sr * a.nvec;
+  constexpr int U = 4;
+  for (int64_t v0 = lane; v0 < a.nvec; v0 += 32 * U) {
+    int4 val[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (v0 + u * 32 < a.nvec) val[u] = in[v0 + u * 32];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (v0 + u * 32 < a.nvec) out[v0 + u * 32] = val[u];
+  }
+}
+
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
 
 namespace {
+
+moe_status check_rho(int32_t M, int32_t N, const int32_t* rho) {
+  if (M < 1 || M > kMaxExperts || N < 1 || N > kMaxExperts || !rho) return MOE_ERR_INVALID_ARG;
+  for (int e = 0; e < N; ++e)
+    if (rho[e] < 0 || rho[e] >= M) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status check_rows_copy(const void* src, int64_t src_rows, int64_t src_div, const void* dst,
+                           int64_t dst_rows, int64_t n, int64_t row_bytes) {
+  if (n < 0 || src_rows < 0 || dst_rows < 0 || row_bytes <= 0 || src_div < 1) return MOE_ERR_INVALID_ARG;
+  if (row_bytes % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if (n > 0 && (!dst || (src_rows > 0 && !src))) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(src) & 15u) || (reinterpret_cast<uintptr_t>(dst) & 15u))
+    return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
 
 moe_status check_ep(int32_t M, int32_t N, int32_t K, int32_t cap_policy, double c,
                     const int32_t* rho) {
@@ -142,6 +274,140 @@ moe_status moe_ep_place_host(int32_t M, int32_t src_rank, int64_t T, int32_t N, 
     const int32_t e = topk_idx[r];
     if (e < 0 || e >= N) return MOE_ERR_INVALID_ARG;
     dst_row[r] = ep_place_route(src_rank, N, e, seen[e]++, keep, recv_off);
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+moe_status moe_ep_send_pos(int32_t M, int32_t src_rank, int64_t T, int32_t N, int32_t K,
+                           const int32_t* rho, const int32_t* topk_idx, const int32_t* keep,
+                           const int32_t* recv_off, const int32_t* dst_row, int32_t* send_pos,
+                           int32_t* send_counts, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  moe_status s = check_rho(M, N, rho);
+  if (s != MOE_OK) return s;
+  if (T < 0 || K < 1 || K > N || src_rank < 0 || src_rank >= M) return MOE_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < 256 || !keep) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_idx || !recv_off || !dst_row || !send_pos)) return MOE_ERR_INVALID_ARG;
+  EpSendArgs a{};
+  std::memcpy(a.rho, rho, sizeof(int32_t) * N);
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.src = src_rank;
+  a.routes = T * K;
+  a.topk_idx = topk_idx;
+  a.keep = keep;
+  a.recv_off = recv_off;
+  a.dst_row = dst_row;
+  a.send_pos = send_pos;
+  a.send_counts = send_counts;
+  a.status = static_cast<int32_t*>(workspace);
+  const int64_t blocks = a.routes > 0 ? (a.routes + 255) / 256 : 1;   // block 0 writes the counts
+  ep_send_pos_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_ep_recv_rows(int32_t M, int32_t dst_rank, int32_t N, const int32_t* rho,
+                            const int32_t* keep, const int32_t* recv_off, int32_t* recv_row,
+                            int64_t recv_cap, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  moe_status s = check_rho(M, N, rho);
+  if (s != MOE_OK) return s;
+  if (dst_rank < 0 || dst_rank >= M || recv_cap < 0) return MOE_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < 256 || !keep || !recv_off) return MOE_ERR_INVALID_ARG;
+  if (recv_cap > 0 && !recv_row) return MOE_ERR_INVALID_ARG;
+  EpRecvArgs a{};
+  std::memcpy(a.rho, rho, sizeof(int32_t) * N);
+  a.M = M;
+  a.N = N;
+  a.q = dst_rank;
+  a.keep = keep;
+  a.recv_off = recv_off;
+  a.recv_row = recv_row;
+  a.cap = recv_cap;
+  a.status = static_cast<int32_t*>(workspace);
+  ep_recv_rows_kernel<<<static_cast<unsigned>(M) * static_cast<unsigned>(N), 256, 0, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_rows_copy(const void* src, int64_t src_rows, const int32_t* src_index,
+                         int64_t src_div, void* dst, int64_t dst_rows, const int32_t* dst_index,
+                         int64_t n, int64_t row_bytes, int32_t zero_missing, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+  moe_status s = check_rows_copy(src, src_rows, src_div, dst, dst_rows, n, row_bytes);
+  if (s != MOE_OK) return s;
+  if (!workspace || workspace_bytes < 256) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  RowsCopyArgs a{};
+  a.src = static_cast<const int4*>(src);
+  a.src_rows = src_rows;
+  a.src_index = src_index;
+  a.src_div = src_div;
+  a.dst = static_cast<int4*>(dst);
+  a.dst_rows = dst_rows;
+  a.dst_index = dst_index;
+  a.n = n;
+  a.nvec = row_bytes / 16;
+  a.zero_missing = zero_missing ? 1 : 0;
+  a.status = static_cast<int32_t*>(workspace);
+  rows_copy_kernel<<<static_cast<unsigned>((n + 7) / 8), 256, 0, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_ep_send_pos_host(int32_t M, int32_t src_rank, int64_t T, int32_t N, int32_t K,
+                                const int32_t* rho, const int32_t* topk_idx, const int32_t* keep,
+                                const int32_t* recv_off, const int32_t* dst_row,
+                                int32_t* send_pos, int32_t* send_counts) {
+  moe_status s = check_rho(M, N, rho);
+  if (s != MOE_OK) return s;
+  if (T < 0 || K < 1 || K > N || src_rank < 0 || src_rank >= M || !keep) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_idx || !recv_off || !dst_row || !send_pos)) return MOE_ERR_INVALID_ARG;
+  int32_t base[kMaxExperts];
+  ep_send_base(src_rank, M, N, rho, keep, base, send_counts);
+  for (int64_t r = 0; r < T * K; ++r) {
+    const int32_t e = topk_idx[r];
+    if (e < 0 || e >= N) return MOE_ERR_INVALID_ARG;
+    send_pos[r] = ep_send_pos_route(src_rank, N, e, dst_row[r], base, recv_off);
+  }
+  return MOE_OK;
+}
+
+moe_status moe_ep_recv_rows_host(int32_t M, int32_t dst_rank, int32_t N, const int32_t* rho,
+                                 const int32_t* keep, const int32_t* recv_off, int32_t* recv_row,
+                                 int64_t recv_cap) {
+  moe_status s = check_rho(M, N, rho);
+  if (s != MOE_OK) return s;
+  if (dst_rank < 0 || dst_rank >= M || recv_cap < 0 || !keep || !recv_off) return MOE_ERR_INVALID_ARG;
+  int64_t need = 0;
+  for (int32_t q = 0; q < M; ++q)
+    for (int32_t e = 0; e < N; ++e)
+      if (rho[e] == dst_rank) need += keep[static_cast<int64_t>(q) * N + e];
+  if (need > recv_cap || (need > 0 && !recv_row)) return MOE_ERR_INVALID_ARG;
+  ep_recv_rows(dst_rank, M, N, rho, keep, recv_off, recv_row);
+  return MOE_OK;
+}
+
+moe_status moe_rows_copy_host(const void* src, int64_t src_rows, const int32_t* src_index,
+                              int64_t src_div, void* dst, int64_t dst_rows,
+                              const int32_t* dst_index, int64_t n, int64_t row_bytes,
+                              int32_t zero_missing) {
+  moe_status s = check_rows_copy(src, src_rows, src_div, dst, dst_rows, n, row_bytes);
+  if (s != MOE_OK) return s;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t t = dst_index ? dst_index[i] : i;
+    if (t < 0) continue;
+    const int64_t sr = src_index ? src_index[i] : i / src_div;
+    if (t >= dst_rows || sr >= src_rows) return MOE_ERR_INVALID_ARG;
+    char* out = static_cast<char*>(dst) + t * row_bytes;
+    if (sr < 0) {
+      if (zero_missing) std::memset(out, 0, static_cast<size_t>(row_bytes));
+      continue;
+    }
+    std::memcpy(out, static_cast<const char*>(src) + sr * row_bytes, static_cast<size_t>(row_bytes));
   }
   return MOE_OK;
 }

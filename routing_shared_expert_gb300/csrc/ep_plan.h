@@ -94,4 +94,46 @@ MOE_HD inline int32_t ep_place_route(int32_t src, int32_t N, int32_t e, int32_t 
   return rank < keep[i] ? recv_off[i] + rank : -1;
 }
 
+// A source's send buffer holds, for each destination rank q in ascending order, the rows it
+// sends to q in q's buffer order (q's experts in ascending index, each split's kept prefix in
+// token order).  base[e] is the send-buffer position of the first kept route of split
+// (src, e); send_counts[q] (may be null) the rows the source sends to q.  base [N], rho [N].
+MOE_HD inline void ep_send_base(int32_t src, int32_t M, int32_t N, const int32_t* rho,
+                                const int32_t* keep, int32_t* base, int32_t* send_counts) {
+  int64_t pos = 0;
+  for (int32_t q = 0; q < M; ++q) {
+    int64_t n = 0;
+    for (int32_t e = 0; e < N; ++e) {
+      if (rho[e] != q) continue;
+      base[e] = static_cast<int32_t>(pos + n);
+      n += keep[static_cast<int64_t>(src) * N + e];
+    }
+    if (send_counts) send_counts[q] = static_cast<int32_t>(n);
+    pos += n;
+  }
+}
+
+// Send-buffer position of a route of source `src` placed at destination row `row` (from
+// ep_place_route) for expert e, or -1 when the route is dropped (row < 0).
+MOE_HD inline int32_t ep_send_pos_route(int32_t src, int32_t N, int32_t e, int32_t row,
+                                        const int32_t* base, const int32_t* recv_off) {
+  return row < 0 ? -1 : base[e] + (row - recv_off[static_cast<int64_t>(src) * N + e]);
+}
+
+// Destination q's receive buffer from the exchange: the blocks of sources 0, 1, ... in
+// order, each in the source's send order for q.  recv_row[j] is the row of q's packed
+// buffer that received row j belongs to.  Writes R_keep[q] entries; returns their count.
+MOE_HD inline int64_t ep_recv_rows(int32_t q, int32_t M, int32_t N, const int32_t* rho,
+                                   const int32_t* keep, const int32_t* recv_off,
+                                   int32_t* recv_row) {
+  int64_t j = 0;
+  for (int32_t s = 0; s < M; ++s)
+    for (int32_t e = 0; e < N; ++e) {
+      if (rho[e] != q) continue;
+      const int64_t i = static_cast<int64_t>(s) * N + e;
+      for (int32_t r = 0; r < keep[i]; ++r) recv_row[j++] = recv_off[i] + r;
+    }
+  return j;
+}
+
 }  // namespace moe

@@ -8,17 +8,21 @@ Figure 41).  Each rank holds a batch of tokens and the experts rho maps to it.  
    the destination row of each of its routes (``moe_ep_keep_matrix`` / ``moe_ep_place`` on
    CUDA tensors, their host twins on CPU tensors): destination q packs, per local expert in
    ascending index, the kept rows of source 0, then source 1, ...;
-3. dispatch: every kept route's token row goes to rank rho(e), row dst_row of its buffer
-   (one all-to-all of rows and their destination rows, then a scatter);
+3. dispatch: each source lays its kept rows out in a send buffer (destinations in
+   ascending rank, each in the destination's buffer order), one all-to-all moves them, and
+   each destination scatters its receive buffer into its packed buffer
+   (``moe_ep_send_pos``, ``moe_rows_copy``, ``moe_ep_recv_rows``);
 4. each rank runs its local experts over its packed buffer (segments from the keep matrix);
-5. combine: the expert outputs go back to their sources (the reverse all-to-all), and each
-   source merges them with its shared branch (Eq. 80; dropped routes add nothing).
+5. combine: the expert outputs go back the same way (gather, reverse all-to-all, gather by
+   send position), and each source merges them with its shared branch (Eq. 80; dropped
+   routes add nothing).
 
-This module plans and moves data; the routing, the expert GEMMs and the merge are callables
-(on a GPU: the library's kernels).  The collectives are ``torch.distributed`` (NCCL on GPUs,
-gloo on CPU).  The all-to-all takes split sizes on the host, so each forward reads the M x M
-send counts back once (a sync-free variant would write rows straight into capacity-shaped
-receive buffers on the peers).
+This module plans and moves data with the library's entry points (on CUDA tensors the
+device kernels, on CPU tensors their host twins); the routing, the expert GEMMs and the
+merge are callables (on a GPU: the library's kernels).  The collectives are
+``torch.distributed`` (NCCL on GPUs, gloo on CPU).  The all-to-all takes split sizes on the
+host, so each forward reads the M x N keep matrix back once (a sync-free variant would
+write rows straight into capacity-shaped receive buffers on the peers).
 """
 from __future__ import annotations
 
@@ -41,11 +45,13 @@ class EpPlan:
     R_req: torch.Tensor      # [M] requested rows per destination (Eq. 20)
     R_keep: torch.Tensor     # [M] kept rows per destination (Eq. 21)
     dst_row: torch.Tensor    # [T, K] int32: row of the route in rho(e)'s buffer, -1 dropped
+    send_pos: torch.Tensor   # [T, K] int32: row of the route in this rank's send buffer, -1
+    keep_host: torch.Tensor  # [M, N] int64 copy of keep on the host (the split sizes)
 
     def local_offsets(self) -> torch.Tensor:
         """Eq. 26 over this rank's experts in ascending index: [n_local + 1] int32 (host)."""
-        keep = self.keep.cpu()
-        sizes = [int(keep[:, e].sum()) for e in range(keep.shape[1]) if self.rho[e] == self.rank]
+        sizes = [int(self.keep_host[:, e].sum()) for e in range(self.keep_host.shape[1])
+                 if self.rho[e] == self.rank]
         off = [0]
         for m in sizes:
             off.append(off[-1] + m)
@@ -53,16 +59,18 @@ class EpPlan:
 
     def send_counts(self) -> torch.Tensor:
         """[M, M] host: rows source s sends to destination q (from the keep matrix alone)."""
-        keep = self.keep.cpu().to(torch.int64)
-        M = self.world
-        out = torch.zeros((M, M), dtype=torch.int64)
+        out = torch.zeros((self.world, self.world), dtype=torch.int64)
         for e, q in enumerate(self.rho):
-            out[:, q] += keep[:, e]
+            out[:, q] += self.keep_host[:, e]
         return out
 
 
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _rho(rho):
+    return (ctypes.c_int32 * len(rho))(*[int(v) for v in rho])
 
 
 def gather_counts(counts_local: torch.Tensor, group=None) -> torch.Tensor:
@@ -78,27 +86,32 @@ def make_plan(counts_all: torch.Tensor, topk_idx: torch.Tensor, rank: int, K: in
               cap_policy: str = "rank_wide", capacity_factor: float = 1.0,
               route_pos: Optional[torch.Tensor] = None, offsets: Optional[torch.Tensor] = None,
               workspace: Optional[torch.Tensor] = None, stream=None) -> EpPlan:
-    """The keep matrix and this rank's destination rows.  CUDA tensors use the device
-    entries (route_pos / offsets of a capacity-free moe_permute of the rank's batch and a
-    layer workspace are then required); CPU tensors use the host entries."""
+    """The keep matrix, this rank's destination rows and send positions.  CUDA tensors use the
+    device entries (route_pos / offsets of a capacity-free moe_permute of the rank's batch and
+    a layer workspace are then required); CPU tensors use the host entries."""
     lib = nat.library()
     M, N = counts_all.shape
     T = topk_idx.shape[0]
     pol = nat.CAP_POLICIES[cap_policy] if isinstance(cap_policy, str) else int(cap_policy)
-    rho_arr = (ctypes.c_int32 * N)(*[int(v) for v in rho])
+    rho_arr = _rho(rho)
     dev = counts_all.device
     keep = torch.empty((M, N), dtype=torch.int32, device=dev)
     recv_off = torch.empty((M, N), dtype=torch.int32, device=dev)
     R_req = torch.empty((M,), dtype=torch.int32, device=dev)
     R_keep = torch.empty((M,), dtype=torch.int32, device=dev)
     dst_row = torch.empty((T, K), dtype=torch.int32, device=dev)
+    send_pos = torch.empty((T, K), dtype=torch.int32, device=dev)
     if dev.type == "cuda":
+        st = nat._stream(stream)
         nat._check("moe_ep_keep_matrix", lib.moe_ep_keep_matrix(
             M, N, K, rho_arr, pol, float(capacity_factor), _ptr(counts_all), _ptr(keep),
-            _ptr(recv_off), _ptr(R_req), _ptr(R_keep), nat._stream(stream)))
+            _ptr(recv_off), _ptr(R_req), _ptr(R_keep), st))
         nat._check("moe_ep_place", lib.moe_ep_place(
             M, rank, T, N, K, _ptr(topk_idx), _ptr(route_pos), _ptr(offsets), _ptr(keep),
-            _ptr(recv_off), _ptr(dst_row), _ptr(workspace), workspace.numel(), nat._stream(stream)))
+            _ptr(recv_off), _ptr(dst_row), _ptr(workspace), workspace.numel(), st))
+        nat._check("moe_ep_send_pos", lib.moe_ep_send_pos(
+            M, rank, T, N, K, rho_arr, _ptr(topk_idx), _ptr(keep), _ptr(recv_off), _ptr(dst_row),
+            _ptr(send_pos), None, _ptr(workspace), workspace.numel(), st))
     else:
         counts_all = counts_all.to(torch.int32).contiguous()
         nat._check("moe_ep_keep_matrix_host", lib.moe_ep_keep_matrix_host(
@@ -107,58 +120,91 @@ def make_plan(counts_all: torch.Tensor, topk_idx: torch.Tensor, rank: int, K: in
         idx = topk_idx.to(torch.int32).contiguous()
         nat._check("moe_ep_place_host", lib.moe_ep_place_host(
             M, rank, T, N, K, _ptr(idx), _ptr(keep), _ptr(recv_off), _ptr(dst_row)))
-    return EpPlan(rank, M, list(rho), keep, recv_off, R_req, R_keep, dst_row)
+        nat._check("moe_ep_send_pos_host", lib.moe_ep_send_pos_host(
+            M, rank, T, N, K, rho_arr, _ptr(idx), _ptr(keep), _ptr(recv_off), _ptr(dst_row),
+            _ptr(send_pos), None))
+    return EpPlan(rank, M, list(rho), keep, recv_off, R_req, R_keep, dst_row, send_pos,
+                  keep.cpu().to(torch.int64))
+
+
+def rows_copy(src: torch.Tensor, dst: torch.Tensor, n: int, src_index=None, src_div: int = 1,
+              dst_index=None, zero_missing: bool = False, workspace=None, stream=None):
+    """dst[dst_index[i]] = src[src_index[i]] for i < n (moe_rows_copy; see the C header):
+    row-major 2-D tensors of the same row width, device or host alike."""
+    lib = nat.library()
+    row_bytes = src.shape[1] * src.element_size()
+    if src.device.type == "cuda":
+        nat._check("moe_rows_copy", lib.moe_rows_copy(
+            _ptr(src), src.shape[0], _ptr(src_index), src_div, _ptr(dst), dst.shape[0],
+            _ptr(dst_index), n, row_bytes, 1 if zero_missing else 0, _ptr(workspace),
+            workspace.numel(), nat._stream(stream)))
+    else:
+        nat._check("moe_rows_copy_host", lib.moe_rows_copy_host(
+            _ptr(src), src.shape[0], _ptr(src_index), src_div, _ptr(dst), dst.shape[0],
+            _ptr(dst_index), n, row_bytes, 1 if zero_missing else 0))
+
+
+def recv_rows(plan: EpPlan, workspace=None, stream=None) -> torch.Tensor:
+    """Row of this rank's packed buffer for each row of its receive buffer (moe_ep_recv_rows)."""
+    lib = nat.library()
+    M, N = plan.keep.shape
+    n = int(plan.send_counts()[:, plan.rank].sum())
+    out = torch.empty((n,), dtype=torch.int32, device=plan.keep.device)
+    if plan.keep.device.type == "cuda":
+        nat._check("moe_ep_recv_rows", lib.moe_ep_recv_rows(
+            M, plan.rank, N, _rho(plan.rho), _ptr(plan.keep), _ptr(plan.recv_off), _ptr(out), n,
+            _ptr(workspace), workspace.numel(), nat._stream(stream)))
+    else:
+        nat._check("moe_ep_recv_rows_host", lib.moe_ep_recv_rows_host(
+            M, plan.rank, N, _rho(plan.rho), _ptr(plan.keep), _ptr(plan.recv_off), _ptr(out), n))
+    return out
 
 
 @dataclasses.dataclass
 class Dispatched:
     rows: torch.Tensor            # [R_keep[rank], d] this rank's packed buffer
-    sent_routes: torch.Tensor     # [n_sent] flat route index (t * K + k) of each sent row
+    recv_row: torch.Tensor        # [n_recv] packed row of each received row
     send_split: List[int]         # rows sent to each destination
     recv_split: List[int]         # rows received from each source
-    recv_rows: torch.Tensor       # [n_recv] packed row of each received row
 
 
-def dispatch(x_local: torch.Tensor, plan: EpPlan, topk_idx: torch.Tensor, group=None) -> Dispatched:
-    """Send every kept route's token row to row dst_row of rank rho(e)'s packed buffer."""
+def dispatch(x_local: torch.Tensor, plan: EpPlan, K: int, group=None, workspace=None,
+             stream=None) -> Dispatched:
+    """Send every kept route's token row to its row of rank rho(e)'s packed buffer."""
     import torch.distributed as dist
-    M, me = plan.world, plan.rank
-    K = topk_idx.shape[1]
-    rho_t = torch.tensor(plan.rho, dtype=torch.int64, device=x_local.device)
-    flat_e = topk_idx.reshape(-1).to(torch.int64)
-    flat_row = plan.dst_row.reshape(-1).to(torch.int64)
-    kept = flat_row >= 0
-    dest = torch.where(kept, rho_t[flat_e.clamp(min=0)], torch.full_like(flat_e, M))
-    # kept routes grouped by destination, each group in destination-row order
-    order = torch.argsort(dest * (1 << 40) + flat_row.clamp(min=0), stable=True)
-    order = order[: int(kept.sum())]
     counts = plan.send_counts()
+    me = plan.rank
     send_split = [int(v) for v in counts[me].tolist()]
     recv_split = [int(v) for v in counts[:, me].tolist()]
-    send_rows = x_local[order // K].contiguous()
-    send_idx = flat_row[order].contiguous()
-    d = x_local.shape[1]
+    T, d = x_local.shape
+    send = torch.empty((sum(send_split), d), dtype=x_local.dtype, device=x_local.device)
+    rows_copy(x_local, send, T * K, src_div=K, dst_index=plan.send_pos, workspace=workspace,
+              stream=stream)
     recv = torch.empty((sum(recv_split), d), dtype=x_local.dtype, device=x_local.device)
-    recv_idx = torch.empty((sum(recv_split),), dtype=torch.int64, device=x_local.device)
-    dist.all_to_all_single(recv, send_rows, recv_split, send_split, group=group)
-    dist.all_to_all_single(recv_idx, send_idx, recv_split, send_split, group=group)
-    n_local = int(plan.R_keep.cpu()[me])
-    rows = torch.empty((n_local, d), dtype=x_local.dtype, device=x_local.device)
-    rows[recv_idx] = recv
-    return Dispatched(rows, order, send_split, recv_split, recv_idx)
+    dist.all_to_all_single(recv, send, recv_split, send_split, group=group)
+    rr = recv_rows(plan, workspace, stream)
+    rows = torch.empty((int(plan.keep_host[:, [e for e in range(len(plan.rho))
+                                                if plan.rho[e] == me]].sum()), d),
+                       dtype=x_local.dtype, device=x_local.device)
+    rows_copy(recv, rows, recv.shape[0], dst_index=rr, workspace=workspace, stream=stream)
+    return Dispatched(rows, rr, send_split, recv_split)
 
 
-def return_outputs(f_packed: torch.Tensor, disp: Dispatched, T: int, K: int, group=None) -> torch.Tensor:
-    """The reverse exchange: the output row of every received route goes back to its
-    source.  Returns [T * K, d] on each source: row t * K + k is route (t, k)'s expert
-    output, zero for dropped routes."""
+def return_outputs(f_packed: torch.Tensor, plan: EpPlan, disp: Dispatched, T: int, K: int,
+                   group=None, workspace=None, stream=None) -> torch.Tensor:
+    """The reverse exchange: the output row of every received route goes back to its source.
+    Returns [T * K, d] on each source: row t * K + k is route (t, k)'s expert output, zero for
+    dropped routes."""
     import torch.distributed as dist
-    send = f_packed[disp.recv_rows].contiguous()
-    back = torch.empty((sum(disp.send_split), f_packed.shape[1]), dtype=f_packed.dtype,
-                       device=f_packed.device)
+    d = f_packed.shape[1]
+    send = torch.empty((disp.recv_row.shape[0], d), dtype=f_packed.dtype, device=f_packed.device)
+    rows_copy(f_packed, send, send.shape[0], src_index=disp.recv_row, workspace=workspace,
+              stream=stream)
+    back = torch.empty((sum(disp.send_split), d), dtype=f_packed.dtype, device=f_packed.device)
     dist.all_to_all_single(back, send, disp.send_split, disp.recv_split, group=group)
-    out = torch.zeros((T * K, f_packed.shape[1]), dtype=f_packed.dtype, device=f_packed.device)
-    out[disp.sent_routes] = back
+    out = torch.empty((T * K, d), dtype=f_packed.dtype, device=f_packed.device)
+    rows_copy(back, out, T * K, src_index=plan.send_pos, zero_missing=True, workspace=workspace,
+              stream=stream)
     return out
 
 
@@ -176,7 +222,8 @@ def ep_layer_forward(x_local: torch.Tensor, topk_idx: torch.Tensor, rho: List[in
     rank = dist.get_rank(group)
     counts_all = gather_counts(counts_local, group)
     plan = make_plan(counts_all, topk_idx, rank, K, rho, cap_policy, capacity_factor, **plan_kw)
-    disp = dispatch(x_local, plan, topk_idx, group)
+    ws, st = plan_kw.get("workspace"), plan_kw.get("stream")
+    disp = dispatch(x_local, plan, K, group, ws, st)
     f_packed = expert_fn(disp.rows, plan.local_offsets())
-    route_out = return_outputs(f_packed, disp, x_local.shape[0], K, group)
+    route_out = return_outputs(f_packed, plan, disp, x_local.shape[0], K, group, ws, st)
     return merge_fn(route_out, plan.dst_row >= 0), plan

@@ -5,6 +5,9 @@ token total recovered from the counts), and moe_ep_place gives each route of a s
 destination row from the stable ranks of a capacity-free moe_permute of that source's
 batch.  Both must equal the host entries (which the two-rank gloo test checks against the
 oracle) bit for bit, for several source counts, with and without the rank-wide budget.
+The exchange kernels (send positions, receive rows, indexed row copies) are checked by
+running the dispatch and the return of M sources on one GPU, the all-to-all itself replaced
+by slicing the send buffers.
 """
 import pytest
 import torch
@@ -48,8 +51,89 @@ def test_device_plan_equals_host_plan(M, cap):
     dev = ep.make_plan(counts.cuda(), idx, M - 1, K, rho, cap, 0.6, route_pos=rpos, offsets=off,
                        workspace=ws)
     torch.cuda.synchronize()
-    for k in ("keep", "recv_off", "R_req", "R_keep", "dst_row"):
+    for k in ("keep", "recv_off", "R_req", "R_keep", "dst_row", "send_pos"):
         assert torch.equal(getattr(dev, k).cpu(), getattr(host, k)), k
     assert moe.moe_read_status(ws) == 0
     if cap == "rank_wide" and M > 1:
         assert int(host.keep.sum()) < int(counts.sum())   # the budget dropped some routes
+
+
+def _route_source(spec, seed):
+    cfg = moe.config_from_spec(spec)
+    inp = make_inputs(spec, "cuda", seed=seed)
+    ws = moe.alloc_workspace(cfg)
+    T, K, N = spec.T, spec.K, spec.N
+    idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    moe.moe_route(cfg, inp["x"], inp["W_router"], None, None, None, idx, w, None, None, ws)
+    cnt = torch.empty(N, dtype=torch.int32, device="cuda")
+    ck = torch.empty(N, dtype=torch.int32, device="cuda")
+    off = torch.empty(N + 1, dtype=torch.int32, device="cuda")
+    rpos = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    psrc = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    moe.moe_permute(cfg, None, idx, cnt, ck, off, rpos, psrc, None, None, None, None, ws)
+    return inp["x"], idx, cnt, off, rpos, ws
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_device_exchange_of_m_sources(M):
+    """Dispatch: every kept route's x row reaches row dst_row of destination rho(e)'s packed
+    buffer; return: every route gets back its row of the destination's outputs (here 2 x the
+    row), dropped routes zero.  All row movement by the library's kernels."""
+    spec = CONFIGS["dsv3"].replace(T=300, d_model=256, N=32, K=4, d_expert=128, d_shared=128)
+    N, K, T, d = spec.N, spec.K, spec.T, spec.d_model
+    rho = [e % M for e in range(N)]
+    src = [_route_source(spec, seed=11 + s) for s in range(M)]
+    counts = torch.stack([c for (_, _, c, _, _, _) in src])
+    plans = [ep.make_plan(counts, src[s][1], s, K, rho, "rank_wide", 0.6, route_pos=src[s][4],
+                          offsets=src[s][3], workspace=src[s][5]) for s in range(M)]
+    split = plans[0].send_counts()                      # [source, destination] rows
+    sends = []
+    for s in range(M):
+        buf = torch.empty((int(split[s].sum()), d), dtype=torch.bfloat16, device="cuda")
+        ep.rows_copy(src[s][0], buf, T * K, src_div=K, dst_index=plans[s].send_pos,
+                     workspace=src[s][5])
+        sends.append(buf)
+    start = torch.cat([torch.zeros((M, 1), dtype=torch.int64), split.cumsum(1)], 1)
+    packed = []
+    for q in range(M):
+        # the all-to-all: destination q receives source s's block for q, sources in order
+        recv = torch.cat([sends[s][int(start[s, q]):int(start[s, q + 1])] for s in range(M)])
+        rr = ep.recv_rows(plans[q], workspace=src[q][5])
+        rows = torch.zeros((int(plans[q].R_keep[q]), d), dtype=torch.bfloat16, device="cuda")
+        ep.rows_copy(recv, rows, recv.shape[0], dst_index=rr, workspace=src[q][5])
+        packed.append((rows, rr, recv.shape[0]))
+    torch.cuda.synchronize()
+    # every kept route's row sits at its destination row
+    for s in range(M):
+        x, idx = src[s][0], src[s][1]
+        dst = plans[s].dst_row
+        kept = dst >= 0
+        q_of = torch.tensor(rho, device="cuda")[idx.long()]
+        for q in range(M):
+            sel = kept & (q_of == q)
+            t = torch.nonzero(sel)[:, 0]
+            assert torch.equal(packed[q][0][dst[sel].long()], x[t])
+        if M > 1:
+            assert int((~kept).sum()) > 0   # the budget dropped some routes
+    # the return path: each destination's outputs (2 x its rows) go back to the sources
+    backs = {}
+    for q in range(M):
+        rows, rr, n = packed[q]
+        f = rows * 2
+        send_back = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+        ep.rows_copy(f, send_back, n, src_index=rr, workspace=src[q][5])
+        backs[q] = send_back
+    rstart = torch.cat([torch.zeros((1, M), dtype=torch.int64), split.cumsum(0)], 0)
+    for s in range(M):
+        back = torch.cat([backs[q][int(rstart[s, q]):int(rstart[s + 1, q])] for q in range(M)])
+        out = torch.full((T * K, d), 5.0, dtype=torch.bfloat16, device="cuda")
+        ep.rows_copy(back, out, T * K, src_index=plans[s].send_pos, zero_missing=True,
+                     workspace=src[s][5])
+        torch.cuda.synchronize()
+        kept = (plans[s].dst_row >= 0).reshape(-1)
+        want = (src[s][0] * 2).repeat_interleave(K, 0)
+        want[~kept] = 0
+        assert torch.equal(out, want)
+    for s in range(M):
+        assert moe.moe_read_status(src[s][5]) == 0
