@@ -137,3 +137,83 @@ def test_device_exchange_of_m_sources(M):
         assert torch.equal(out, want)
     for s in range(M):
         assert moe.moe_read_status(src[s][5]) == 0
+
+
+def _ep_nccl_worker(port, q):
+    """One NCCL rank: the expert-parallel forward with the library's kernels throughout."""
+    import sys
+    from tests.conftest import ROOT
+    sys.path.insert(0, ROOT)
+    try:
+        import torch.distributed as dist
+        torch.cuda.set_device(0)
+        dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0,
+                                world_size=1)
+        spec = CONFIGS["dsv3"].replace(T=600, d_model=256, N=32, K=4, d_expert=128,
+                                       d_shared=128, cap_policy="rank_wide",
+                                       capacity_factor=0.7, num_ranks=1)
+        T, K, N, d = spec.T, spec.K, spec.N, spec.d_model
+        inp = make_inputs(spec, "cuda")
+        layer = moe.MoELayer(moe.config_from_spec(spec), inp, "cuda")
+        y_ref = layer.forward(inp["x"], logits=False).clone()
+        cfg, ws, x = layer.cfg, layer.ws, inp["x"]
+        i32 = dict(dtype=torch.int32, device="cuda")
+        idx, cnt, ck, off = (torch.empty((T, K), **i32), torch.empty(N, **i32),
+                             torch.empty(N, **i32), torch.empty(N + 1, **i32))
+        rpos, psrc = torch.empty((T, K), **i32), torch.empty(T * K, **i32)
+        w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        sc = torch.empty(T, dtype=torch.float32, device="cuda")
+        moe.moe_route(cfg, x, inp["W_router"], None, None, None, idx, w, sc, None, ws)
+        moe.moe_permute(moe.copy_config(cfg, cap_policy=0), None, idx, cnt, ck, off, rpos, psrc,
+                        None, None, None, None, ws)
+        g = torch.empty((T, d), dtype=torch.float16, device="cuda")
+        moe.moe_shared_mlp(cfg, x, inp["Ws_gate"], inp["Ws_up"], layer.down["Ws_down"], g, ws)
+
+        def expert_fn(rows, local_off):
+            buf = torch.zeros((T * K, d), dtype=torch.bfloat16, device="cuda")
+            buf[:rows.shape[0]] = rows
+            f = torch.zeros((T * K, d), dtype=torch.float16, device="cuda")
+            moe.moe_grouped_swiglu(cfg, buf, local_off.to(torch.int32).cuda(), None,
+                                   inp["W_gate"], inp["W_up"], layer.down["W_down"], f, ws)
+            return f[:rows.shape[0]]
+
+        def merge_fn(route_out, kept):
+            rp = torch.where(kept, torch.arange(T * K, **i32).view(T, K), -1).contiguous()
+            y = torch.empty((T, d), dtype=torch.float32, device="cuda")
+            moe.moe_combine(cfg, route_out, rp, w, g, sc, y)
+            return y
+
+        y, plan = ep.ep_layer_forward(x, idx, [0] * N, K, expert_fn, merge_fn, cnt, "rank_wide",
+                                      0.7, route_pos=rpos, offsets=off, workspace=ws)
+        torch.cuda.synchronize()
+        dropped = int((plan.dst_row < 0).sum())
+        q.put(("ok", bool(torch.equal(y, y_ref)), float((y - y_ref).abs().max()), dropped,
+               moe.moe_read_status(ws)))
+        dist.destroy_process_group()
+    except Exception:
+        import traceback
+        q.put(("error", traceback.format_exc()))
+
+
+def test_expert_parallel_forward_on_one_nccl_rank_equals_the_fused_layer():
+    """ep_layer_forward over NCCL with one rank and the library's kernels for every step
+    (router, capacity-free permutation, keep matrix, send and receive layouts, row copies,
+    grouped experts, shared expert, combine) gives the fused layer's y under the same
+    rank-wide budget bit for bit: the same kept rows in the same packed order."""
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    ctx = torch.multiprocessing.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_ep_nccl_worker, args=(port, q))
+    p.start()
+    res = q.get(timeout=300)
+    p.join(timeout=60)
+    assert res[0] == "ok", res[1]
+    _, equal, err, dropped, status = res
+    assert status == 0
+    assert dropped > 0             # the budget is binding
+    assert equal, f"max |y_ep - y_layer| = {err}"
+    assert p.exitcode == 0
