@@ -278,3 +278,34 @@ def test_layer_full_size_sampled(name):
     assert err <= TOL["bf16"], f"{name}: rel err {err:.3e}"
     if spec.cap_policy != "none":
         assert rt.drops["dropped_routes"] > 0
+
+
+@pytest.mark.parametrize("N,K,T,score", [(129, 8, 129, "sigmoid"), (256, 1, 127, "sigmoid"),
+                                         (200, 3, 128, "softmax"), (256, 8, 1, "softmax")])
+def test_wide_router_shapes(N, K, T, score):
+    """The CTA-pair router at its edges: 129 experts (the upper half holds one column), top-1
+    (two-entry lists), an odd K, one token, and token counts around the 128-token pair."""
+    spec = C["dsv3"].replace(T=T, d_model=192, N=N, K=K, d_expert=128, d_shared=128, score=score,
+                             alpha=float(K))
+    inp = make_inputs(spec, "cuda")
+    layer = run_layer(spec, inp)
+    assert layer.status() == 0
+    check_logits(layer, spec, host(inp))
+    check_routing_exact(layer, spec)
+
+
+def test_wide_router_ties_across_halves():
+    """Equal keys spanning the two TMEM lanes of a token: experts 130-135 share the largest
+    logit and every other expert the same smaller one.  K = 8 takes 130-135, then the two
+    lowest-index experts of the rest (0 and 1, from the lower half)."""
+    spec = C["dsv3"].replace(T=300, d_model=192, N=256, K=8, d_expert=128, d_shared=128)
+    inp = make_inputs(spec, "cuda")
+    W = torch.zeros_like(inp["W_router"])
+    W[130:136] = 0.01
+    inp["W_router"] = W
+    inp["x"] = inp["x"].abs() + 0.5          # every token's logit of 130-135 is positive
+    layer = run_layer(spec, inp)
+    assert layer.status() == 0
+    rt = check_routing_exact(layer, spec)
+    want = np.array(list(range(130, 136)) + [0, 1])
+    assert (rt.topk_idx == want[None, :]).all()
