@@ -323,6 +323,30 @@ def stage_algorithmic_bytes(spec, kept: int) -> int:
     return int(kept * d * b + 3 * N * d * dr * b + 2 * kept * dr * b + kept * d * b)
 
 
+def stage_roofline(spec, kept: int, g_ms: float, pk) -> dict:
+    """The grouped stage against the roof that binds it.  Its algorithmic intensity (routed
+    expert FLOP over the stage's algorithmic bytes) against the measured ridge (bf16 peak over
+    HBM rate) decides: below the ridge the stage is bound by HBM and is measured in GB/s,
+    above it by the tensor cores in TFLOP/s.  Both fractions are reported."""
+    flops = 6.0 * spec.d_model * spec.d_expert * kept
+    nbytes = stage_algorithmic_bytes(spec, kept)
+    sec = g_ms / 1e3
+    ai = flops / nbytes
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    tf = flops / sec / 1e12
+    gbs = nbytes / sec / 1e9
+    out = {"intensity_flop_per_byte": ai, "ridge_flop_per_byte": ridge,
+           "frac_tensor": tf / pk["bf16_tflops"], "frac_hbm": gbs / pk["hbm_gbs"]}
+    if ai < ridge:
+        out.update({"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / pk["hbm_gbs"]})
+    else:
+        out.update({"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": tf / pk["bf16_tflops"],
+                    "frac_sustained": tf / pk["bf16_tflops_sustained"]})
+    return out
+
+
 def launches_per_step(spec, sms: int = 152) -> int:
     """Kernels moe_layer_forward launches for a layer (counted from the library's launch
     sequence): router 1; permutation 2 (counting, capacity and placement in one launch while
@@ -453,6 +477,7 @@ def summarize(spec, r, args, world: int, pk):
     return {"ms_per_step": ms, "tokens_per_s": job_tokens_per_s(world, spec.T, args.steps, r["total_ms"]),
             "tflops": tflops, "pct_bf16_peak": 100.0 * tflops / pk["bf16_tflops"],
             "grouped_tflops": g_tf, "grouped_frac": g_tf / pk["bf16_tflops"],
+            "grouped_roofline": stage_roofline(spec, kept, g_ms, pk),
             "stages_ms": r["stage_ms"], "kept_routes": kept}
 
 
@@ -665,7 +690,10 @@ def main():
         clk = rr["clocks"] or {}
         per_config[name] = {"ms_per_step": sm["ms_per_step"], "tokens_per_s": sm["tokens_per_s"],
                             "tflops": sm["tflops"], "pct_bf16_peak": sm["pct_bf16_peak"],
-                            "grouped_frac": sm["grouped_frac"], "stages_ms": sm["stages_ms"],
+                            "grouped_frac": sm["grouped_frac"],
+                            "grouped_roofline": {k: sm["grouped_roofline"][k]
+                                                 for k in ("bound", "frac", "frac_tensor", "frac_hbm")},
+                            "stages_ms": sm["stages_ms"],
                             "kept_routes": sm["kept_routes"],
                             "clocks": {k: clk.get(k) for k in ("sm_mhz", "reasons", "samples")}}
         del rr
@@ -681,13 +709,12 @@ def main():
                               "stage events recorded inside it"),
         "tflops": head["tflops"], "pct_bf16_peak": head["pct_bf16_peak"],
         "stages_ms": head["stages_ms"],
-        "roofline": {"kernel": "grouped_swiglu stage (tcgen05 gate/up + down GEMM launches over packed segments)",
-                     "bound": "tensor", "achieved": head["grouped_tflops"], "peak": pk["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": head["grouped_frac"],
-                     "frac_sustained": head["grouped_tflops"] / pk["bf16_tflops_sustained"],
-                     "peak_source": pk["source"], "traffic": stage_traffic(spec.name),
-                     "traffic_unit": "bytes per stage (gate/up + down launches)",
-                     "algorithmic_bytes": stage_algorithmic_bytes(spec, kept)},
+        "roofline": dict({"kernel": "grouped_swiglu stage (tcgen05 gate/up + down GEMM launches "
+                                    "over packed segments)"},
+                         **head["grouped_roofline"],
+                         peak_source=pk["source"], traffic=stage_traffic(spec.name),
+                         traffic_unit="bytes per stage (gate/up + down launches)",
+                         algorithmic_bytes=stage_algorithmic_bytes(spec, kept)),
         "e2e": e2e,
         "gpu_launches": launches_per_step(
             spec, torch.cuda.get_device_properties(dev).multi_processor_count) * args.steps,
