@@ -347,6 +347,17 @@ def stage_roofline(spec, kept: int, g_ms: float, pk) -> dict:
     return out
 
 
+def experts_window(spec, kept: int, stage_ms: dict, world: int, pk) -> dict:
+    """All expert GEMM FLOP (routed and shared) over the window they run in: from the start
+    of the layer to the end of the routed experts (the router, the permutation and the
+    routed experts on the caller's stream; the shared expert beside them on the second
+    stream).  The grouped stage alone counts only routed FLOP while a large shared expert's
+    tail runs inside it."""
+    ms = stage_ms["route"] + stage_ms["permute"] + stage_ms["grouped_swiglu"]
+    tf = world * spec.expert_flops(kept) / (ms / 1e3) / 1e12
+    return {"ms": ms, "tflops": tf, "frac_tensor": tf / pk["bf16_tflops"]}
+
+
 def launches_per_step(spec, sms: int = 152) -> int:
     """Kernels moe_layer_forward launches for a layer (counted from the library's launch
     sequence): router 1; permutation 2 (counting, capacity and placement in one launch while
@@ -478,6 +489,7 @@ def summarize(spec, r, args, world: int, pk):
             "tflops": tflops, "pct_bf16_peak": 100.0 * tflops / pk["bf16_tflops"],
             "grouped_tflops": g_tf, "grouped_frac": g_tf / pk["bf16_tflops"],
             "grouped_roofline": stage_roofline(spec, kept, g_ms, pk),
+            "experts_window": experts_window(spec, kept, r["stage_ms"], world, pk),
             "stages_ms": r["stage_ms"], "kept_routes": kept}
 
 
@@ -693,6 +705,7 @@ def main():
                             "grouped_frac": sm["grouped_frac"],
                             "grouped_roofline": {k: sm["grouped_roofline"][k]
                                                  for k in ("bound", "frac", "frac_tensor", "frac_hbm")},
+                            "experts_window": sm["experts_window"],
                             "stages_ms": sm["stages_ms"],
                             "kept_routes": sm["kept_routes"],
                             "clocks": {k: clk.get(k) for k in ("sm_mhz", "reasons", "samples")}}
@@ -709,6 +722,7 @@ def main():
                               "stage events recorded inside it"),
         "tflops": head["tflops"], "pct_bf16_peak": head["pct_bf16_peak"],
         "stages_ms": head["stages_ms"],
+        "experts_window": head["experts_window"],
         "roofline": dict({"kernel": "grouped_swiglu stage (tcgen05 gate/up + down GEMM launches "
                                     "over packed segments)"},
                          **head["grouped_roofline"],
