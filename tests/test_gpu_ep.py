@@ -9,6 +9,8 @@ The exchange kernels (send positions, receive rows, indexed row copies) are chec
 running the dispatch and the return of M sources on one GPU, the all-to-all itself replaced
 by slicing the send buffers.
 """
+import ctypes
+
 import pytest
 import torch
 
@@ -217,3 +219,39 @@ def test_expert_parallel_forward_on_one_nccl_rank_equals_the_fused_layer():
     assert dropped > 0             # the budget is binding
     assert equal, f"max |y_ep - y_layer| = {err}"
     assert p.exitcode == 0
+
+
+def test_device_rows_copy_and_send_pos_bounds():
+    """An index past a buffer records MOE_ERR_DEVICE_BOUNDS in the workspace and skips that
+    row (the others are copied); an expert id out of range gets send position -1 with the
+    same status."""
+    from routing_shared_expert_gb300 import _native as nat
+    spec = CONFIGS["olmo"].replace(T=64, d_model=128, N=8, K=2, d_expert=128, d_shared=128)
+    ws = moe.alloc_workspace(moe.config_from_spec(spec))
+    src = torch.arange(4 * 8, dtype=torch.float32, device="cuda").reshape(4, 8)
+    dst = torch.full((4, 8), -1.0, device="cuda")
+    di = torch.tensor([3, 9, 1, 0], dtype=torch.int32, device="cuda")   # 9 is past dst
+    ep.rows_copy(src, dst, 4, dst_index=di, workspace=ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_status(ws) == -6  # MOE_ERR_DEVICE_BOUNDS
+    want = torch.full((4, 8), -1.0, device="cuda")
+    want[3], want[1], want[0] = src[0], src[2], src[3]
+    assert torch.equal(dst, want)
+    assert moe.moe_read_status(ws) == 0                                 # read clears it
+    # send positions with one expert id out of range
+    rho = [0, 1] * 4
+    keep = torch.tensor([[2, 1, 1, 0, 0, 0, 0, 0], [0] * 8], dtype=torch.int32, device="cuda")
+    off = torch.zeros((2, 8), dtype=torch.int32, device="cuda")
+    idx = torch.tensor([[0, 1], [0, 12]], dtype=torch.int32, device="cuda")
+    dst_row = torch.tensor([[0, 0], [1, -1]], dtype=torch.int32, device="cuda")
+    pos = torch.empty((2, 2), dtype=torch.int32, device="cuda")
+    cnt = torch.empty(2, dtype=torch.int32, device="cuda")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = nat.library().moe_ep_send_pos(2, 0, 2, 8, 2, (ctypes.c_int32 * 8)(*rho), p(idx), p(keep),
+                                       p(off), p(dst_row), p(pos), p(cnt), p(ws), ws.numel(),
+                                       nat._stream(None))
+    assert st == 0
+    torch.cuda.synchronize()
+    # experts of rank 0: 0, 2 (keep 2, 1) -> send rows 0-2; rank 1: 1 (keep 1) -> row 3
+    assert pos.tolist() == [[0, 3], [1, -1]] and cnt.tolist() == [3, 1]
+    assert moe.moe_read_status(ws) == -6  # MOE_ERR_DEVICE_BOUNDS
