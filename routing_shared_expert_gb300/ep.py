@@ -215,7 +215,9 @@ def ep_layer_forward(x_local: torch.Tensor, topk_idx: torch.Tensor, rho: List[in
                      capacity_factor: float = 1.0, group=None, **plan_kw):
     """Steps 2-5 for this rank's tokens, given its routing (topk_idx [T, K] and the count
     vector of its requests).  expert_fn(rows, local_offsets) computes the outputs of this
-    rank's packed buffer (local experts in ascending index, segments local_offsets);
+    rank's packed buffer (local experts in ascending index, segments local_offsets; rows
+    holds exactly R_keep[rank] rows, so a grouped GEMM whose configuration expects a buffer
+    of T' K rows gets them copied into one of that size);
     merge_fn(route_out [T*K, d], kept [T, K]) merges them into y (Eq. 80).
     Returns (y, plan)."""
     import torch.distributed as dist
