@@ -93,14 +93,105 @@ __device__ __forceinline__ float lth_largest32(float (&v)[32]) {
   return v[L - 1];
 }
 
+// Pass 1 over one 32-column chunk: the logits z (+ the logit bias), the logits output, the
+// running maximum logit and, per column slot, the largest key (z + the selection-only
+// bias).  BIAS / SEL: the layer has that bias; FULL: every column of the chunk is below N
+// (no range checks).  NaN keys are ignored by the maxima.
+template <bool BIAS, bool SEL, bool FULL>
+__device__ __forceinline__ void chunk_pass1(const RouteParams& p, const float* s_bias,
+                                            const float* s_sel, int c0, const uint32_t (&r)[32],
+                                            float* lrow, float (&slot_max)[32], float& zmax) {
+  float z[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    z[i] = __uint_as_float(r[i]);
+    if (BIAS && (FULL || c0 + i < p.N)) z[i] += s_bias[c0 + i];
+  }
+  if (lrow) {
+    if (FULL && (p.N & 3) == 0 && (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0) {
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        *reinterpret_cast<float4*>(lrow + c0 + 4 * v) =
+            make_float4(z[4 * v], z[4 * v + 1], z[4 * v + 2], z[4 * v + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (FULL || c0 + i < p.N) lrow[c0 + i] = z[i];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (FULL || c0 + i < p.N) {
+      zmax = fmaxf(zmax, z[i]);
+      slot_max[i] = fmaxf(slot_max[i], SEL ? z[i] + s_sel[c0 + i] : z[i]);
+    }
+}
+
+// Pass 2 over one chunk: the candidates whose key is not below thr, inserted in ascending
+// column order.  Their keys and logits are staged in this thread's shared-memory scratch
+// rows (entry i at i * stride; the key row only when it differs from the logit): the
+// candidates are picked by a run-time index, which on registers would place the chunk in
+// local memory.  The tokens of a warp insert at different candidates, so the loop runs
+// over a mask rather than branching per candidate; it runs as often as the warp's busiest
+// token has candidates.
+template <int L, bool BIAS, bool SEL, bool FULL>
+__device__ __forceinline__ void chunk_pass2(const RouteParams& p, const float* s_bias,
+                                            const float* s_sel, int c0, const uint32_t (&r)[32],
+                                            float thr, float* s_cv, float* s_z, int stride,
+                                            float (&bv)[L], float (&bz)[L], int (&bi)[L]) {
+  uint32_t mask = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float z = __uint_as_float(r[i]);
+    if (BIAS && (FULL || c0 + i < p.N)) z += s_bias[c0 + i];
+    float cv = z;
+    if (SEL && (FULL || c0 + i < p.N)) cv = z + s_sel[c0 + i];
+    s_z[i * stride] = z;
+    if (SEL) s_cv[i * stride] = cv;
+    if ((FULL || c0 + i < p.N) && !(cv < thr)) mask |= 1u << i;
+  }
+  while (mask != 0u) {
+    const int i = __ffs(mask) - 1;
+    mask &= mask - 1u;
+    const float z = s_z[i * stride];
+    list_insert<L>(SEL ? s_cv[i * stride] : z, z, c0 + i, bv, bz, bi);
+  }
+}
+
+template <int L, bool BIAS, bool SEL, class Load32>
+__device__ __forceinline__ void list_columns_impl(const RouteParams& p, const float* s_bias,
+                                                  const float* s_sel, int c_lo, int c_hi,
+                                                  float* lrow, float* s_cv, float* s_z,
+                                                  int stride, Load32&& load32, float (&bv)[L],
+                                                  float (&bz)[L], int (&bi)[L], float& zmax) {
+  float slot_max[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) slot_max[i] = -INFINITY;
+  for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+    uint32_t r[32];
+    load32(c0, r);
+    if (c0 + 32 <= p.N)
+      chunk_pass1<BIAS, SEL, true>(p, s_bias, s_sel, c0, r, lrow, slot_max, zmax);
+    else
+      chunk_pass1<BIAS, SEL, false>(p, s_bias, s_sel, c0, r, lrow, slot_max, zmax);
+  }
+  const float thr = lth_largest32<L>(slot_max);
+  for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+    uint32_t r[32];
+    load32(c0, r);
+    if (c0 + 32 <= p.N)
+      chunk_pass2<L, BIAS, SEL, true>(p, s_bias, s_sel, c0, r, thr, s_cv, s_z, stride, bv, bz, bi);
+    else
+      chunk_pass2<L, BIAS, SEL, false>(p, s_bias, s_sel, c0, r, thr, s_cv, s_z, stride, bv, bz, bi);
+  }
+}
+
 // Selection over the columns [c_lo, c_hi) (c_lo a multiple of 32) of one token: the keys
 // z (+ the selection-only bias), the logits output row (when lrow is given), the maximum
 // logit and the sorted list.  load32(c0, r) fills r[0..31] with the fp32 accumulators (bit
 // patterns) of columns c0 .. c0 + 31; every thread of the warp calls it with the same c0
 // (the tensor-memory load it may wrap is warp-collective).  s_cv and s_z are this thread's
-// 32-entry scratch rows in shared memory, entry i at index i * stride: the candidates are
-// picked by a run-time index, which on registers would place the chunk in local memory
-// (behind the large shared-memory carve-out of these kernels, a round trip to L2 each).
+// 32-entry scratch rows in shared memory, entry i at index i * stride.
 //
 // Two passes.  The first keeps, for each of the 32 column slots of a chunk, the largest
 // key over the chunks; those are maxima of distinct columns, so the L-th largest of them
@@ -108,65 +199,30 @@ __device__ __forceinline__ float lth_largest32(float (&v)[32]) {
 // second pass inserts, in ascending column order, only the columns whose key is not below
 // that threshold (a handful), so the result is the selection over all columns with the
 // lower index first on equal keys.  A single pass would insert every candidate of the
-// first chunk (the list starts empty), each insertion a chain of dependent steps.
+// first chunk (the list starts empty), each insertion a chain of dependent steps.  The
+// layer's biases pick one of four compiled variants, so a layer without them issues no
+// instruction for them.
 template <int L, class Load32>
 __device__ __forceinline__ void list_columns(const RouteParams& p, const float* s_bias,
                                              const float* s_sel, int c_lo, int c_hi, float* lrow,
                                              float* s_cv, float* s_z, int stride, Load32&& load32,
                                              float (&bv)[L], float (&bz)[L], int (&bi)[L],
                                              float& zmax) {
-  const bool sel = p.selection_bias != nullptr;
-  const bool bias = p.router_bias != nullptr;   // the shared-memory loads only when given
-  float slot_max[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) slot_max[i] = -INFINITY;
-  for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-    uint32_t r[32];
-    load32(c0, r);
-    float z[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      z[i] = __uint_as_float(r[i]) + (bias && c0 + i < p.N ? s_bias[c0 + i] : 0.f);
-    if (lrow) {
-      if (c0 + 32 <= p.N && (p.N & 3) == 0 && (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0) {
-#pragma unroll
-        for (int v = 0; v < 8; ++v)
-          *reinterpret_cast<float4*>(lrow + c0 + 4 * v) =
-              make_float4(z[4 * v], z[4 * v + 1], z[4 * v + 2], z[4 * v + 3]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (c0 + i < p.N) lrow[c0 + i] = z[i];
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (c0 + i < p.N) {
-        zmax = fmaxf(zmax, z[i]);
-        slot_max[i] = fmaxf(slot_max[i], sel ? z[i] + s_sel[c0 + i] : z[i]);   // NaN ignored
-      }
-  }
-  const float thr = lth_largest32<L>(slot_max);
-  for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-    uint32_t r[32];
-    load32(c0, r);
-    uint32_t mask = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float z = __uint_as_float(r[i]) + (bias && c0 + i < p.N ? s_bias[c0 + i] : 0.f);
-      const float cv = sel && c0 + i < p.N ? z + s_sel[c0 + i] : z;
-      s_z[i * stride] = z;
-      s_cv[i * stride] = cv;
-      if (c0 + i < p.N && !(cv < thr)) mask |= 1u << i;
-    }
-    // The tokens of a warp insert at different candidates, so the loop runs over a mask
-    // rather than branching per candidate; it runs as often as the warp's busiest token
-    // has candidates.
-    while (mask != 0u) {
-      const int i = __ffs(mask) - 1;
-      mask &= mask - 1u;
-      list_insert<L>(s_cv[i * stride], s_z[i * stride], c0 + i, bv, bz, bi);
-    }
+  const bool bias = p.router_bias != nullptr, sel = p.selection_bias != nullptr;
+  if (bias) {
+    if (sel)
+      list_columns_impl<L, true, true>(p, s_bias, s_sel, c_lo, c_hi, lrow, s_cv, s_z, stride,
+                                       load32, bv, bz, bi, zmax);
+    else
+      list_columns_impl<L, true, false>(p, s_bias, s_sel, c_lo, c_hi, lrow, s_cv, s_z, stride,
+                                        load32, bv, bz, bi, zmax);
+  } else {
+    if (sel)
+      list_columns_impl<L, false, true>(p, s_bias, s_sel, c_lo, c_hi, lrow, s_cv, s_z, stride,
+                                        load32, bv, bz, bi, zmax);
+    else
+      list_columns_impl<L, false, false>(p, s_bias, s_sel, c_lo, c_hi, lrow, s_cv, s_z, stride,
+                                         load32, bv, bz, bi, zmax);
   }
 }
 
