@@ -227,18 +227,31 @@ __device__ __forceinline__ void list_columns(const RouteParams& p, const float* 
 }
 
 // Sum of exp(z - m) over the columns [c_lo, c_hi) below N (the softmax denominator's part).
-template <class Load32>
-__device__ __forceinline__ float exp_sum_columns(const RouteParams& p, const float* s_bias,
-                                                 int c_lo, int c_hi, float m, Load32&& load32) {
+template <bool BIAS, class Load32>
+__device__ __forceinline__ float exp_sum_impl(const RouteParams& p, const float* s_bias, int c_lo,
+                                              int c_hi, float m, Load32&& load32) {
   float s = 0.f;
   for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
     uint32_t r[32];
     load32(c0, r);
+    if (c0 + 32 <= p.N) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (c0 + i < p.N) s += expf(__uint_as_float(r[i]) + s_bias[c0 + i] - m);
+      for (int i = 0; i < 32; ++i)
+        s += expf(__uint_as_float(r[i]) + (BIAS ? s_bias[c0 + i] : 0.f) - m);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (c0 + i < p.N) s += expf(__uint_as_float(r[i]) + (BIAS ? s_bias[c0 + i] : 0.f) - m);
+    }
   }
   return s;
+}
+
+template <class Load32>
+__device__ __forceinline__ float exp_sum_columns(const RouteParams& p, const float* s_bias,
+                                                 int c_lo, int c_hi, float m, Load32&& load32) {
+  return p.router_bias ? exp_sum_impl<true>(p, s_bias, c_lo, c_hi, m, load32)
+                       : exp_sum_impl<false>(p, s_bias, c_lo, c_hi, m, load32);
 }
 
 // Whether the scores need the softmax denominator over all N experts.
