@@ -471,8 +471,11 @@ def max_mean_imbalance(x) -> float:
 
 
 def entropy_deficit(x) -> float:
-    """I_H(x) = 1 - H(pi) / log n with pi = x / sum x ("Section 10.2")."""
+    """I_H(x) = 1 - H(pi) / log n with pi = x / sum x ("Section 10.2").  With one expert
+    (n = 1) the ratio is 0/0; a single expert cannot be imbalanced, so the deficit is 0."""
     x = f64(x)
+    if len(x) < 2:
+        return 0.0
     pi = x / x.sum()
     nz = pi[pi > 0]
     return float(1.0 + (nz * np.log(nz)).sum() / np.log(len(x)))

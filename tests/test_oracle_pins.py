@@ -477,6 +477,7 @@ def test_eq52_many_expert_limit(golden):
 
 def test_entropy_deficit_and_cv_closed_forms():
     assert O.entropy_deficit(np.full(8, 5)) == 0.0
+    assert O.entropy_deficit(np.array([7])) == 0.0                # one expert: no deficit
     assert abs(O.entropy_deficit(np.eye(8)[3]) - 1.0) < 1e-15
     x = np.array([1, 1, 0, 0])
     assert abs(O.entropy_deficit(x) - 0.5) < 1e-15            # log 2 / log 4
