@@ -367,6 +367,64 @@ def launches_per_step(spec, sms: int = 152) -> int:
     return 1 + permute + 2 + (2 if spec.d_shared > 0 else 0) + 1
 
 
+# ----------------------------------------------------------------- balance
+def bench_balance(args, spec, config, dev) -> int:
+    """The load-balancing side outputs of one routed batch (moe_balance_stats: P, f and the
+    statistics of Eq. 22, 27, 30 and 39 and the entropy deficit) and one bias-controller step
+    (moe_bias_update, Eq. 37): three launches, timed together per call with CUDA events
+    (queued behind a device-side wait, so the interval excludes host launch cost), L2
+    flushed between calls, on the routing of the workload's own router and permutation.  They read only the
+    routing (logits [T][N] fp32 and the counts), so the expert widths are reduced to keep
+    the device footprint small."""
+    import torch
+    import routing_shared_expert_gb300 as moe
+    from routing_shared_expert_gb300 import _native as nat
+    from workloads import make_inputs
+    sp = spec.replace(d_expert=128, d_shared=128 if spec.d_shared else 0)
+    inp = make_inputs(sp, dev, seed=0)
+    layer = moe.MoELayer(moe.config_from_spec(sp), inp, dev)
+    layer.forward(inp["x"], logits=True)
+    o, c, ws = layer.out, layer.cfg, layer.ws
+    f32 = dict(dtype=torch.float32, device=dev)
+    P, f, stats = torch.empty(sp.N, **f32), torch.empty(sp.N, **f32), torch.empty(len(nat.STATS), **f32)
+    bias = torch.zeros(sp.N, **f32)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        nat.moe_balance_stats(c, o["logits"], o["counts_req"], o["counts_keep"], o["R_req"],
+                              o["R_keep"], P, f, stats, ws)
+        nat.moe_bias_update(sp.N, o["counts_req"], 1e-3, bias)
+
+    times = []
+    for i in range(args.warmup + args.steps):
+        flush.add_(1)
+        # a device-side wait ahead of the start event, so that the three launches are queued
+        # before the GPU reaches it and the interval holds device time only
+        torch.cuda._sleep(2_000_000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1) * 1e3)
+    if layer.status() != 0:
+        raise RuntimeError(f"layer status {layer.status()}")
+    us = statistics.median(times)
+    M = sp.num_ranks
+    nbytes = sp.T * sp.N * 4 + 2 * sp.N * 4 + 2 * M * 4 + 2 * sp.N * 4 + len(nat.STATS) * 4 + 2 * sp.N * 4
+    pk = peaks()
+    gbs = nbytes / (us / 1e6) / 1e9
+    print(json.dumps({"mode": "balance", "workload": spec.name, "us_per_call": us,
+                      "calls": args.steps, "gpu_launches_per_call": 3, "algorithmic_bytes": nbytes,
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
+                                   "unit": "GB/s", "frac": gbs / pk["hbm_gbs"]},
+                      "stats": {k: float(v) for k, v in zip(nat.STATS, stats.cpu().tolist())},
+                      "config": dict(config, note="expert widths reduced to 128 (the statistics "
+                                                  "read only the routing)")}), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------- backward
 
 def bench_backward(args, spec, layer, x, config, dev):
@@ -518,9 +576,10 @@ def main():
     ap.add_argument("--override", default="", metavar="K=V,...",
                     help="change integer fields of the workload (e.g. N=32,T=1024: a smaller layer "
                          "of the same shape per expert, for profiler captures)")
-    ap.add_argument("--mode", choices=["forward", "backward"], default="forward",
+    ap.add_argument("--mode", choices=["forward", "backward", "balance"], default="forward",
                     help="backward: time moe_layer_backward (router coefficients fixed) on the "
-                         "routing of one forward call, instead of the forward benchmark line")
+                         "routing of one forward call, instead of the forward benchmark line; "
+                         "balance: time the load-balancing statistics and the bias-controller step")
     ap.add_argument("--router-grad", action="store_true",
                     help="with --mode backward: include the gradient through the router coefficients")
     ap.add_argument("--forward-only", type=int, default=0, metavar="R",
@@ -612,6 +671,8 @@ def main():
         inp = make_inputs(spec, dev, seed=0)
         layer = moe.MoELayer(moe.config_from_spec(spec), inp, dev)
         return bench_backward(args, spec, layer, inp["x"], config, dev)
+    if args.mode == "balance":
+        return bench_balance(args, spec, config, dev)
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     pk = peaks()

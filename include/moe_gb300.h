@@ -328,13 +328,14 @@ typedef enum {
   MOE_STAT_IMAX_KEEP = 2,      /* I_max of C^keep; NaN without counts_keep */
   MOE_STAT_IMAX_RANK_REQ = 3,  /* I_max of R^req; NaN without R_req */
   MOE_STAT_IMAX_RANK_KEEP = 4, /* I_max of R^keep; NaN without R_keep */
-  MOE_STAT_IH_REQ = 5,         /* entropy deficit 1 - H(pi)/log N of C^req (Section 10.2) */
+  MOE_STAT_IH_REQ = 5,         /* entropy deficit 1 - H(pi)/log N of C^req (Section 10.2); 0 for N = 1 */
   MOE_STAT_IH_KEEP = 6,        /* entropy deficit of C^keep; NaN without counts_keep */
   MOE_STAT_CV_REQ = 7,         /* coefficient of variation of C^req */
   MOE_STAT_NEVER_SELECTED = 8, /* experts with C^req = 0 */
   MOE_STAT_DROP_FRACTION = 9,  /* delta_route = sum D / (K T) (Eq. 27); NaN without counts_keep */
   MOE_STAT_COUNT = 10
 } moe_stat;
+/* I_max, I_H and the coefficient of variation of a load vector that sums to 0 are reported as 0. */
 
 /* Load-balancing statistics of one routed batch (Section 10.5, Eq. 30 and 38; Section 10.2,
  * Eq. 22; Eq. 27).  logits [T][N] fp32 as moe_route wrote them (may be NULL: no P, no LBL);

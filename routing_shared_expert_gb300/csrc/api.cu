@@ -281,7 +281,7 @@ Layout make_layout(const moe_config& c) {
   L.R_req = take(M * 4);
   L.R_keep = take(M * 4);
   L.drop_stats = take(16);
-  L.score_partial = take(static_cast<size_t>(L.hist_tiles) * N * 4);
+  L.score_partial = take(static_cast<size_t>((c.T + kScoreTile - 1) / kScoreTile) * N * 4);
   L.x_perm = take(T * K * d * eb);
   L.h = take(T * K * dr * eb);
   L.f = take(T * K * d * out_bytes(c));

@@ -16,6 +16,7 @@ namespace moe {
 constexpr int kMaxExperts = 256;   // N limit (routing keeps up to 8 logits per lane of a warp)
 constexpr int kMaxTopK = 8;
 constexpr int kHistTile = 256;     // tokens per counting tile of the permutation
+constexpr int kScoreTile = 64;     // tokens per partial-sum tile of the balance statistics
 constexpr int kTcRows = 128;       // rows per tensor-core tile (tcgen05 M)
 
 // Byte offsets of the regions of one workspace (each region 256-byte aligned).

@@ -119,3 +119,55 @@ def test_bias_controller_feedback_loop_balances_requests():
         torch.cuda.synchronize()
         np.testing.assert_array_equal(b.cpu().numpy(), O.bias_update(before, counts, 0.05))
     assert last < 0.6 * first, (first, last)
+
+
+@pytest.mark.parametrize("N,T,K,M,score", [
+    (1, 65, 1, 1, "softmax"), (2, 1, 1, 2, "sigmoid"), (3, 129, 2, 3, "softmax"),
+    (5, 700, 2, 2, "sigmoid"), (8, 4100, 2, 8, "softmax"), (12, 63, 3, 4, "sigmoid"),
+    (17, 1000, 4, 1, "softmax"), (33, 257, 4, 5, "sigmoid"), (60, 2049, 4, 6, "softmax"),
+    (100, 64, 6, 7, "sigmoid"), (200, 3000, 8, 16, "softmax"), (256, 9000, 8, 256, "sigmoid"),
+])
+def test_balance_statistics_widths(N, T, K, M, score):
+    """moe_balance_stats alone on seeded logits and routings of every lane mapping of the score
+    pass (1 to 32 lanes per token, 1 to 8 experts per lane), ragged last tiles and T below one
+    tile, against the oracle's statistics."""
+    import routing_shared_expert_gb300 as moe
+    rng = np.random.default_rng(N * 1000 + T)
+    z = (rng.standard_normal((T, N)) * 2.0).astype(np.float32)
+    # top-K sets drawn with a skew, some experts never chosen when N is large
+    w = rng.gamma(0.5, size=N)
+    w[rng.random(N) < 0.1] = 0.0
+    w = (w + 1e-12) / (w + 1e-12).sum()
+    idx = np.stack([rng.choice(N, size=K, replace=False, p=w) for _ in range(T)]).astype(np.int64)
+    req = np.bincount(idx.ravel(), minlength=N).astype(np.int32)
+    # kept counts: at least one route of every requested expert (the oracle's I_max and I_H
+    # are defined for a nonzero load vector)
+    keep = np.maximum((req * rng.uniform(0.5, 1.0, N)).astype(np.int32), np.minimum(req, 1))
+    rho = np.arange(N) % M
+    R_req = np.bincount(rho, weights=req, minlength=M).astype(np.int32)
+    R_keep = np.bincount(rho, weights=keep, minlength=M).astype(np.int32)
+    cfg = moe.make_config(T=T, d_model=64, N=N, K=K, d_expert=128, d_shared=0, dtype="f32",
+                          score=score, shared_mode="none", num_ranks=M, rho=rho.tolist())
+    ws = torch.zeros(moe.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    moe.moe_workspace_init(ws)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda")
+    P = torch.empty(N, dtype=torch.float32, device="cuda")
+    f = torch.empty(N, dtype=torch.float32, device="cuda")
+    st = torch.empty(len(moe.STATS), dtype=torch.float32, device="cuda")
+    moe.moe_balance_stats(cfg, dev(z), dev(req), dev(keep), dev(R_req), dev(R_keep), P, f, st, ws)
+    torch.cuda.synchronize()
+    p = O.normalized_scores(z.astype(np.float64), score)
+    f_ref, P_ref, L_ref = O.lbl_statistics(p, idx, N)
+    np.testing.assert_allclose(P.cpu().numpy(), P_ref, rtol=2e-5, atol=1e-7)
+    np.testing.assert_allclose(f.cpu().numpy(), f_ref, rtol=1e-6)
+    s = dict(zip(moe.STATS, st.cpu().numpy().tolist()))
+    assert abs(s["lbl"] - L_ref) <= 1e-5 * L_ref
+    assert abs(s["imax_req"] - O.max_mean_imbalance(req)) < 1e-5
+    assert abs(s["imax_keep"] - O.max_mean_imbalance(keep)) < 1e-5
+    assert abs(s["imax_rank_req"] - O.max_mean_imbalance(R_req)) < 1e-5
+    assert abs(s["imax_rank_keep"] - O.max_mean_imbalance(R_keep)) < 1e-5
+    assert abs(s["ih_req"] - O.entropy_deficit(req)) < 1e-5
+    assert abs(s["ih_keep"] - O.entropy_deficit(keep)) < 1e-5
+    assert abs(s["cv_req"] - O.coefficient_of_variation(req)) < 1e-5
+    assert s["never_selected"] == O.never_selected(req)
+    assert abs(s["drop_fraction"] - (req.sum() - keep.sum()) / (K * T)) < 1e-6
