@@ -258,8 +258,10 @@ moe_status moe_pack_weights(const void* W, int64_t elements, void* packed, size_
  *   perm_src [K*T]: x_rows is x [T][d] and packed row r is x[perm_src[r]]; the rows are
  *                   gathered inside the GEMM's operand load, so no K*T x d buffer is
  *                   needed.  Same results bit for bit; on a GB300 this form measured about
- *                   2.7x slower on bf16 layers (32 four-row TMA gathers per K step), so
- *                   moe_layer_forward uses the packed form.
+ *                   1.5x slower on bf16 layers with 256-row tiles (the rows arrive by
+ *                   16-byte asynchronous copies, slower than tile loads) and about 2.7x
+ *                   with 128-row tiles (four-row TMA gathers), so moe_layer_forward uses
+ *                   the packed form.
  * Out: f [K*T][d]: f[row] = SwiGLU_e(packed row) for rows < offsets[N], fp32 (fp16 holding
  * f 2^-h_scale_log2 under MOE_H_F16).  The intermediate h = SiLU(x W_g) * (x W_u) is kept
  * in the workspace (bf16 or fp16 per cfg->h_format; W_down is a moe_pack_weights buffer

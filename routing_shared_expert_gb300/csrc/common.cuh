@@ -87,20 +87,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same with acquire at cluster scope: for a phase completed by arrivals that other
+// CTAs of the cluster made with release at cluster scope.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete, for at most
 // `limit_ns` nanoseconds.  Gives up early when another role of the CTA has
 // raised `abort_flag`.  On timeout it raises the flag and records
 // MOE_ERR_TIMEOUT in the status word.  Returns true when the phase completed.
+// CLUSTER: acquire at cluster scope (mbar_try_wait_cluster).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag, int32_t* status,
                                                   uint64_t limit_ns) {
+  auto try_once = [&]() {
+    return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
 #pragma unroll 1
   for (int i = 0; i < 256; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_once()) return true;
   const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_once()) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
@@ -305,6 +324,20 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16-byte asynchronous copy global -> shared through L2 (cp.async, generic proxy):
+// src_bytes of 16 copies the piece, 0 writes 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// every committed group of this thread but the newest N has landed in shared memory
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Four-row gather (see tma_gather4) completing on an mbarrier of either CTA of the pair.

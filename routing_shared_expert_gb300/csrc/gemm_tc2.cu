@@ -27,12 +27,17 @@
 // B columns [0,128) and lanes 64-127 for columns [128,256), TMEM columns 0-127,
 // rows 64 r + (lane mod 64) in CTA r.
 // The gate/up A rows are either read from a packed buffer (one TMA tile load) or
-// gathered straight from x through the packed-row source table: each lane of the
-// producer warp issues one tile::gather4 of four rows, so the row permutation of
-// Section 10.3 costs no extra pass over memory.
-// Roles per CTA (192 threads): warp 0 TMA producer (both CTAs; completions are
-// counted on the even CTA's barrier), warp 1 TMEM allocation and, in the even
-// CTA only, the MMA issuer; warps 2-5 epilogue.  The epilogue stages each
+// gathered straight from x through the packed-row source table, so that the row
+// permutation of Section 10.3 costs no extra pass over memory.  Gathering, six more
+// warps per CTA, one per K block of the ring, copy the CTA's A rows of their K block with
+// 16-byte cp.async pieces (a warp instruction moves four whole 128-byte row pieces), wait
+// for them, make them visible to the tensor core's proxy and arrive on the even CTA's
+// stage barrier, which then counts the producer's arrival, the gatherer arrivals of both
+// CTAs and the B bytes.
+// Roles per CTA (192 threads, 384 gathering): warp 0 TMA producer (both CTAs;
+// completions are counted on the even CTA's barrier), warp 1 TMEM allocation and, in
+// the even CTA only, the MMA issuer; warps 2-5 epilogue; warps 6-11 A-row gatherers.
+// The epilogue stages each
 // 32 x 32 block through shared memory: h blocks go out as row-contiguous lane stores,
 // fp32 f blocks as TMA bulk tensor stores (lane stores at a segment's end).
 // Every wait is bounded by %globaltimer; a wait that runs out records
@@ -62,6 +67,8 @@ constexpr int EPI_LD = 36;                 // 32-bit words per staged row (16-by
 constexpr int EPI_WARP_WORDS = 32 * EPI_LD;
 constexpr int EPI_BYTES = 4 * EPI_WARP_WORDS * 4;
 constexpr int THREADS = 192;
+constexpr int GATHER_THREADS = 384;        // six gatherer warps more
+constexpr int GATHER_WARP0 = 6;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 100000000ull;
@@ -80,6 +87,7 @@ struct PairArgs {
   const int32_t* gather_src; // non-null: A rows are gathered from x through this table
   int64_t gather_cap;        // entries of gather_src
   int64_t src_rows;          // rows of x
+  const uint16_t* gather_x;  // x [src_rows][k_dim] (16-bit elements, 16-byte aligned rows)
   // fp16 intermediate: SwiGLU mode stores fp16(h * h_scale); plain mode reads the packed
   // weights' header and writes fp16(accumulator * 2^-k)
   float h_scale;
@@ -141,7 +149,7 @@ __device__ __forceinline__ void load_b(uint32_t sB, bool half, bool leader, cons
 }
 
 template <int MODE, bool GATHER, int KSUB, bool H16>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? GATHER_THREADS : THREADS, 1)
     tc_pair_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA64,
                  const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                  const __grid_constant__ CUtensorMap tmB0h, const __grid_constant__ CUtensorMap tmB1h,
@@ -177,7 +185,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < RING_BLOCKS; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
+      // gathering: the producer and, in each CTA, one gatherer warp per K block of the stage
+      mbar_init(smem_u32(&full[s]), GATHER ? 1 + 2 * KSUB : 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -223,8 +232,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_map(&tmA);
-    if (!GATHER) tma_prefetch_map(&tmA64);
+    if (!GATHER) {
+      tma_prefetch_map(&tmA);
+      tma_prefetch_map(&tmA64);
+    }
     tma_prefetch_map(&tmB0);
     if (SWIGLU) {
       tma_prefetch_map(&tmB1);
@@ -248,74 +259,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int s = 0; s < RING_BLOCKS; ++s) issued_parity[s] = -1;
     bool ok = true;
     Tile tl;
-    if constexpr (!GATHER) {
-      // Lane 0 alone: wait for a free stage, arm the even CTA's barrier, load A and B.
-      if (lane == 0) {
-        for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl); t += n_pairs) {
-          const int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * (tl.half ? HM : BM);
-          const CUtensorMap* mapA = tl.half ? &tmA64 : &tmA;
-          const uint32_t tx = 2u * ((tl.half ? A_BYTES / 2 : A_BYTES) + B_BYTES);
-          const int b_row = b_first_row<SWIGLU>(args, tl, rank);
-          for (int kb0 = 0; kb0 < k_blocks; kb0 += ksub) {
-            if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
-                                   kWaitLimitNs)) {
-              ok = false;
-              break;
-            }
-            const uint32_t fb_local = smem_u32(&full[stage]);
-            const uint32_t fb_leader = mapa_shared(fb_local, 0);
-            const int nv = ksub == 1 ? 1 : min(ksub, k_blocks - kb0);
-            if (leader) mbar_arrive_expect_tx(fb_local, tx * static_cast<uint32_t>(nv));
-#pragma unroll
-            for (int u = 0; u < nv; ++u) {
-              const int kb = kb0 + u;
-              const uint32_t sA = smem_base + stage * stage_bytes + u * SUB_BYTES;
-              tma_load_2d_pair(sA, mapA, kb * BK, a_row, fb_leader);
-              load_b<SWIGLU>(sA + A_BYTES, tl.half, leader, &tmB0, &tmB1, &tmB0h, &tmB1h, kb * BK,
-                             b_row, fb_leader);
-            }
-            issued_parity[stage] = static_cast<int>(phase);
-            if (++stage == stages) { stage = 0; phase ^= 1u; }
-          }
-        }
-      }
-    } else {
-      // Whole warp: lane 0 waits and loads B; each lane gathers four of the CTA's 128 A
-      // rows (lanes 0-15 the 64 rows of a half tile).
+    // Lane 0 alone: wait for a free stage, arm the even CTA's barrier, load A (unless the
+    // gatherer warps copy it) and B.
+    if (lane == 0) {
       for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl); t += n_pairs) {
         const int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * (tl.half ? HM : BM);
-        const uint32_t tx = 2u * ((tl.half ? A_BYTES / 2 : A_BYTES) + B_BYTES);
-        const bool gathers = !tl.half || lane < HM / 4;
+        const CUtensorMap* mapA = tl.half ? &tmA64 : &tmA;
+        const uint32_t tx =
+            GATHER ? 2u * B_BYTES : 2u * ((tl.half ? A_BYTES / 2 : A_BYTES) + B_BYTES);
         const int b_row = b_first_row<SWIGLU>(args, tl, rank);
-        int32_t src[4];
-        gather_rows4(args.gather_src, args.gather_cap, a_row + 4 * lane, tl.seg_start, tl.seg_end,
-                     args.src_rows, args.status, src);
         for (int kb0 = 0; kb0 < k_blocks; kb0 += ksub) {
-          bool go = true;
-          if (lane == 0)
-            go = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
-                                   kWaitLimitNs);
-          go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
-          if (!go) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.status,
+                                 kWaitLimitNs)) {
             ok = false;
             break;
           }
           const uint32_t fb_local = smem_u32(&full[stage]);
           const uint32_t fb_leader = mapa_shared(fb_local, 0);
           const int nv = ksub == 1 ? 1 : min(ksub, k_blocks - kb0);
-          if (lane == 0) {
-            if (leader) mbar_arrive_expect_tx(fb_local, tx * static_cast<uint32_t>(nv));
-            issued_parity[stage] = static_cast<int>(phase);
-          }
+          if (leader) mbar_arrive_expect_tx(fb_local, tx * static_cast<uint32_t>(nv));
 #pragma unroll
           for (int u = 0; u < nv; ++u) {
             const int kb = kb0 + u;
             const uint32_t sA = smem_base + stage * stage_bytes + u * SUB_BYTES;
-            if (lane == 0)
-              load_b<SWIGLU>(sA + A_BYTES, tl.half, leader, &tmB0, &tmB1, &tmB0h, &tmB1h, kb * BK,
-                             b_row, fb_leader);
-            if (gathers) tma_gather4_pair(sA + lane * 512, &tmA, kb * BK, src, fb_leader);
+            if (!GATHER) tma_load_2d_pair(sA, mapA, kb * BK, a_row, fb_leader);
+            load_b<SWIGLU>(sA + A_BYTES, tl.half, leader, &tmB0, &tmB1, &tmB0h, &tmB1h, kb * BK,
+                           b_row, fb_leader);
           }
+          issued_parity[stage] = static_cast<int>(phase);
           if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -353,8 +324,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const uint32_t d_acc = tmem_base + static_cast<uint32_t>(buf * 256);
         const uint32_t idesc = tl.half ? idesc_half : idesc_full;
         for (int kb0 = 0; kb0 < k_blocks; kb0 += ksub) {
-          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, args.status,
-                                 kWaitLimitNs)) {
+          // gathered A rows: the partner's gatherers release their rows at cluster scope
+          if (!mbar_wait_bounded<GATHER>(smem_u32(&full[stage]), phase, abort_flag, args.status,
+                                         kWaitLimitNs)) {
             ok = false;
             break;
           }
@@ -381,7 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         mbar_wait_bounded(smem_u32(drain), 0, never, nullptr, kDrainLimitNs);
       }
     }
-  } else {
+  } else if (warp < GATHER_WARP0) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
     uint32_t* stg = epi + (warp - 2) * EPI_WARP_WORDS;
@@ -552,6 +524,87 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
     }
     if (!SWIGLU && lane == 0) bulk_wait_all();   // the output blocks are written
+  } else if constexpr (GATHER) {
+    // ------------------------------------------------------------ A-row gatherers (both CTAs)
+    // One warp per ring slot and K block of a stage (six warps): warp gw fills K block
+    // gw / stages of slot gw mod stages at every use of that slot, with all R A rows of the
+    // CTA (R = 128, or 64 in a half tile).  Lanes 8j..8j+7 take the eight 16-byte pieces of
+    // one row, so a warp instruction moves four whole 128-byte row pieces; piece v of row r
+    // lands at piece v ^ (r mod 8) of the row's 128 bytes (the 128-byte swizzle the MMA
+    // descriptors expect).  Rows past the segment are zero-filled.  The warp waits for its
+    // own copies, fences them into the async proxy and arrives once on the even CTA's
+    // stage barrier, so every slot refills as soon as the MMAs release it, independently
+    // of the others.
+    constexpr int kGatherWarps = (GATHER_THREADS - THREADS) / 32;
+    static_assert(kGatherWarps == RING_BLOCKS, "one gatherer warp per ring K block");
+    const int gw = warp - GATHER_WARP0;
+    const int my_slot = gw % stages, my_u = gw / stages;
+    const int sub = lane >> 3, piece = lane & 7;
+    const int64_t ld_bytes = static_cast<int64_t>(args.k_dim) * 2;
+    const char* xb = reinterpret_cast<const char*>(args.gather_x);
+    const int stages_per_tile = (k_blocks + ksub - 1) / ksub;
+    int64_t j0 = 0;   // ring stages of the tiles before this one
+    bool ok = true;
+    Tile tl;
+    for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl);
+         t += n_pairs, j0 += stages_per_tile) {
+      // this warp's first stage of the tile: the first j >= j0 with j mod stages == my_slot
+      int q = static_cast<int>((my_slot - j0 % stages + stages) % stages);
+      if (q >= stages_per_tile) continue;
+      const int rows = tl.half ? HM : BM;
+      const int n_i = rows / 4;   // instructions per K block: 32 (full tile) or 16 (half)
+      const int64_t a_row = static_cast<int64_t>(tl.seg_start) + tl.m * PM + rank * rows;
+      int32_t tok[32];
+      uint32_t valid = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int64_t pr = a_row + 4 * i + sub;
+        int32_t v = 0;
+        if (i < n_i && pr < tl.seg_end && pr < args.gather_cap) {
+          v = args.gather_src[pr];
+          if (v < 0 || v >= args.src_rows) {
+            set_status(args.status, MOE_ERR_DEVICE_BOUNDS);
+            v = 0;
+          } else {
+            valid |= 1u << i;
+          }
+        }
+        tok[i] = v;
+      }
+      for (; q < stages_per_tile; q += stages) {
+        const int64_t j = j0 + q;
+        const uint32_t phase = static_cast<uint32_t>((j / stages) & 1);
+        bool go = true;
+        if (lane == 0)
+          go = mbar_wait_bounded(smem_u32(&empty[my_slot]), phase ^ 1u, abort_flag, args.status,
+                                 kWaitLimitNs);
+        go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+        if (!go) {
+          ok = false;
+          break;
+        }
+        const int kb = q * ksub + my_u;
+        if (kb < k_blocks) {
+          const uint32_t sA = smem_base + my_slot * stage_bytes + my_u * SUB_BYTES;
+          const bool in_k = kb * BK + piece * 8 < args.k_dim;
+          // a piece past the width reads nothing (zero fill); its address stays in the row
+          const int64_t koff = in_k ? static_cast<int64_t>(kb) * (BK * 2) + piece * 16 : 0;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (i < n_i) {
+              const int r = 4 * i + sub;
+              cp_async16(sA + r * 128 + ((piece ^ (r & 7)) * 16), xb + tok[i] * ld_bytes + koff,
+                         (in_k && (valid >> i & 1u)) ? 16u : 0u);
+            }
+          }
+          cp_async_commit();
+          cp_async_wait<0>();
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&full[my_slot]), 0));
+      }
+    }
   }
 
   __syncwarp();
@@ -580,7 +633,8 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a64, const CUte
   if (e != cudaSuccess) return e;
   const int64_t pairs_max = device_sm_count() >= 2 ? device_sm_count() / 2 : 1;
   const int64_t pairs = max_pair_tiles < pairs_max ? max_pair_tiles : pairs_max;
-  kern<<<static_cast<unsigned>(2 * pairs), THREADS, smem, s>>>(a, a64, b0, b1, b0h, b1h, out, args);
+  kern<<<static_cast<unsigned>(2 * pairs), GATHER ? GATHER_THREADS : THREADS, smem, s>>>(
+      a, a64, b0, b1, b0h, b1h, out, args);
   return cudaGetLastError();
 }
 
@@ -593,12 +647,12 @@ cudaError_t run_pair(const MlpParams& p, cudaStream_t s) {
   if (rows_cap == 0 || (dense && p.dense_rows == 0)) return cudaSuccess;
   const int64_t mt_ub = dense ? (p.dense_rows + PM - 1) / PM : (rows_cap + PM - 1) / PM + p.groups;
 
-  // Full-tile boxes of 128 rows and half-tile boxes of 64 (a gathered A is loaded four
-  // rows at a time through its one-row map).
+  // Full-tile boxes of 128 rows and half-tile boxes of 64 (a gathered A is copied by the
+  // gatherer warps and needs no map).
   CUtensorMap mA, mA64, mG, mU, mG64, mU64, mH, mH64, mD;
   const bool gather = p.gather_src != nullptr;
   const uint64_t w_rows = static_cast<uint64_t>(p.groups) * p.width;
-  if (!make_bf16_map(&mA, p.A, p.d, gather ? p.src_rows : rows_cap, gather ? 1 : BM) ||
+  if ((!gather && !make_bf16_map(&mA, p.A, p.d, rows_cap, BM)) ||
       (!gather && !make_bf16_map(&mA64, p.A, p.d, rows_cap, HM)) ||
       !make_bf16_map(&mG, p.W_gate, p.d, w_rows, 128) ||
       !make_bf16_map(&mU, p.W_up, p.d, w_rows, 128) ||
@@ -611,7 +665,7 @@ cudaError_t run_pair(const MlpParams& p, cudaStream_t s) {
       !(H16 ? make_f16_map(&mD, down_values(p), p.width, static_cast<uint64_t>(p.groups) * p.d, 128)
             : make_bf16_map(&mD, p.W_down, p.width, static_cast<uint64_t>(p.groups) * p.d, 128)))
     return cudaErrorInvalidValue;
-  if (gather) mA64 = mA;
+  if (gather) mA = mA64 = mG;   // unused placeholders
 
   PairArgs a{};
   a.offsets = p.offsets;
@@ -622,13 +676,14 @@ cudaError_t run_pair(const MlpParams& p, cudaStream_t s) {
   a.gather_src = p.gather_src;
   a.gather_cap = rows_cap;
   a.src_rows = p.src_rows;
+  a.gather_x = static_cast<const uint16_t*>(p.A);
   a.h_scale = p.h_scale;
   a.down_hdr = H16 ? static_cast<const PackHeader*>(p.W_down) : nullptr;
   a.down_elements = static_cast<int64_t>(p.groups) * p.d * p.width;
   // Two K blocks per ring stage when the average group has at least 512 rows (each
   // weight byte feeds enough rows for the tensor pipe to bound the launch); one
-  // otherwise, and for gathered A rows.
-  const bool wide = !gather && (dense ? p.dense_rows : rows_cap / (p.groups > 0 ? p.groups : 1)) >= 512;
+  // otherwise.
+  const bool wide = (dense ? p.dense_rows : rows_cap / (p.groups > 0 ? p.groups : 1)) >= 512;
 
   a.k_dim = p.d;
   a.n_out = p.width;
@@ -637,7 +692,8 @@ cudaError_t run_pair(const MlpParams& p, cudaStream_t s) {
   a.ldo = p.width;
   const int64_t gu_tiles = mt_ub * ((p.width + 127) / 128);
   cudaError_t e =
-      gather ? launch_pair<kSwiGLU, true, 1, H16>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s)
+      gather ? (wide ? launch_pair<kSwiGLU, true, 2, H16>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s)
+                     : launch_pair<kSwiGLU, true, 1, H16>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s))
       : wide ? launch_pair<kSwiGLU, false, 2, H16>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s)
              : launch_pair<kSwiGLU, false, 1, H16>(mA, mA64, mG, mU, mG64, mU64, mA, a, gu_tiles, s);
   if (e != cudaSuccess) return e;
