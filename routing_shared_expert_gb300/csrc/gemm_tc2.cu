@@ -67,7 +67,7 @@ constexpr int EPI_LD = 36;                 // 32-bit words per staged row (16-by
 constexpr int EPI_WARP_WORDS = 32 * EPI_LD;
 constexpr int EPI_BYTES = 4 * EPI_WARP_WORDS * 4;
 constexpr int THREADS = 192;
-constexpr int GATHER_THREADS = 384;        // six gatherer warps more
+constexpr int GATHER_THREADS = THREADS + 32 * RING_BLOCKS;   // one gatherer warp per ring K block
 constexpr int GATHER_WARP0 = 6;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
