@@ -347,6 +347,38 @@ def stage_roofline(spec, kept: int, g_ms: float, pk) -> dict:
     return out
 
 
+def layer_algorithmic_bytes(spec, kept: int) -> int:
+    """Bytes one layer forward must move at least once, summed over its steps: the router
+    (x and W_router read, top-K written), the permutation (top-K read, route tables written,
+    x read, x_perm written), the grouped stage (stage_algorithmic_bytes), the shared expert
+    (x and its weights read, its intermediate written and read, g written) and the combine
+    (f, g and the route tables read, fp32 y written).  Intermediates h, f and g take the
+    layer's element size (fp16 for bf16 layers, whose intermediate format is fp16)."""
+    b = spec.elem_bytes
+    T, d, N, K, ds = spec.T, spec.d_model, spec.N, spec.K, spec.d_shared
+    routes = T * K
+    router = T * d * b + N * d * b + 2 * routes * 4
+    permute = routes * 4 + 2 * routes * 4 + T * d * b + kept * d * b
+    shared = (T * d * b + 3 * d * ds * b + 2 * T * ds * b + T * d * b) if ds > 0 else 0
+    combine = kept * d * b + (T * d * b if ds > 0 else 0) + T * d * 4 + 2 * routes * 4
+    return int(router + permute + stage_algorithmic_bytes(spec, kept) + shared + combine)
+
+
+def layer_roofline(spec, kept: int, ms: float, pk) -> dict:
+    """The whole layer against its roofline: executed expert and shared FLOP over the layer's
+    algorithmic bytes gives its intensity; the roof is the lower of the bf16 peak and
+    intensity x HBM rate (both measured), and frac is the achieved FLOP rate over that roof."""
+    flops = spec.expert_flops(kept)
+    nbytes = layer_algorithmic_bytes(spec, kept)
+    ai = flops / nbytes
+    roof = min(pk["bf16_tflops"], ai * pk["hbm_gbs"] / 1e3)
+    tf = flops / (ms / 1e3) / 1e12
+    return {"flops": flops, "bytes": nbytes, "intensity_flop_per_byte": ai,
+            "ridge_flop_per_byte": pk["bf16_tflops"] * 1e3 / pk["hbm_gbs"],
+            "bound": "tensor" if roof >= pk["bf16_tflops"] else "hbm",
+            "roof_tflops": roof, "achieved_tflops": tf, "frac": tf / roof}
+
+
 def experts_window(spec, kept: int, stage_ms: dict, world: int, pk) -> dict:
     """All expert GEMM FLOP (routed and shared) over the window they run in: from the start
     of the layer to the end of the routed experts (the router, the permutation and the
@@ -548,6 +580,7 @@ def summarize(spec, r, args, world: int, pk):
             "grouped_tflops": g_tf, "grouped_frac": g_tf / pk["bf16_tflops"],
             "grouped_roofline": stage_roofline(spec, kept, g_ms, pk),
             "experts_window": experts_window(spec, kept, r["stage_ms"], world, pk),
+            "layer_roofline": layer_roofline(spec, kept, ms, pk),
             "stages_ms": r["stage_ms"], "kept_routes": kept}
 
 
@@ -767,6 +800,7 @@ def main():
                             "grouped_roofline": {k: sm["grouped_roofline"][k]
                                                  for k in ("bound", "frac", "frac_tensor", "frac_hbm")},
                             "experts_window": sm["experts_window"],
+                            "layer_roofline": sm["layer_roofline"],
                             "stages_ms": sm["stages_ms"],
                             "kept_routes": sm["kept_routes"],
                             "clocks": {k: clk.get(k) for k in ("sm_mhz", "reasons", "samples")}}
@@ -784,6 +818,7 @@ def main():
         "tflops": head["tflops"], "pct_bf16_peak": head["pct_bf16_peak"],
         "stages_ms": head["stages_ms"],
         "experts_window": head["experts_window"],
+        "layer_roofline": head["layer_roofline"],
         "roofline": dict({"kernel": "grouped_swiglu stage (tcgen05 gate/up + down GEMM launches "
                                     "over packed segments)"},
                          **head["grouped_roofline"],
