@@ -340,17 +340,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Four-row gather (see tma_gather4) completing on an mbarrier of either CTA of the pair.
-__device__ __forceinline__ void tma_gather4_pair(uint32_t smem_dst, const CUtensorMap* map, int32_t c0,
-                                                 const int32_t (&r)[4], uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]),
-      "r"(bar)
-      : "memory");
-}
-
 // Source rows of four consecutive packed rows starting at `row` (gathered GEMM A-load).
 // Rows past the segment (or the table) read the segment's first row; their results
 // are never stored.  A source index outside [0, src_rows) is reported and replaced by 0.
