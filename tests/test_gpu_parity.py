@@ -280,6 +280,34 @@ def test_layer_full_size_sampled(name):
         assert rt.drops["dropped_routes"] > 0
 
 
+def test_gathered_rows_equal_packed_rows_full_size_dsv3():
+    """The gathered-row form of the routed expert GEMMs at the DeepSeek-V3 layer's full size
+    (65,536 routed rows over 256 experts; 112 K blocks per gate/up tile, so every gatherer
+    warp's ring slot goes through many phases and half tiles interleave with full ones): the
+    rows read from x through perm_src give exactly the f of the packed copy x_perm."""
+    import routing_shared_expert_gb300 as moe
+    spec = C["dsv3"]
+    inp = make_inputs(spec, "cuda")
+    layer = run_layer(spec, inp)
+    c, o = layer.cfg, layer.out
+    T, K, d = spec.T, spec.K, spec.d_model
+    x_perm = torch.empty((T * K, d), dtype=spec.torch_dtype, device="cuda")
+    moe.moe_permute(c, inp["x"], o["topk_idx"], None, o["counts_keep"], o["offsets"],
+                    o["route_pos"], o["perm_src"], x_perm, None, None, None, layer.ws)
+    ft = layer.staged["f"].dtype
+    f_packed = torch.empty((T * K, d), dtype=ft, device="cuda")
+    f_gather = torch.empty((T * K, d), dtype=ft, device="cuda")
+    moe.moe_grouped_swiglu(c, x_perm, o["offsets"], None, inp["W_gate"], inp["W_up"],
+                           layer.down["W_down"], f_packed, layer.ws)
+    moe.moe_grouped_swiglu(c, inp["x"], o["offsets"], o["perm_src"], inp["W_gate"], inp["W_up"],
+                           layer.down["W_down"], f_gather, layer.ws)
+    torch.cuda.synchronize()
+    kept = int(o["offsets"][-1])
+    assert kept == T * K
+    assert torch.equal(f_packed[:kept], f_gather[:kept])
+    assert layer.status() == 0
+
+
 @pytest.mark.parametrize("N,K,T,score", [(129, 8, 129, "sigmoid"), (256, 1, 127, "sigmoid"),
                                          (200, 3, 128, "softmax"), (256, 8, 1, "softmax")])
 def test_wide_router_shapes(N, K, T, score):
