@@ -65,7 +65,8 @@ def peaks():
 class ClockSampler:
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "power.draw.instant")
 
     def __init__(self, index: int):
         self.index = index
@@ -115,7 +116,10 @@ def _stamp(text: str):
 
 
 def summarize_clocks(rows, t0=None, t1=None):
-    """rows: nvidia-smi CSV records (timestamp, index, sm, max sm, power, active, four reasons)."""
+    """rows: nvidia-smi CSV records (timestamp, index, sm, max sm, power, active, four reasons,
+    and optionally the instantaneous power).  power.draw is a one-second average, which in a
+    timed region of a fraction of a second still reads mostly the idle time before it; the
+    instantaneous reading follows the load."""
     if not rows:
         return None
     stamped = [(_stamp(r[0]), r) for r in rows]
@@ -137,11 +141,14 @@ def summarize_clocks(rows, t0=None, t1=None):
     sm = [v for v in (num(r[2]) for r in inside) if v is not None]
     mx = [v for v in (num(r[3]) for r in inside) if v is not None]
     pw = [v for v in (num(r[4]) for r in inside) if v is not None]
+    pi = [v for v in (num(r[10]) for r in inside if len(r) > 10) if v is not None]
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     reasons = sorted({names[i] for r in inside for i in range(4) if r[6 + i].lower() == "active"})
     return {"sm_mhz": statistics.median(sm) if sm else None,
             "sm_max_mhz": max(mx) if mx else None,
             "power_w": statistics.median(pw) if pw else None,
+            "power_instant_w": statistics.median(pi) if pi else None,
+            "power_instant_max_w": max(pi) if pi else None,
             "reasons": reasons, "samples": len(inside), "window": window}
 
 

@@ -78,6 +78,11 @@ def test_clock_summary_keeps_only_the_timed_window():
     assert c["samples"] == 2 and c["window"] == "timed region"
     assert c["sm_mhz"] == pytest.approx(2055.0)
     assert c["reasons"] == ["sw_power_cap"]          # the idle sample's hw_slowdown is outside
+    assert c["power_w"] == pytest.approx(925.0) and c["power_instant_w"] is None
+    # with the instantaneous power column
+    rows11 = [r + [p] for r, p in zip(rows, ["310", "1180", "1240", "205"])]
+    c = bench.summarize_clocks(rows11, t0, t1)
+    assert c["power_instant_w"] == pytest.approx(1210.0) and c["power_instant_max_w"] == 1240.0
     # a window shorter than the sampling interval falls back to the nearest samples
     t0 = bench._stamp("2026/01/01 00:00:02.000")
     c = bench.summarize_clocks(rows, t0, t0 + 0.01)
