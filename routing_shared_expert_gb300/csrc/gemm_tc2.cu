@@ -263,7 +263,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? GATHER_THRE
     // gatherer warps copy it) and B.
     if (lane == 0) {
       for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl); t += n_pairs) {
-        const int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * (tl.half ? HM : BM);
+        int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * (tl.half ? HM : BM);
+        // A CTA whose A rows all lie past the segment (the odd CTA of a half tile over a tail
+        // of at most 64 rows) loads its box from past the last row of the buffer instead:
+        // TMA fills it with zeros, reads no memory, and the MMAs on those rows (whose results
+        // are never stored) multiply zeros instead of the next segment's rows.
+        if (a_row >= tl.seg_end) a_row = static_cast<int>(args.out_rows);
         const CUtensorMap* mapA = tl.half ? &tmA64 : &tmA;
         const uint32_t tx =
             GATHER ? 2u * B_BYTES : 2u * ((tl.half ? A_BYTES / 2 : A_BYTES) + B_BYTES);
