@@ -464,6 +464,139 @@ def bench_balance(args, spec, config, dev) -> int:
     return 0
 
 
+# ----------------------------------------------------------------- expert parallelism
+def bench_ep(args, spec, config, dev) -> int:
+    """The device side of one rank's expert-parallel forward (F4: Section 10.3, Figure 41) for
+    the layout rho(i) = i mod M with M = the workload's rank count, on this GPU: the plan
+    (moe_ep_keep_matrix, moe_ep_place, moe_ep_send_pos: three launches), the dispatch's two
+    indexed row copies (the rank's x rows into its send buffer; a received buffer into its
+    packed expert buffer by moe_ep_recv_rows) and the return's two (the packed outputs into
+    the send-back buffer; the received outputs into one row per route, dropped routes zero).
+    The all-to-all between them needs a second GPU and is not run: the other M - 1 sources
+    are emulated with this rank's own request counts, so the buffers have the sizes of M
+    equal sources.  CUDA events around each step, L2 flushed before each; bytes are the
+    rows each copy must read and write once.  The expert widths are reduced (the exchange
+    moves d_model-wide rows only)."""
+    import torch
+    import routing_shared_expert_gb300 as moe
+    from routing_shared_expert_gb300 import _native as nat
+    from routing_shared_expert_gb300 import ep
+    from workloads import make_inputs
+    sp = spec.replace(d_expert=128, d_shared=128 if spec.d_shared else 0)
+    inp = make_inputs(sp, dev, seed=0)
+    layer = moe.MoELayer(moe.config_from_spec(sp), inp, dev, staged_buffers=False)
+    layer.forward(inp["x"], logits=False)
+    c, o, ws = layer.cfg, layer.out, layer.ws
+    T, K, N, d, M = sp.T, sp.K, sp.N, sp.d_model, max(sp.num_ranks, 1)
+    rho = [e % M for e in range(N)]
+    x = inp["x"]
+    eb = x.element_size()
+    # this rank's requests and its capacity-free permutation (the stable ranks moe_ep_place reads)
+    i32 = dict(dtype=torch.int32, device=dev)
+    cnt, ck, off = torch.empty(N, **i32), torch.empty(N, **i32), torch.empty(N + 1, **i32)
+    rpos, psrc = torch.empty((T, K), **i32), torch.empty(T * K, **i32)
+    free = moe.config_from_spec(sp.replace(cap_policy="none"))
+    moe.moe_permute(free, None, o["topk_idx"], cnt, ck, off, rpos, psrc, None, None, None, None, ws)
+    counts_all = cnt.unsqueeze(0).repeat(M, 1).contiguous()
+    policy = sp.cap_policy if sp.cap_policy != "per_expert" else "rank_wide"
+    rank = 0
+
+    pl = ep.make_plan(counts_all, o["topk_idx"], rank, K, rho, policy, sp.capacity_factor,
+                      route_pos=rpos, offsets=off, workspace=ws)
+    lib = nat.library()
+    rho_arr = ep._rho(rho)
+    pol = nat.CAP_POLICIES[policy]
+    keep, roff = torch.empty_like(pl.keep), torch.empty_like(pl.recv_off)
+    rq, rk = torch.empty_like(pl.R_req), torch.empty_like(pl.R_keep)
+    dst, spos = torch.empty_like(pl.dst_row), torch.empty_like(pl.send_pos)
+    P = ep._ptr
+
+    def plan():
+        # the three device entries of the plan, without the host read of the keep matrix that
+        # ep.make_plan adds for the all-to-all's split sizes
+        st = nat._stream(None)
+        nat._check("moe_ep_keep_matrix", lib.moe_ep_keep_matrix(
+            M, N, K, rho_arr, pol, float(sp.capacity_factor), P(counts_all), P(keep), P(roff),
+            P(rq), P(rk), st))
+        nat._check("moe_ep_place", lib.moe_ep_place(
+            M, rank, T, N, K, P(o["topk_idx"]), P(rpos), P(off), P(keep), P(roff), P(dst), P(ws),
+            ws.numel(), st))
+        nat._check("moe_ep_send_pos", lib.moe_ep_send_pos(
+            M, rank, T, N, K, rho_arr, P(o["topk_idx"]), P(keep), P(roff), P(dst), P(spos), None,
+            P(ws), ws.numel(), st))
+
+    split = pl.send_counts()
+    n_send = int(split[rank].sum())
+    n_recv = int(split[:, rank].sum())
+    n_local = int(pl.R_keep[rank])
+    send = torch.empty((max(n_send, 1), d), dtype=x.dtype, device=dev)
+    recv = torch.empty((max(n_recv, 1), d), dtype=x.dtype, device=dev).normal_()
+    rows = torch.empty((max(n_local, 1), d), dtype=x.dtype, device=dev)
+    back = torch.empty((max(n_send, 1), d), dtype=x.dtype, device=dev).normal_()
+    out = torch.empty((T * K, d), dtype=x.dtype, device=dev)
+    rr = ep.recv_rows(pl, workspace=ws)
+    send_back = torch.empty((max(n_recv, 1), d), dtype=x.dtype, device=dev)
+    steps = {
+        "plan: keep matrix": (None, 3 * M * N * 4),
+        "plan (keep matrix, destination rows, send positions)":
+            (plan, T * K * 4 * 5 + 2 * M * N * 4),
+        "dispatch: receive rows (moe_ep_recv_rows)":
+            (lambda: nat._check("moe_ep_recv_rows", lib.moe_ep_recv_rows(
+                M, rank, N, rho_arr, P(keep), P(roff), P(rr), rr.numel(), P(ws), ws.numel(),
+                nat._stream(None))), n_recv * 4 + 2 * M * N * 4),
+        "dispatch: x rows into the send buffer":
+            (lambda: ep.rows_copy(x, send, T * K, src_div=K, dst_index=pl.send_pos, workspace=ws),
+             T * d * eb + n_send * d * eb),
+        "dispatch: received rows into the packed expert buffer":
+            (lambda: ep.rows_copy(recv, rows, n_recv, dst_index=rr, workspace=ws),
+             2 * n_recv * d * eb),
+        "return: packed outputs into the send-back buffer":
+            (lambda: ep.rows_copy(rows, send_back, n_recv, src_index=rr, workspace=ws),
+             2 * n_recv * d * eb),
+        "return: received outputs into one row per route (dropped routes zero)":
+            (lambda: ep.rows_copy(back, out, T * K, src_index=pl.send_pos, zero_missing=True,
+                                  workspace=ws),
+             n_send * d * eb + T * K * d * eb),
+    }
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    pk = peaks()
+    results = {}
+    def keep_only():
+        nat._check("moe_ep_keep_matrix", lib.moe_ep_keep_matrix(
+            M, N, K, rho_arr, pol, float(sp.capacity_factor), P(counts_all), P(keep), P(roff),
+            P(rq), P(rk), nat._stream(None)))
+
+    steps["plan: keep matrix"] = (keep_only, steps["plan: keep matrix"][1])
+    for name, (fn, nbytes) in steps.items():
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(args.steps):
+            flush.add_(1)
+            torch.cuda._sleep(2_000_000)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+        us = statistics.median(times)
+        gbs = nbytes / (us / 1e6) / 1e9
+        results[name] = {"us": us, "algorithmic_bytes": nbytes, "GB_s": gbs,
+                         "frac_hbm": gbs / pk["hbm_gbs"]}
+    if layer.status() != 0:
+        raise RuntimeError(f"layer status {layer.status()}")
+    print(json.dumps({"mode": "ep", "workload": spec.name, "ranks": M, "policy": policy,
+                      "rows": {"send": n_send, "receive": n_recv, "packed": n_local},
+                      "calls": args.steps, "steps": results, "hbm_peak_gbs": pk["hbm_gbs"],
+                      "not_run": "the all-to-all between the dispatch's and the return's two copies "
+                                 "(one GPU: the other sources are emulated)",
+                      "config": dict(config, note="expert widths reduced to 128 (the exchange "
+                                                  "moves d_model-wide rows only)")}), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------- backward
 
 def bench_backward(args, spec, layer, x, config, dev):
@@ -616,10 +749,11 @@ def main():
     ap.add_argument("--override", default="", metavar="K=V,...",
                     help="change integer fields of the workload (e.g. N=32,T=1024: a smaller layer "
                          "of the same shape per expert, for profiler captures)")
-    ap.add_argument("--mode", choices=["forward", "backward", "balance"], default="forward",
+    ap.add_argument("--mode", choices=["forward", "backward", "balance", "ep"], default="forward",
                     help="backward: time moe_layer_backward (router coefficients fixed) on the "
                          "routing of one forward call, instead of the forward benchmark line; "
-                         "balance: time the load-balancing statistics and the bias-controller step")
+                         "balance: time the load-balancing statistics and the bias-controller step; "
+                         "ep: time the device side of one rank's expert-parallel exchange")
     ap.add_argument("--router-grad", action="store_true",
                     help="with --mode backward: include the gradient through the router coefficients")
     ap.add_argument("--forward-only", type=int, default=0, metavar="R",
@@ -713,6 +847,8 @@ def main():
         return bench_backward(args, spec, layer, inp["x"], config, dev)
     if args.mode == "balance":
         return bench_balance(args, spec, config, dev)
+    if args.mode == "ep":
+        return bench_ep(args, spec, config, dev)
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     pk = peaks()

@@ -27,14 +27,83 @@ struct EpKeepArgs {
   int32_t* R_keep;
 };
 
-// One thread per destination rank; every thread recomputes the (small) route total.
-__global__ void ep_keep_kernel(EpKeepArgs a) {
-  const int q = threadIdx.x;
-  if (q >= a.M) return;
-  const int64_t B =
-      ep_rank_budget(a.capacity_factor, a.K, ep_total_tokens(a.counts, a.M, a.N, a.K), a.M);
-  ep_keep_dest(q, a.counts, a.M, a.N, a.rho, a.cap_policy, B, a.keep, a.recv_off, a.R_req,
-               a.R_keep);
+constexpr int kEpThreads = 256;   // every kernel below: one thread per expert fits (N <= 256)
+
+// Exclusive prefix of v over the kEpThreads threads of the block in thread order; *total
+// receives the block's sum.  Every thread of the block calls it.
+__device__ int64_t block_exclusive_scan(int64_t v, int64_t* total) {
+  __shared__ int64_t warp_sums[kEpThreads / 32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_sums[w] = x;
+  __syncthreads();
+  int64_t before = 0, all = 0;
+#pragma unroll
+  for (int i = 0; i < kEpThreads / 32; ++i) {
+    const int64_t ws = warp_sums[i];
+    before += i < w ? ws : 0;
+    all += ws;
+  }
+  __syncthreads();   // warp_sums is reused by the next call
+  *total = all;
+  return before + x - v;
+}
+
+// One block per destination rank q: the rule of ep_keep_dest in parallel.  Along q's
+// sequence of splits (its experts in ascending index, within an expert the sources in
+// ascending rank), with P the requests of the splits before one and B the budget, the
+// cumulative admission keeps min(c, max(0, B - P)) of a split's c requests at row
+// min(P, B) of q's buffer (no policy: all c at row P): a prefix sum of the requests.
+__global__ void __launch_bounds__(kEpThreads) ep_keep_kernel(EpKeepArgs a) {
+  __shared__ int32_t local[kMaxExperts];   // q's experts in ascending index
+  const int q = blockIdx.x;
+  const int64_t splits = static_cast<int64_t>(a.M) * a.N;
+  // tokens over all sources (K requests each) give the budget
+  int64_t part = 0;
+  for (int64_t i = threadIdx.x; i < splits; i += kEpThreads) part += a.counts[i];
+  int64_t routes = 0;
+  block_exclusive_scan(part, &routes);
+  const int64_t B = ep_rank_budget(a.capacity_factor, a.K, routes / a.K, a.M);
+  const int e = threadIdx.x;
+  const bool mine = e < a.N && a.rho[e] == q;
+  int64_t n_local = 0;
+  const int64_t li = block_exclusive_scan(mine ? 1 : 0, &n_local);
+  if (mine) local[li] = e;
+  __syncthreads();
+  const int64_t L = n_local * a.M;
+  int64_t carry = 0;   // requests of the splits before this chunk
+  for (int64_t base = 0; base < L; base += kEpThreads) {
+    const int64_t j = base + threadIdx.x;
+    int64_t c = 0, idx = -1;
+    if (j < L) {
+      const int ee = local[j / a.M], src = static_cast<int>(j % a.M);
+      idx = static_cast<int64_t>(src) * a.N + ee;
+      c = a.counts[idx];
+    }
+    int64_t chunk = 0;
+    const int64_t P = carry + block_exclusive_scan(c, &chunk);
+    if (idx >= 0) {
+      int64_t k = c, row = P;
+      if (a.cap_policy == MOE_CAP_RANK_WIDE) {
+        const int64_t left = B - P;
+        k = left < c ? (left > 0 ? left : 0) : c;
+        row = P < B ? P : B;
+      }
+      a.keep[idx] = static_cast<int32_t>(k);
+      a.recv_off[idx] = static_cast<int32_t>(row);
+    }
+    carry += chunk;
+  }
+  if (threadIdx.x == 0) {
+    if (a.R_req) a.R_req[q] = static_cast<int32_t>(carry);
+    if (a.R_keep)
+      a.R_keep[q] = static_cast<int32_t>(a.cap_policy == MOE_CAP_RANK_WIDE && carry > B ? B : carry);
+  }
 }
 
 // One thread per route of the source rank: its rank among the source's requests to its
@@ -68,11 +137,31 @@ struct EpSendArgs {
   int32_t* status;
 };
 
-// One thread per route; every block first lays out the source's send buffer (O(M + N)).
-__global__ void ep_send_pos_kernel(EpSendArgs a) {
+// One thread per route.  Every block first lays out the source's send buffer (the rule of
+// ep_send_base, one thread per expert): base[e] sums the source's kept routes of the
+// experts before e in the order (destination rank, expert index).
+__global__ void __launch_bounds__(kEpThreads) ep_send_pos_kernel(EpSendArgs a) {
   __shared__ int32_t base[kMaxExperts];
-  if (threadIdx.x == 0)
-    ep_send_base(a.src, a.M, a.N, a.rho, a.keep, base, blockIdx.x == 0 ? a.send_counts : nullptr);
+  __shared__ int32_t kept[kMaxExperts];
+  for (int e = threadIdx.x; e < a.N; e += kEpThreads)
+    kept[e] = a.keep[static_cast<int64_t>(a.src) * a.N + e];
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.N; e += kEpThreads) {
+    const int q = a.rho[e];
+    int64_t b = 0;
+    for (int e2 = 0; e2 < a.N; ++e2) {
+      const int q2 = a.rho[e2];
+      b += (q2 < q || (q2 == q && e2 < e)) ? kept[e2] : 0;
+    }
+    base[e] = static_cast<int32_t>(b);
+  }
+  if (blockIdx.x == 0 && a.send_counts) {
+    for (int q = threadIdx.x; q < a.M; q += kEpThreads) {
+      int64_t n = 0;
+      for (int e2 = 0; e2 < a.N; ++e2) n += a.rho[e2] == q ? kept[e2] : 0;
+      a.send_counts[q] = static_cast<int32_t>(n);
+    }
+  }
   __syncthreads();
   const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (r >= a.routes) return;
@@ -95,31 +184,40 @@ struct EpRecvArgs {
   int32_t* status;
 };
 
-// One block per split (s, e) of a local expert: the split's rows sit in the receive buffer
-// after the earlier sources' blocks and, within source s, after its earlier local experts.
-__global__ void ep_recv_rows_kernel(EpRecvArgs a) {
-  const int s = blockIdx.x / a.N, e = blockIdx.x % a.N;
-  if (a.rho[e] != a.q) return;
-  __shared__ int64_t j0;
-  if (threadIdx.x == 0) {
-    int64_t j = 0;
-    for (int s2 = 0; s2 < a.M; ++s2)
-      for (int e2 = 0; e2 < a.N; ++e2) {
-        if (a.rho[e2] != a.q) continue;
-        if (s2 == s && e2 == e) { s2 = a.M; break; }
-        j += a.keep[static_cast<int64_t>(s2) * a.N + e2];
-      }
-    j0 = j;
-  }
+// One block per source s: its rows sit in the receive buffer after the earlier sources'
+// (the rule of ep_recv_rows), and within source s its splits of q's experts follow in
+// ascending expert index; a block sum and a scan over the experts give each split's first
+// receive row, then the block writes the split's rows one after another.
+__global__ void __launch_bounds__(kEpThreads) ep_recv_rows_kernel(EpRecvArgs a) {
+  __shared__ int64_t first[kMaxExperts];
+  __shared__ int32_t rho[kMaxExperts];
+  for (int e = threadIdx.x; e < a.N; e += kEpThreads) rho[e] = a.rho[e];
   __syncthreads();
-  const int64_t i = static_cast<int64_t>(s) * a.N + e;
-  const int32_t n = a.keep[i];
-  for (int32_t r = threadIdx.x; r < n; r += blockDim.x) {
-    if (j0 + r >= a.cap) {
-      set_status(a.status, MOE_ERR_DEVICE_BOUNDS);
-      return;
+  const int s = blockIdx.x;
+  int64_t part = 0;   // rows of q's receive buffer from sources before s
+  for (int64_t i = threadIdx.x; i < static_cast<int64_t>(s) * a.N; i += kEpThreads)
+    part += rho[i % a.N] == a.q ? a.keep[i] : 0;
+  int64_t before = 0;
+  block_exclusive_scan(part, &before);
+  const int e = threadIdx.x;
+  const bool mine = e < a.N && a.rho[e] == a.q;
+  int64_t total = 0;
+  const int64_t pre =
+      block_exclusive_scan(mine ? a.keep[static_cast<int64_t>(s) * a.N + e] : 0, &total);
+  if (e < a.N) first[e] = before + pre;
+  __syncthreads();
+  for (int e2 = 0; e2 < a.N; ++e2) {
+    if (a.rho[e2] != a.q) continue;
+    const int64_t i = static_cast<int64_t>(s) * a.N + e2;
+    const int32_t n = a.keep[i], off = a.recv_off[i];
+    const int64_t j0 = first[e2];
+    for (int32_t r = threadIdx.x; r < n; r += kEpThreads) {
+      if (j0 + r >= a.cap) {
+        set_status(a.status, MOE_ERR_DEVICE_BOUNDS);
+        break;
+      }
+      a.recv_row[j0 + r] = off + r;
     }
-    a.recv_row[j0 + r] = a.recv_off[i] + r;
   }
 }
 
@@ -226,7 +324,7 @@ moe_status moe_ep_keep_matrix(int32_t M, int32_t N, int32_t K, const int32_t* rh
   a.recv_off = recv_off;
   a.R_req = R_req;
   a.R_keep = R_keep;
-  ep_keep_kernel<<<1, 256, 0, stream>>>(a);
+  ep_keep_kernel<<<static_cast<unsigned>(M), kEpThreads, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -307,7 +405,7 @@ moe_status moe_ep_send_pos(int32_t M, int32_t src_rank, int64_t T, int32_t N, in
   a.send_counts = send_counts;
   a.status = static_cast<int32_t*>(workspace);
   const int64_t blocks = a.routes > 0 ? (a.routes + 255) / 256 : 1;   // block 0 writes the counts
-  ep_send_pos_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  ep_send_pos_kernel<<<static_cast<unsigned>(blocks), kEpThreads, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -330,7 +428,7 @@ moe_status moe_ep_recv_rows(int32_t M, int32_t dst_rank, int32_t N, const int32_
   a.recv_row = recv_row;
   a.cap = recv_cap;
   a.status = static_cast<int32_t*>(workspace);
-  ep_recv_rows_kernel<<<static_cast<unsigned>(M) * static_cast<unsigned>(N), 256, 0, stream>>>(a);
+  ep_recv_rows_kernel<<<static_cast<unsigned>(M), kEpThreads, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
