@@ -24,15 +24,24 @@
 namespace moe {
 namespace {
 
+// Offsets of the segments padded to multiples of 64 rows: one warp, an exclusive prefix
+// sum 32 experts at a time.
 __global__ void pad_offsets_kernel(const int32_t* counts_keep, int N, int32_t* seg_pad) {
-  if (threadIdx.x == 0) {
-    int32_t o = 0;
-    for (int e = 0; e < N; ++e) {
-      seg_pad[e] = o;
-      o += (counts_keep[e] + 63) / 64 * 64;
+  const int lane = threadIdx.x;
+  int32_t run = 0;
+  for (int base = 0; base < N; base += 32) {
+    const int e = base + lane;
+    const int32_t v = e < N ? (counts_keep[e] + 63) / 64 * 64 : 0;
+    int32_t incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
     }
-    seg_pad[N] = o;
+    if (e < N) seg_pad[e] = run + incl - v;
+    run += __shfl_sync(0xffffffffu, incl, 31);
   }
+  if (lane == 0) seg_pad[N] = run;
 }
 
 // One warp per token: the row of x and the upstream gradient dy (as bf16, unscaled) are
