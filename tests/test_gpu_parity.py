@@ -161,6 +161,34 @@ def test_equal_logits_ties_and_dense_reduction():
     assert err <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("name", ["olmo_s", "dsv3_s"])
+def test_integer_logits_with_ties(name):
+    """x and W_router with entries in {-1, 0, 1}: every logit is an exact integer and many
+    experts of a token tie (logits of at most |d| in magnitude over 32 or 256 experts), on
+    the one-CTA router (32 experts) and the CTA-pair router (256).  The logits must be those
+    integers exactly, and the selection, counts and permutation bit-exact with ties taken by
+    the lower index; y within the bar."""
+    spec = SMALL[name]
+    g = torch.Generator(device="cpu").manual_seed(5)
+    x = torch.randint(-1, 2, (spec.T, spec.d_model), generator=g).to(torch.bfloat16).cuda()
+    wr = torch.randint(-1, 2, (spec.N, spec.d_model), generator=g).to(torch.bfloat16).cuda()
+    spec, inp = _spec_and_inputs(name, x=x, W_router=wr)
+    layer = run_layer(spec, inp)
+    assert layer.status() == 0
+    hin = host(inp)
+    z_exact = hin["x"].double().numpy() @ hin["W_router"].double().numpy().T
+    z_dev = layer.out["logits"].cpu().double().numpy()
+    np.testing.assert_array_equal(z_dev, z_exact)
+    # ties among the selected: some token's K-th and (K+1)-th largest logits are equal
+    zs = -np.sort(-z_exact, axis=1)
+    assert (zs[:, spec.K - 1] == zs[:, spec.K]).any()
+    rt = check_routing_exact(layer, spec)
+    y_ref, _ = oracle_y(spec, hin, rt, np.arange(spec.T))
+    err = layer_error(spec, layer.out["y"].cpu().double().numpy(), y_ref, rt.route_pos)
+    record_error(f"{name} integer logits with ties", err, TOL["bf16"])
+    assert err <= TOL["bf16"]
+
+
 def test_empty_batch():
     import routing_shared_expert_gb300 as moe
     spec = SMALL["olmo_s"].replace(T=0)
