@@ -104,8 +104,12 @@ struct Tile {
   bool half;   // at most BM real rows: an M = 128 tile
 };
 
+// Tile t of a launch: groups in order; within a group, by default the row tiles of one
+// output-column block together (the tiles that read one weight slice run at once), or with
+// rows_first the column blocks of one row tile together (dense launches: a block of rows is
+// read once while the whole weight matrix, reused by every row tile, stays in L2).
 __device__ __forceinline__ bool pair_tile(const int* s_tp, const int* s_off, int G, int n_tiles,
-                                          int64_t t, Tile& o) {
+                                          int64_t t, Tile& o, bool rows_first = false) {
   if (t >= static_cast<int64_t>(s_tp[G]) * n_tiles) return false;
   int lo = 0, hi = G;   // s_tp[lo] * n_tiles <= t < s_tp[hi] * n_tiles
   while (hi - lo > 1) {
@@ -115,8 +119,8 @@ __device__ __forceinline__ bool pair_tile(const int* s_tp, const int* s_off, int
   const int mt = s_tp[lo + 1] - s_tp[lo];
   const int64_t local = t - static_cast<int64_t>(s_tp[lo]) * n_tiles;
   o.g = lo;
-  o.n = static_cast<int>(local / mt);
-  o.m = static_cast<int>(local % mt);
+  o.n = static_cast<int>(rows_first ? local % n_tiles : local / mt);
+  o.m = static_cast<int>(rows_first ? local / n_tiles : local % mt);
   o.seg_start = s_off[lo];
   o.seg_end = s_off[lo + 1];
   o.half = o.seg_end - (o.seg_start + o.m * PM) <= BM;
@@ -182,6 +186,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? GATHER_THRE
   constexpr int stage_bytes = KSUB * SUB_BYTES;
   const uint32_t smem_base = smem_u32(smem);
   const int64_t pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+  const bool dense_rows_first = args.offsets == nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < RING_BLOCKS; ++s) {
@@ -262,7 +267,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? GATHER_THRE
     // Lane 0 alone: wait for a free stage, arm the even CTA's barrier, load A (unless the
     // gatherer warps copy it) and B.
     if (lane == 0) {
-      for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl); t += n_pairs) {
+      for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl, dense_rows_first); t += n_pairs) {
         int a_row = tl.seg_start + tl.m * PM + static_cast<int>(rank) * (tl.half ? HM : BM);
         // A CTA whose A rows all lie past the segment (the odd CTA of a half tile over a tail
         // of at most 64 rows) loads its box from past the last row of the buffer instead:
@@ -316,7 +321,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? GATHER_THRE
       bool ok = true;
       Tile tl;
       int64_t local = 0;
-      for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl);
+      for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl, dense_rows_first);
            t += n_pairs, ++local) {
         const int buf = static_cast<int>(local & 1);
         const uint32_t use = static_cast<uint32_t>(local >> 1);
@@ -374,7 +379,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? GATHER_THRE
     }
     Tile tl;
     int64_t local = 0;
-    for (int64_t t = pair_id; pair_tile(s_tp, s_off, G, n_tiles, t, tl); t += n_pairs, ++local) {
+    for (int64_t t = pair_id; pair_tile(s_tp, s_off, G, n_tiles, t, tl, dense_rows_first); t += n_pairs, ++local) {
       const int buf = static_cast<int>(local & 1);
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       bool ready = true;
@@ -551,7 +556,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GATHER ? GATHER_THRE
     int64_t j0 = 0;   // ring stages of the tiles before this one
     bool ok = true;
     Tile tl;
-    for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl);
+    for (int64_t t = pair_id; ok && pair_tile(s_tp, s_off, G, n_tiles, t, tl, dense_rows_first);
          t += n_pairs, j0 += stages_per_tile) {
       // this warp's first stage of the tile: the first j >= j0 with j mod stages == my_slot
       int q = static_cast<int>((my_slot - j0 % stages + stages) % stages);
