@@ -75,6 +75,12 @@ struct BwdTile {
   int seg_start, seg_end;   // padded segment rows of group g
 };
 
+// Tile t of a launch.  Within a group the tiles of one output-column block run together
+// (the operand block they share is read once while the other streams), except in dense
+// launches (one group, no segments: the shared expert's and the router's GEMMs) whose row
+// operand is the larger one: there the column blocks of one row block run together, so the
+// rows are read once while the smaller column operand, reused by every row block, stays in
+// L2.
 __device__ __forceinline__ bool bwd_tile(const BwdGemmArgs& a, bool k_seg, const int* s_off,
                                          const int* s_tp, int n_tiles, int64_t t, BwdTile& o) {
   const int G = a.seg_off ? a.groups : 1;
@@ -84,8 +90,9 @@ __device__ __forceinline__ bool bwd_tile(const BwdGemmArgs& a, bool k_seg, const
     if (t >= per * G) return false;
     o.g = static_cast<int>(t / per);
     const int64_t local = t - static_cast<int64_t>(o.g) * per;
-    o.n = static_cast<int>(local / mt);
-    o.m = static_cast<int>(local % mt);
+    const bool rows_first = a.seg_off == nullptr && a.m_dim > a.n_dim;
+    o.n = static_cast<int>(rows_first ? local % n_tiles : local / mt);
+    o.m = static_cast<int>(rows_first ? local / n_tiles : local % mt);
   } else {
     if (t >= static_cast<int64_t>(s_tp[G]) * n_tiles) return false;
     int lo = 0, hi = G;   // s_tp[lo] * n_tiles <= t < s_tp[hi] * n_tiles
@@ -96,8 +103,9 @@ __device__ __forceinline__ bool bwd_tile(const BwdGemmArgs& a, bool k_seg, const
     const int mt = s_tp[lo + 1] - s_tp[lo];
     const int64_t local = t - static_cast<int64_t>(s_tp[lo]) * n_tiles;
     o.g = lo;
-    o.n = static_cast<int>(local / mt);
-    o.m = static_cast<int>(local % mt);
+    const bool rows_first = a.seg_off == nullptr && a.dense_rows > a.n_dim;
+    o.n = static_cast<int>(rows_first ? local % n_tiles : local / mt);
+    o.m = static_cast<int>(rows_first ? local / n_tiles : local % mt);
   }
   o.seg_start = s_off[o.g];
   o.seg_end = s_off[o.g + 1];
