@@ -212,19 +212,21 @@ def oracle_inputs(inp_host: dict) -> dict:
 
 def oracle_seconds(spec, inp_host, S: int) -> float:
     """Wall time of the oracle's full layer forward on the first S tokens, its weights
-    already converted where they fit the cache (the run is repeated, at most twice more,
-    while it converted any); ``oracle_seconds.converted`` holds the last run's conversions."""
+    already converted where they fit the cache: the run is repeated, at most twice more,
+    while it converted weights that the cache kept (conversions past the cache's cap recur
+    on every run, so a repeat would not remove them); ``oracle_seconds.converted`` holds the
+    last run's conversions."""
     sub = spec.replace(T=S)
     d = dict(inp_host)
     d["x"] = inp_host["x"][:S]
     import oracle as O
     for _ in range(3):
-        c0 = ExpertsF64.conversions
+        c0, h0 = ExpertsF64.conversions, ExpertsF64.held
         t0 = time.perf_counter()
         O.moe_forward(sub, d)
         t = time.perf_counter() - t0
         oracle_seconds.converted = ExpertsF64.conversions - c0
-        if oracle_seconds.converted == 0:
+        if oracle_seconds.converted == 0 or ExpertsF64.held == h0:
             break
     return t
 
@@ -232,13 +234,18 @@ def oracle_seconds(spec, inp_host, S: int) -> float:
 oracle_seconds.converted = 0
 
 
-def time_oracle(spec, inp_host, budget_s: float, min_tokens: int = 64):
-    """Run the oracle on the first S tokens of the workload; S sized for ~budget_s seconds."""
+def time_oracle(spec, inp_host, budget_s: float, min_tokens: int = 64, max_sizes: int = 5):
+    """Run the oracle on the first S tokens of the workload, S grown (at least doubling, aimed
+    at budget_s) until one run takes three quarters of budget_s or covers every token, trying
+    at most ``max_sizes`` sizes.  The run time need not grow in proportion to S: a few tokens
+    already touch most experts, whose weights the oracle converts to float64."""
     S = min(min_tokens, spec.T)
     t = oracle_seconds(spec, inp_host, S)
-    while t < budget_s / 4 and S < spec.T:
-        S = min(spec.T, max(S * 2, int(S * budget_s / max(t, 1e-3) / 2)))
+    sizes = 1
+    while t < 0.75 * budget_s and S < spec.T and sizes < max_sizes:
+        S = min(spec.T, max(S * 2, int(S * budget_s / max(t, 1e-3))))
         t = oracle_seconds(spec, inp_host, S)
+        sizes += 1
     return S, t
 
 
