@@ -21,21 +21,6 @@ namespace {
 template <typename T>
 struct Vec;
 template <>
-struct Vec<__nv_bfloat16> {
-  static constexpr int N = 8;
-  __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-      const float2 f = __bfloat1622float2(b);
-      v[2 * i] = f.x;
-      v[2 * i + 1] = f.y;
-    }
-  }
-};
-template <>
 struct Vec<__half> {
   static constexpr int N = 8;
   __device__ static void load(const __half* p, float (&v)[8]) {
