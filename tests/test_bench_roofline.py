@@ -57,3 +57,23 @@ def test_layer_roof_is_hbm_below_the_ridge_and_tensor_above():
     r = b.layer_roofline(olmo, olmo.T * olmo.K, 1.0, PK)
     assert r["bound"] == "tensor" and r["roof_tflops"] == PK["bf16_tflops"]
     assert r["frac"] == pytest.approx(olmo.expert_flops(olmo.T * olmo.K) / 1e-3 / 1e12 / PK["bf16_tflops"])
+
+
+def test_stage_traffic_is_reported_only_for_the_captured_sources(monkeypatch):
+    """The ncu traffic figure comes with the hash of the kernel sources it was captured on:
+    the bench reports it while the sources hash to that value and null otherwise (a changed
+    kernel has not been measured), and null for a workload without a capture."""
+    import hashlib
+    import os
+    bench = _bench()
+    h = hashlib.sha256()
+    for f in bench.TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    current = h.hexdigest()[:16]
+    monkeypatch.setattr(bench, "STAGE_TRAFFIC", {
+        "same": {"sources_sha256": current, "bytes": 123},
+        "changed": {"sources_sha256": "0" * 16 if current != "0" * 16 else "1" * 16, "bytes": 456}})
+    assert bench.stage_traffic("same") == 123
+    assert bench.stage_traffic("changed") is None
+    assert bench.stage_traffic("no capture") is None
